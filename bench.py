@@ -1,0 +1,441 @@
+#!/usr/bin/env python
+"""Throughput of the attention core (forward + backward) on one GB300.
+
+A step is one xt_attn_fwd + xt_attn_bwd (all kernels of the path) over one
+batch of synthetic inputs resident in HBM. Metric: causal GQA attention
+fwd+bwd TFLOP/s, FLOPs counted as 2*B*H*S^2*D forward and 2.5x that
+backward. The L2 is flushed (a 512 MB write) between timed steps, outside the
+per-step CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle timed on host cores
+
+Under torchrun (N > 1) every rank runs its own shard of independent batch
+units on its own GPU (weak scaling, no collective on the data path); rank 0
+prints one JSON line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal GQA attention fwd+bwd TFLOP/s at 1 GB300 and % of dense BF16 peak"
+UNIT = "TFLOP/s"
+DEFAULT_WORKLOAD = "qwen3_like_bf16"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(tflops=float(p["bf16_tflops"]), tflops_sustained=float(p["bf16_tflops_sustained"]),
+                    hbm_gbs=float(p["hbm_gbs"]), source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(tflops=1900.0, tflops_sustained=1700.0, hbm_gbs=6800.0, source="fallback")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id=None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd.insert(1, f"--id={self.gpu_id}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def gpu_pci_id(torch):
+    try:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ CPU oracle
+def oracle_sample(w, s_len, cores):
+    """A bounded sample of workload w for the CPU oracle: batch element 0, as
+    many kv groups as give one query head per core, sequence cut to s_len.
+    Returns (sub-workload, inputs as float64, description)."""
+    import numpy as np  # noqa: F401
+    from causal_gqa_attention_xt_gb300.inputs import make_inputs, to_f64
+    n_groups = max(1, min(w.G, cores // w.group))
+    sub = w.with_(B=1, S=s_len, H=n_groups * w.group, G=n_groups)
+    x = to_f64(make_inputs(sub))
+    desc = (f"B=1, S={s_len}, {sub.H} query heads / {sub.G} kv heads (group {w.group}), "
+            f"D={w.D}: oracle fwd + bwd, fp64, {min(cores, sub.H)} threads")
+    return sub, x, desc
+
+
+def run_oracle_step(sub, x, threads):
+    import oracle
+    oracle.attn_fwd(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], sub.eps, sub.theta,
+                    nthreads=threads)
+    oracle.attn_bwd(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"], sub.eps,
+                    sub.theta, nthreads=threads)
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, seconds_target=20.0):
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    sub, x, desc = oracle_sample(w, w.S, cores)
+    threads = min(cores, sub.H)
+    t0 = time.perf_counter()
+    run_oracle_step(sub, x, threads)
+    dt = time.perf_counter() - t0
+    flops = sub.fwd_flops + sub.bwd_flops
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": desc, "seconds": dt}
+
+
+def bench_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    s_len = min(w.S, args.ref_seq)
+    sub, x, desc = oracle_sample(w, s_len, cores)
+    threads = min(cores, sub.H)
+    for _ in range(args.warmup):
+        run_oracle_step(sub, x, threads)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_oracle_step(sub, x, threads)
+        times.append(time.perf_counter() - t0)
+    flops = sub.fwd_flops + sub.bwd_flops
+    value = flops * len(times) / sum(times) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G,
+                   "head_dim": w.D, "theta": w.theta, "eps": w.eps, "sample_per_step": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def bench_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from causal_gqa_attention_xt_gb300 import build as xbuild
+    from causal_gqa_attention_xt_gb300 import xt
+    from causal_gqa_attention_xt_gb300.inputs import make_inputs
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    xbuild.build()
+    xt.lib()
+
+    # each rank owns its own shard of batch units (weak scaling)
+    wr = w.with_(seed=w.seed + rank)
+    cpu = make_inputs(wr)
+    d = {k: v.to(dev) for k, v in cpu.items()}
+    saved = xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta)
+    grads = xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
+                           w.eps, w.theta)
+    ws = torch.empty(xt.xt_attn_workspace_bytes(w.B, w.S, w.H, w.G, w.D, w.dtype == "bf16" and 1 or 0, True),
+                     device=dev, dtype=torch.uint8)
+    flush = torch.empty(512 * 1024 * 1024, device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
+                       out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
+                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"])
+        xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
+                       w.eps, w.theta, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
+                       dgamma_q=grads["dgamma_q"], dgamma_k=grads["dgamma_k"], workspace=ws)
+
+    def fwd_only():
+        xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
+                       out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
+                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"])
+
+    def bwd_only():
+        xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
+                       w.eps, w.theta, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
+                       dgamma_q=grads["dgamma_q"], dgamma_k=grads["dgamma_k"], workspace=ws)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if xt.xt_attn_check() != xt.XT_OK:
+        raise RuntimeError("device error flag raised during warm-up")
+
+    # ---- timed region: K steps, events per step, L2 flushed between steps
+    clocks = ClockSampler(gpu_pci_id(torch))
+    clocks.start()
+    time.sleep(0.4)
+    xt.xt_timing_reset()
+    xt.xt_timing_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fwd_only()
+        ev[i][1].record(stream)
+        bwd_only()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    xt.xt_timing_enable(False)
+    per_kernel = xt.xt_timing_query()
+    clk = clocks.stop()
+    if xt.xt_attn_check() != xt.XT_OK:
+        raise RuntimeError("device error flag raised during the timed steps")
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    step_ms_local = sum(fwd_ms + bwd_ms) / args.steps
+    fwd_ms_local = sum(fwd_ms) / args.steps
+    bwd_ms_local = sum(bwd_ms) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms_local, fwd_ms_local, bwd_ms_local], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, fwd_ms_m, bwd_ms_m = t.tolist()
+    else:
+        step_ms, fwd_ms_m, bwd_ms_m = step_ms_local, fwd_ms_local, bwd_ms_local
+
+    # ---- end to end through the public API: pinned host buffers in and out
+    pin = {k: v.pin_memory() for k, v in cpu.items()}
+    outs_host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+                 for k, v in [("out", saved["out"]), ("dq", grads["dq"]), ("dk", grads["dk"]),
+                              ("dv", grads["dv"]), ("dgamma_q", grads["dgamma_q"]),
+                              ("dgamma_k", grads["dgamma_k"])]}
+    src = {"out": saved["out"], "dq": grads["dq"], "dk": grads["dk"], "dv": grads["dv"],
+           "dgamma_q": grads["dgamma_q"], "dgamma_k": grads["dgamma_k"]}
+    h2d = sum(v.numel() * v.element_size() for v in pin.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+
+    def e2e_step():
+        for k_, v_ in pin.items():
+            d[k_].copy_(v_, non_blocking=True)
+        step()
+        for k_, v_ in outs_host.items():
+            v_.copy_(src[k_], non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+
+    flops_step = w.fwd_flops + w.bwd_flops
+    value = world * flops_step / (step_ms * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # ---- roofline of the dominant kernel (largest share of the timed region)
+    fwd_f, D = w.fwd_flops, w.D
+    algo_flops = {  # algorithmic FLOPs per launch
+        "fwd_tcgen05_bf16": fwd_f, "fwd_simt_f32": fwd_f,
+        "bwd_dkdv_tcgen05_bf16": 2.0 * fwd_f, "bwd_dkdv_simt_f32": 2.0 * fwd_f,
+        "bwd_dq_tcgen05_bf16": 0.5 * fwd_f, "bwd_dq_simt_f32": 0.5 * fwd_f,
+    }
+    top = max(per_kernel.items(), key=lambda kv: kv[1][0]) if per_kernel else None
+    roofline = None
+    if top is not None:
+        name, (tot_ms, n) = top
+        avg_s = tot_ms / n * 1e-3
+        esz = 2 if w.dtype == "bf16" else 4
+        if name in algo_flops:
+            ach = algo_flops[name] / avg_s / 1e12
+            roofline = {"kernel": name, "bound": "tensor", "achieved": ach,
+                        "peak": peaks["tflops"], "unit": "TFLOP/s", "frac": ach / peaks["tflops"],
+                        "peak_source": f"{peaks['source']} bf16 burst",
+                        "frac_of_sustained": ach / peaks["tflops_sustained"],
+                        "traffic": None, "avg_launch_ms": tot_ms / n}
+        else:
+            rows_q, rows_k = w.B * w.S * w.H, w.B * w.S * w.G
+            algo_bytes = {
+                "prologue_qknorm_rope": 2 * esz * D * (rows_q + rows_k) + 4 * (rows_q + rows_k),
+                "bwd_epilogue_rope_norm": (4 + 2 * esz) * D * (rows_q + rows_k) + 4 * (rows_q + rows_k),
+                "bwd_pre_dlt": 2 * esz * D * rows_q + 4 * rows_q,
+            }.get(name, 0)
+            ach = algo_bytes / avg_s / 1e9
+            roofline = {"kernel": name, "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                        "peak_source": f"{peaks['source']} copy", "traffic": None,
+                        "avg_launch_ms": tot_ms / n}
+    traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+    if roofline is not None and os.path.exists(traffic_file):
+        try:
+            with open(traffic_file) as f:
+                tr = json.load(f)
+            ent = tr.get(roofline["kernel"], {})
+            if ent.get("workload") == w.name and ent.get("source_hash") == source_hash():
+                roofline["traffic"] = ent.get("bytes_per_launch")
+        except (OSError, ValueError):
+            pass
+
+    launches = sum(n for _, n in per_kernel.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G,
+                   "head_dim": w.D, "theta": w.theta, "eps": w.eps, "per_rank_batch": w.B,
+                   "l2": "flushed between timed steps (512 MB write, outside the step events)",
+                   "inputs": "N(0,1) q/k/v/dout rounded to bf16, gammas 1+0.1*N(0,1) fp32, seed 0+rank"},
+        "fwd": {"ms": fwd_ms_m, "tflops": w.fwd_flops / (fwd_ms_m * 1e-3) / 1e12,
+                "frac_of_peak": w.fwd_flops / (fwd_ms_m * 1e-3) / 1e12 / peaks["tflops"]},
+        "bwd": {"ms": bwd_ms_m, "tflops": w.bwd_flops / (bwd_ms_m * 1e-3) / 1e12,
+                "frac_of_peak": w.bwd_flops / (bwd_ms_m * 1e-3) / 1e12 / peaks["tflops"]},
+        "frac_of_peak": value / world / peaks["tflops"],
+        "roofline": roofline,
+        "kernels": {k: {"total_ms": v[0], "launches": v[1], "share": v[0] / max(1e-9, sum(x[0] for x in per_kernel.values()))}
+                    for k, v in per_kernel.items()},
+        "e2e": {"value": world * flops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def source_hash() -> str:
+    """Hash of the CUDA sources, to tie stored ncu traffic to the kernels it measured."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "causal_gqa_attention_xt_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seq", type=int, default=1024,
+                    help="sequence length of the oracle's per-step sample (reference arm)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from causal_gqa_attention_xt_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return bench_reference(args, w)
+    return bench_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,279 @@
+// xt_api.cu -- the C ABI declared in include/xt_attn.h: host-side argument
+// validation, workspace layout, kernel dispatch and per-launch timing.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/xt_attn.h"
+#include "xt_internal.h"
+
+namespace xt {
+
+// Device error word raised by kernels whose bounded barrier waits run out.
+__device__ unsigned int g_error_word;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = (int)e;
+    return XT_ECUDA;
+}
+
+// ---------------------------------------------------------------- timing
+struct PendingTiming {
+    int kid;
+    cudaEvent_t start, stop;
+};
+
+struct Timing {
+    std::mutex mu;
+    bool on = false;
+    std::vector<PendingTiming> pending;
+    std::vector<std::pair<cudaEvent_t, cudaEvent_t>> free_pairs;
+    double total_ms[KID_COUNT] = {};
+    long launches[KID_COUNT] = {};
+} g_timing;
+
+const char *kKernelNames[KID_COUNT] = {
+    "prologue_qknorm_rope", "fwd_simt_f32", "fwd_tcgen05_bf16", "bwd_pre_dlt",
+    "bwd_dq_simt_f32",      "bwd_dkdv_simt_f32", "bwd_dq_tcgen05_bf16",
+    "bwd_dkdv_tcgen05_bf16", "bwd_epilogue_rope_norm", "bwd_dgamma_reduce"};
+
+void drain_locked() {
+    for (auto &p : g_timing.pending) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(p.stop) == cudaSuccess &&
+            cudaEventElapsedTime(&ms, p.start, p.stop) == cudaSuccess) {
+            g_timing.total_ms[p.kid] += ms;
+            g_timing.launches[p.kid] += 1;
+        }
+        g_timing.free_pairs.push_back({p.start, p.stop});
+    }
+    g_timing.pending.clear();
+}
+
+// Runs one launcher; when timing is on, brackets it with events on `st`.
+template <typename F>
+int timed_launch(int kid, cudaStream_t st, F &&launch) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    bool on;
+    {
+        std::lock_guard<std::mutex> lk(g_timing.mu);
+        on = g_timing.on;
+        if (on) {
+            if (!g_timing.free_pairs.empty()) {
+                a = g_timing.free_pairs.back().first;
+                b = g_timing.free_pairs.back().second;
+                g_timing.free_pairs.pop_back();
+            } else {
+                if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess)
+                    return cuda_fail(cudaGetLastError());
+            }
+        }
+    }
+    if (on && cudaEventRecord(a, st) != cudaSuccess) return cuda_fail(cudaGetLastError());
+    cudaError_t e = launch();
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (on) {
+        if (cudaEventRecord(b, st) != cudaSuccess) return cuda_fail(cudaGetLastError());
+        std::lock_guard<std::mutex> lk(g_timing.mu);
+        g_timing.pending.push_back({kid, a, b});
+    }
+    return XT_OK;
+}
+
+// ---------------------------------------------------------------- validation
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate_shape(int B, int S, int H, int G, int D, int dtype) {
+    if (B <= 0 || S <= 0 || H <= 0 || G <= 0 || D <= 0) return XT_EINVAL;
+    if (H % G != 0) return XT_EINVAL;
+    if (D % 2 != 0) return XT_EINVAL;
+    if (dtype != XT_F32 && dtype != XT_BF16) return XT_EINVAL;
+    const double big = (double)B * (double)S * (double)H * (double)D;
+    if (big >= 2147483648.0) return XT_EINVAL;
+    if (dtype == XT_BF16 && D != 64 && D != 128) return XT_EUNSUPPORTED;
+    if (dtype == XT_F32 && (D % 8 != 0 || D > 128)) return XT_EUNSUPPORTED;
+    return XT_OK;
+}
+
+int validate_scalars(double eps, double theta) {
+    if (!(eps >= 0.0) || !isfinite(eps)) return XT_EINVAL;
+    if (!(theta > 0.0) || !isfinite(theta)) return XT_EINVAL;
+    return XT_OK;
+}
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct BwdWorkspace {
+    size_t off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, total;
+    int nparts;
+};
+
+BwdWorkspace bwd_layout(const Problem &p) {
+    BwdWorkspace w;
+    size_t o = 0;
+    w.off_dlt = o;    o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S);
+    w.off_dqhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S * p.D);
+    w.off_dkhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.G * p.S * p.D);
+    w.nparts = normrope_blocks(p);
+    w.off_part_q = o; o = align_up(o + sizeof(float) * (size_t)w.nparts * p.D);
+    w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)w.nparts * p.D);
+    w.total = o;
+    return w;
+}
+
+Problem make_problem(int B, int S, int H, int G, int D, double eps, double theta, int dtype) {
+    Problem p;
+    p.B = B; p.S = S; p.H = H; p.G = G; p.D = D;
+    p.eps = (float)eps; p.theta = theta; p.dtype = dtype;
+    return p;
+}
+
+}  // namespace
+}  // namespace xt
+
+using namespace xt;
+
+extern "C" {
+
+size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                               int dtype, int backward) {
+    if (validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
+    if (!backward) return 0;
+    return bwd_layout(make_problem(B, S, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype)).total;
+}
+
+int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
+                double theta, const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype, void *out, float *lse,
+                void *q_hat, void *k_hat, float *rstd_q, float *rstd_k, void *workspace,
+                size_t workspace_bytes, void *stream) {
+    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    const void *ptrs[] = {q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k};
+    for (const void *ptr : ptrs)
+        if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
+    (void)workspace; (void)workspace_bytes;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    cudaStream_t s = (cudaStream_t)stream;
+    st = timed_launch(KID_PROLOGUE, s, [&] {
+        return launch_prologue(p, q, k, gamma_q, gamma_k, q_hat, k_hat, rstd_q, rstd_k, s);
+    });
+    if (st != XT_OK) return st;
+    return timed_launch(KID_FWD_SIMT, s, [&] {
+        return launch_fwd_simt(p, q_hat, k_hat, v, out, lse, s);
+    });
+}
+
+int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
+                double theta, const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype, const void *out,
+                const float *lse, const void *q_hat, const void *k_hat, const float *rstd_q,
+                const float *rstd_k, const void *dout, void *dq, void *dk, void *dv,
+                float *dgamma_q, float *dgamma_k, void *workspace, size_t workspace_bytes,
+                void *stream) {
+    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    const void *ptrs[] = {q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k,
+                          dout, dq, dk, dv, dgamma_q, dgamma_k};
+    for (const void *ptr : ptrs)
+        if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    const BwdWorkspace w = bwd_layout(p);
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < w.total)
+        return XT_EWORKSPACE;
+    char *ws = (char *)workspace;
+    float *dlt = (float *)(ws + w.off_dlt);
+    float *dqhat = (float *)(ws + w.off_dqhat);
+    float *dkhat = (float *)(ws + w.off_dkhat);
+    float *part_q = (float *)(ws + w.off_part_q);
+    float *part_k = (float *)(ws + w.off_part_k);
+    cudaStream_t s = (cudaStream_t)stream;
+
+    st = timed_launch(KID_BWD_PRE, s, [&] { return launch_bwd_pre(p, out, dout, dlt, s); });
+    if (st != XT_OK) return st;
+    st = timed_launch(KID_BWD_DKDV_SIMT, s, [&] {
+        return launch_bwd_dkdv_simt(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, s);
+    });
+    if (st != XT_OK) return st;
+    st = timed_launch(KID_BWD_DQ_SIMT, s, [&] {
+        return launch_bwd_dq_simt(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, s);
+    });
+    if (st != XT_OK) return st;
+    st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
+        return launch_epilogue(p, dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q, rstd_k, dq, dk,
+                               part_q, part_k, s);
+    });
+    if (st != XT_OK) return st;
+    return timed_launch(KID_DGAMMA_REDUCE, s, [&] {
+        return launch_dgamma_reduce(p, part_q, part_k, w.nparts, dgamma_q, dgamma_k, s);
+    });
+}
+
+int xt_attn_check(void *stream) {
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int word = 0;
+    e = cudaMemcpyFromSymbol(&word, g_error_word, sizeof(word));
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (word != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+        if (e != cudaSuccess) return cuda_fail(e);
+        return XT_ETIMEOUT;
+    }
+    return XT_OK;
+}
+
+const char *xt_status_str(int status) {
+    switch (status) {
+        case XT_OK: return "ok";
+        case XT_EINVAL: return "invalid argument";
+        case XT_EUNSUPPORTED: return "unsupported dtype/head_dim combination";
+        case XT_ECUDA: return "CUDA error";
+        case XT_EWORKSPACE: return "workspace missing or too small";
+        case XT_ETIMEOUT: return "a kernel timed out waiting on a barrier";
+        default: return "unknown status";
+    }
+}
+
+int xt_last_cuda_error(void) { return g_last_cuda_error; }
+
+int xt_timing_enable(int on) {
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    g_timing.on = on != 0;
+    return XT_OK;
+}
+
+int xt_timing_reset(void) {
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    drain_locked();
+    for (int i = 0; i < KID_COUNT; ++i) { g_timing.total_ms[i] = 0.0; g_timing.launches[i] = 0; }
+    return XT_OK;
+}
+
+int xt_timing_query(int kernel_id, double *total_ms, long *launches) {
+    if (kernel_id < 0 || kernel_id >= KID_COUNT || !total_ms || !launches) return XT_EINVAL;
+    std::lock_guard<std::mutex> lk(g_timing.mu);
+    drain_locked();
+    *total_ms = g_timing.total_ms[kernel_id];
+    *launches = g_timing.launches[kernel_id];
+    return XT_OK;
+}
+
+int xt_kernel_count(void) { return KID_COUNT; }
+
+const char *xt_kernel_name(int kernel_id) {
+    if (kernel_id < 0 || kernel_id >= KID_COUNT) return "";
+    return kKernelNames[kernel_id];
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// xt_common.cuh -- small device helpers shared by the kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace xt {
+
+typedef __nv_bfloat16 bf16;
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(bf16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float x) { return __float2bfloat16_rn(x); }
+
+// 16-byte vector of T: 4 floats or 8 bf16.
+template <typename T> struct Vec16 {
+    static constexpr int N = 16 / sizeof(T);
+    uint4 raw;
+};
+
+template <typename T>
+__device__ __forceinline__ void load16(const T *p, float *dst) {
+    uint4 r = *reinterpret_cast<const uint4 *>(p);
+    if constexpr (sizeof(T) == 4) {
+        dst[0] = __uint_as_float(r.x); dst[1] = __uint_as_float(r.y);
+        dst[2] = __uint_as_float(r.z); dst[3] = __uint_as_float(r.w);
+    } else {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            dst[2 * i] = __uint_as_float(w[i] << 16);
+            dst[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ void store16(T *p, const float *src) {
+    uint4 r;
+    if constexpr (sizeof(T) == 4) {
+        r.x = __float_as_uint(src[0]); r.y = __float_as_uint(src[1]);
+        r.z = __float_as_uint(src[2]); r.w = __float_as_uint(src[3]);
+    } else {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(src[2 * i], src[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        r.x = w[0]; r.y = w[1]; r.z = w[2]; r.w = w[3];
+    }
+    *reinterpret_cast<uint4 *>(p) = r;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Sum over an aligned group of `width` lanes (width a power of two <= 32).
+__device__ __forceinline__ float group_sum(float v, int width) {
+    for (int o = width >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+}  // namespace xt

@@ -1,0 +1,66 @@
+// xt_internal.h -- declarations shared by the library's translation units.
+// Host-side launchers return cudaError_t; the C ABI in xt_api.cu validates
+// arguments, lays out the workspace and times launches.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace xt {
+
+// Kernel ids for the per-launch timing hooks (xt_timing_*).
+enum KernelId {
+    KID_PROLOGUE = 0,     // QK-RMSNorm + RoPE of Q and K
+    KID_FWD_SIMT,         // fp32 CUDA-core flash forward
+    KID_FWD_TC,           // bf16 tcgen05 flash forward
+    KID_BWD_PRE,          // Dlt = rowsum(dO * O)
+    KID_BWD_DQ_SIMT,      // fp32 CUDA-core dQhat
+    KID_BWD_DKDV_SIMT,    // fp32 CUDA-core dKhat, dV (group sum in-block)
+    KID_BWD_DQ_TC,        // bf16 tcgen05 dQhat
+    KID_BWD_DKDV_TC,      // bf16 tcgen05 dKhat, dV (group sum in-block)
+    KID_BWD_EPILOGUE,     // RoPE^-1 + RMSNorm backward, dgamma partials
+    KID_DGAMMA_REDUCE,    // fixed-order sum of dgamma partials
+    KID_COUNT
+};
+
+struct Problem {
+    int B, S, H, G, D;
+    float eps;
+    double theta;
+    int dtype;  // 0 = fp32, 1 = bf16
+    int group() const { return H / G; }
+};
+
+// Error word bits raised by kernels whose bounded waits run out.
+enum : unsigned int { ERR_TIMEOUT = 1u };
+
+// ---- norm / RoPE kernels (xt_normrope.cu) ----
+// Rows of positions handled by one prologue / epilogue block.
+constexpr int kRowsPerBlock = 16;
+inline int normrope_blocks(const Problem &p) {
+    return ((p.S + kRowsPerBlock - 1) / kRowsPerBlock) * p.B;
+}
+cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, const float *gq,
+                            const float *gk, void *qhat, void *khat, float *rstd_q,
+                            float *rstd_k, cudaStream_t st);
+cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, float *dlt,
+                           cudaStream_t st);
+cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *dkhat,
+                            const void *q, const void *k, const float *gq, const float *gk,
+                            const float *rstd_q, const float *rstd_k, void *dq, void *dk,
+                            float *part_q, float *part_k, cudaStream_t st);
+cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
+                                 int nparts, float *dgq, float *dgk, cudaStream_t st);
+
+// ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
+cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,
+                            void *out, float *lse, cudaStream_t st);
+cudaError_t launch_bwd_dq_simt(const Problem &p, const void *qhat, const void *khat,
+                               const void *v, const void *dout, const float *lse,
+                               const float *dlt, float *dqhat, cudaStream_t st);
+cudaError_t launch_bwd_dkdv_simt(const Problem &p, const void *qhat, const void *khat,
+                                 const void *v, const void *dout, const float *lse,
+                                 const float *dlt, float *dkhat, void *dv, cudaStream_t st);
+
+}  // namespace xt

@@ -1,0 +1,134 @@
+/*
+ * xt_attn.h -- C ABI of the GB300 (sm_103a) causal grouped-query attention
+ * core: per-head QK-RMSNorm, rotate_half RoPE and causal GQA scaled-dot-
+ * product attention, forward and backward.
+ *
+ * What the operation is (web pages, cited by title and section):
+ *  - xtrain "Phase T9: Export to xserv", architecture-diff table and
+ *    Decision 1: y = x * rsqrt(mean(x^2) + eps) * gamma over every
+ *    [head_dim] vector of Q and of K (one [head_dim] gamma per tensor, shared
+ *    by all heads), applied before rotate_half RoPE with
+ *    freq_i = theta^(-2i/head_dim) and position = token row; scores scaled
+ *    by 1/sqrt(head_dim); causal masking.
+ *  - Mint project report 5.4.1-5.4.2 (the rotation of the pair
+ *    (i, i + head_dim/2) by the angle pos * theta^(-2i/head_dim)), 5.3.1
+ *    (max-subtracted softmax and P V), 5.5.2 (RMSNorm backward).
+ *  - xtrain "Phase T5: Tiny Transformer", Key Design Decisions: additive
+ *    -1e9 mask above the diagonal (key j is visible to query t iff j <= t).
+ *  - xtrain "Phase T15: GQA", "What is GQA": query head qh reads key/value
+ *    head qh / (n_heads / n_kv_heads); Decision 2: the gradient of a shared
+ *    key/value head is the sum of its group's query-head gradients, formed
+ *    deterministically (no atomics).
+ *  - xtrain "Phase T12: bf16 mixed precision", precision table: bf16
+ *    activations in and out, fp32 accumulation, norm / softmax / RoPE in fp32.
+ *
+ * Layouts (all row-major and contiguous; B batch, S sequence, H = n_heads,
+ * G = n_kv_heads, D = head_dim):
+ *    q, out, dout, dq  [B, S, H, D]  element type `dtype`
+ *    k, v, dk, dv      [B, S, G, D]  element type `dtype`
+ *    q_hat             [B, H, S, D]  `dtype`  (Q after norm + RoPE)
+ *    k_hat             [B, G, S, D]  `dtype`  (K after norm + RoPE)
+ *    lse               [B, H, S]     fp32, natural-log log-sum-exp of the
+ *                                    scaled, masked scores of each query row
+ *    rstd_q / rstd_k   [B, S, H] / [B, S, G]  fp32, 1/sqrt(mean(x^2)+eps)
+ *    gamma_q, gamma_k, dgamma_q, dgamma_k   [D] fp32
+ *
+ * Ownership and execution: every pointer is a device allocation owned by the
+ * caller, 16-byte aligned. The library never allocates, frees or
+ * synchronizes; XT_OK means the work was enqueued on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream) and results are valid once
+ * that stream reaches the enqueued point. Scratch memory is the caller's
+ * `workspace`, sized by xt_attn_workspace_bytes(). dgamma_q and dgamma_k are
+ * overwritten, not accumulated. Forward and backward are deterministic:
+ * identical inputs give bitwise identical outputs.
+ *
+ * Supported shapes: B, S, H, G >= 1, H % G == 0; dtype XT_BF16 with
+ * head_dim 64 or 128 (tensor-core path), dtype XT_F32 with head_dim a
+ * multiple of 8 up to 128 (fp32 CUDA-core path). Every tensor must hold
+ * fewer than 2^31 elements.
+ *
+ * Errors: calls validate their arguments on the host before any launch and
+ * return an xt_status; no call aborts the process. XT_ECUDA reports a launch
+ * or CUDA API failure (xt_last_cuda_error() gives the cudaError_t); it is not
+ * cleared or hidden. Kernels that wait on barriers give up after a bounded
+ * number of polls and raise a device-side error word, which
+ * xt_attn_check() reads back (as XT_ETIMEOUT).
+ */
+#ifndef XT_ATTN_H
+#define XT_ATTN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { XT_F32 = 0, XT_BF16 = 1 } xt_dtype;
+
+typedef enum {
+    XT_OK = 0,
+    XT_EINVAL = 1,        /* bad size, null pointer, H % G != 0, bad eps/theta   */
+    XT_EUNSUPPORTED = 2,  /* valid but unsupported (dtype, head_dim) pair         */
+    XT_ECUDA = 3,         /* a CUDA call or kernel launch failed                  */
+    XT_EWORKSPACE = 4,    /* workspace pointer null or workspace_bytes too small  */
+    XT_ETIMEOUT = 5       /* a kernel gave up waiting on a barrier (device flag)  */
+} xt_status;
+
+/* Bytes of scratch the forward (backward = 0) or backward (backward != 0)
+ * call needs for this problem; 0 on invalid arguments or when none is
+ * needed. */
+size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                               int dtype, int backward);
+
+/* Forward: out = causal GQA SDPA(rope(norm(q)), rope(norm(k)), v) with scale
+ * 1/sqrt(head_dim). Also writes what the backward needs: lse, q_hat, k_hat,
+ * rstd_q, rstd_k. `eps` is the RMSNorm epsilon (added to mean(x^2) inside the
+ * square root), `theta` the RoPE base. */
+int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                double eps, double theta,
+                const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype,
+                void *out, float *lse, void *q_hat, void *k_hat,
+                float *rstd_q, float *rstd_k,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Backward for upstream gradient dout: writes dq, dk, dv (input layouts and
+ * dtype) and dgamma_q, dgamma_k (overwritten). q, k, v, gammas and the saved
+ * tensors are those of the matching xt_attn_fwd call. The gradient of each
+ * shared key/value head is the sum over its group's query heads, formed in a
+ * fixed order inside one thread block. */
+int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                double eps, double theta,
+                const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype,
+                const void *out, const float *lse, const void *q_hat, const void *k_hat,
+                const float *rstd_q, const float *rstd_k, const void *dout,
+                void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
+                void *workspace, size_t workspace_bytes, void *stream);
+
+/* Synchronizes `stream`, then reads and clears the device error word of the
+ * current device: XT_OK, XT_ETIMEOUT (a bounded wait ran out) or XT_ECUDA. */
+int xt_attn_check(void *stream);
+
+/* Human-readable name of an xt_status value (static storage). */
+const char *xt_status_str(int status);
+
+/* The cudaError_t behind the most recent XT_ECUDA on this thread (0 if none). */
+int xt_last_cuda_error(void);
+
+/* Per-kernel timing, for measurement: when enabled, every launch the library
+ * makes is bracketed by CUDA events recorded on the launch stream, and
+ * xt_timing_query() sums their elapsed times (it synchronizes on those
+ * events). Disabled by default; enabling costs two event records per launch.
+ * Kernel ids run from 0 to xt_kernel_count()-1. */
+int xt_timing_enable(int on);
+int xt_timing_reset(void);
+int xt_timing_query(int kernel_id, double *total_ms, long *launches);
+int xt_kernel_count(void);
+const char *xt_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XT_ATTN_H */

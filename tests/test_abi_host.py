@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, it
+exports every function include/xt_attn.h declares, and argument validation
+rejects bad calls before any CUDA work (faults are injected on the host)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from causal_gqa_attention_xt_gb300 import build as xbuild
+from causal_gqa_attention_xt_gb300 import xt
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    xbuild.build()
+    return xt.lib()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names.update(re.findall(r"\b(xt_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("xt_attn_fwd", "xt_attn_bwd", "xt_attn_workspace_bytes", "xt_status_str",
+              "xt_attn_check"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(6):
+        assert xt.xt_status_str(code) not in ("", "unknown status")
+    assert xt.xt_status_str(99) == "unknown status"
+
+
+def _fwd(L, B=1, S=16, H=2, G=2, D=16, eps=1e-5, theta=1e4, dtype=0, ptr=16):
+    p = ctypes.c_void_p(ptr)
+    return L.xt_attn_fwd(B, S, H, G, D, eps, theta, p, p, p, p, p, dtype, p, p, p, p, p, p,
+                         None, 0, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), xt.XT_EINVAL), (dict(S=-1), xt.XT_EINVAL), (dict(H=3, G=2), xt.XT_EINVAL),
+    (dict(D=15), xt.XT_EINVAL), (dict(dtype=7), xt.XT_EINVAL), (dict(eps=-1.0), xt.XT_EINVAL),
+    (dict(theta=0.0), xt.XT_EINVAL), (dict(eps=float("nan")), xt.XT_EINVAL),
+    (dict(ptr=0), xt.XT_EINVAL), (dict(ptr=8), xt.XT_EINVAL),
+    (dict(B=1 << 16, S=1 << 16, H=1, G=1, D=16), xt.XT_EINVAL),
+    (dict(D=32, dtype=1), xt.XT_EUNSUPPORTED), (dict(D=136), xt.XT_EUNSUPPORTED),
+    (dict(D=12), xt.XT_EUNSUPPORTED),
+])
+def test_forward_validation_rejects_before_launch(L, kw, code):
+    assert _fwd(L, **kw) == code
+
+
+def test_backward_validation_and_workspace(L):
+    p = ctypes.c_void_p(16)
+    need = xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, True)
+    assert need > 0 and need % 256 == 0
+    assert xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, False) == 0
+    assert xt.xt_attn_workspace_bytes(1, 16, 3, 2, 16, 0, True) == 0
+    args = [1, 16, 2, 2, 16, 1e-5, 1e4] + [p] * 5 + [0] + [p] * 7 + [p] * 5
+    assert L.xt_attn_bwd(*args, p, need - 1, None) == xt.XT_EWORKSPACE
+    assert L.xt_attn_bwd(*args, None, need, None) == xt.XT_EWORKSPACE
+    bad = list(args)
+    bad[2] = 3
+    assert L.xt_attn_bwd(*bad, p, need, None) == xt.XT_EINVAL
+
+
+def test_timing_hooks_without_launches(L):
+    xt.xt_timing_reset()
+    assert xt.xt_timing_query() == {}
+    assert L.xt_kernel_count() >= 5
