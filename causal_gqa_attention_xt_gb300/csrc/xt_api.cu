@@ -128,6 +128,21 @@ BwdWorkspace bwd_layout(const Problem &p) {
     return w;
 }
 
+unsigned int *error_word_ptr() {
+    // device address of g_error_word on the current device (cached per device)
+    static unsigned int *cache[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!cache[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return nullptr;
+        cache[dev] = (unsigned int *)ptr;
+    }
+    return cache[dev];
+}
+
 Problem make_problem(int B, int S, int H, int G, int D, double eps, double theta, int dtype) {
     Problem p;
     p.B = B; p.S = S; p.H = H; p.G = G; p.D = D;
@@ -167,6 +182,13 @@ int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
         return launch_prologue(p, q, k, gamma_q, gamma_k, q_hat, k_hat, rstd_q, rstd_k, s);
     });
     if (st != XT_OK) return st;
+    if (dtype == XT_BF16) {
+        unsigned int *err = error_word_ptr();
+        if (!err) return cuda_fail(cudaGetLastError());
+        return timed_launch(KID_FWD_TC, s, [&] {
+            return launch_fwd_tc(p, q_hat, k_hat, v, out, lse, err, s);
+        });
+    }
     return timed_launch(KID_FWD_SIMT, s, [&] {
         return launch_fwd_simt(p, q_hat, k_hat, v, out, lse, s);
     });

@@ -1,0 +1,355 @@
+// xt_fwd_tc.cu -- bf16 causal GQA flash forward on sm_103a tensor cores.
+//
+// Operation (web pages): xtrain "Phase T5: Tiny Transformer", multi-head
+// pipeline (per head: scores = q k^T / sqrt(hd) + causal mask, softmax,
+// P V); Mint project report 5.3.1 (max-subtracted softmax, a_t = sum_j
+// p_tj v_j); xtrain "Phase T15: GQA" (query head h reads kv head
+// h / group); xtrain "Phase T12: bf16 mixed precision" (bf16 operands, fp32
+// accumulation and softmax). Keys j > t are skipped; the pages' additive
+// -1e9 mask makes their probabilities exactly 0 in fp32 anyway.
+//
+// One CTA computes two consecutive 128-row query tiles (2p, 2p+1) of one
+// (batch, head), ping-ponging them so that the tensor core works on one tile
+// while the softmax warps work on the other:
+//   warps 0-3  softmax + epilogue of query tile 0 (thread = one query row)
+//   warps 4-7  softmax + epilogue of query tile 1
+//   warp  8    TMA producer: Q tiles once, then a ring of K/V tiles
+//   warp  9    TMEM allocator and MMA issuer (one thread)
+// TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// S_i = Q_i K^T is an SS MMA (both operands K-major, 128B swizzle); the
+// softmax warps overwrite the first 64 columns of S_i with P_i as packed
+// bf16, and O_i += P_i V is a TS MMA (A = P from TMEM, B = V MN-major).
+// Online softmax in the log2 domain with lazy rescaling: the running max
+// used for exp2 is only raised when a row's max grows by more than 8, so O
+// is rescaled in TMEM rarely; the final 1/l and lse use the same max.
+//
+// Every barrier wait is bounded (xt_tc.cuh); on a timeout the CTA raises the
+// library's error word, drains its own copies and MMAs, frees TMEM and exits.
+#include "xt_common.cuh"
+#include "xt_internal.h"
+#include "xt_tc.cuh"
+
+namespace xt {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128;         // query rows per tile
+constexpr int kBN = 128;         // key rows per tile
+constexpr int kThreadsFwd = 320;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int D> struct FwdCfg {
+    static constexpr int kChunks = D / 64;                 // 64-column swizzle atoms per row
+    static constexpr int kTileBytes = kChunks * 16384;     // one 128-row tile
+    static constexpr int kStages = (D == 128) ? 2 : 4;     // K/V ring depth
+    static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + 1024;
+};
+
+struct FwdBarriers {
+    uint64_t q_full;
+    uint64_t k_full[4], v_full[4], kv_empty[4];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__device__ __forceinline__ void raise_error(unsigned int *err, volatile int *abort_flag) {
+    atomicOr(err, ERR_TIMEOUT);
+    *abort_flag = 1;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreadsFwd, 1)
+k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
+         const __grid_constant__ CUtensorMap map_v, bf16 *__restrict__ out,
+         float *__restrict__ lse, int S, int H, int G, int n_pairs, unsigned int *err) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ FwdBarriers bars;
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sQ = smem;                           // 2 tiles
+    uint8_t *sKV = smem + 2 * C::kTileBytes;      // stage s: K at 2s, V at 2s+1
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int BH = gridDim.x / n_pairs;
+    const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);   // longest first
+    const int bh = blockIdx.x % BH;
+    const int b = bh / H, h = bh - b * H, g = h / (H / G);
+    const int n_qtiles = (S + kBM - 1) / kBM;
+    int n_kv[2];
+    for (int i = 0; i < 2; ++i) {
+        const int qt = 2 * pair + i;
+        n_kv[i] = qt < n_qtiles ? qt + 1 : 0;
+    }
+    const int n_iter = max(n_kv[0], n_kv[1]);
+    volatile int *abort_flag = &bars.abort_flag;
+
+    if (threadIdx.x == 0) {
+        bars.abort_flag = 0;
+        mbar_init(&bars.q_full, 1);
+        for (int s = 0; s < C::kStages; ++s) {
+            mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.v_full[s], 1);
+            mbar_init(&bars.kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.p_full[i], 128);
+            mbar_init(&bars.o_done[i], 1);
+        }
+        mbar_init(&bars.drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&map_q);
+            tma_prefetch_desc(&map_k);
+            tma_prefetch_desc(&map_v);
+            const int nq = (n_kv[1] > 0) ? 2 : 1;
+            mbar_expect_tx(&bars.q_full, nq * C::kTileBytes);
+            for (int i = 0; i < nq; ++i)
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sQ + i * C::kTileBytes + c * 16384, &map_q, &bars.q_full, c * 64,
+                                (2 * pair + i) * kBM, bh);
+            int issued = 0;
+            for (int j = 0; j < n_iter; ++j) {
+                const int st = j % C::kStages;
+                if (j >= C::kStages &&
+                    !mbar_wait(&bars.kv_empty[st], ((j / C::kStages) - 1) & 1, abort_flag)) {
+                    if (!*abort_flag) raise_error(err, abort_flag);
+                    break;
+                }
+                uint8_t *sK = sKV + (2 * st) * C::kTileBytes;
+                uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
+                mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_3d(sK + c * 16384, &map_k, &bars.k_full[st], c * 64, j * kBN,
+                                b * G + g);
+                mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sV + c * 16384, &map_v, &bars.v_full[st], c * 64, g, j * kBN, b);
+                issued = j + 1;
+            }
+            // Drain: every copy this CTA issued must land before it exits.
+            mbar_wait(&bars.q_full, 0, nullptr);
+            for (int j = max(0, issued - C::kStages); j < issued; ++j) {
+                const int st = j % C::kStages;
+                mbar_wait(&bars.k_full[st], (j / C::kStages) & 1, nullptr);
+                mbar_wait(&bars.v_full[st], (j / C::kStages) & 1, nullptr);
+            }
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
+            const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
+            const uint32_t tS[2] = {tmem, tmem + 128};
+            const uint32_t tO[2] = {tmem + 256, tmem + 384};
+            bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
+            for (int j = 0; ok && j < n_iter; ++j) {
+                const int st = j % C::kStages;
+                const uint32_t ph = (j / C::kStages) & 1;
+                const uint32_t sK = smem_u32(sKV + (2 * st) * C::kTileBytes);
+                const uint32_t sV = smem_u32(sKV + (2 * st + 1) * C::kTileBytes);
+                if (!(ok = mbar_wait(&bars.k_full[st], ph, abort_flag))) break;
+                for (int i = 0; i < 2 && ok; ++i) {
+                    if (j >= n_kv[i]) continue;
+                    // S_i is free once PV_{j-1,i} (which read P_i from it) completed
+                    if (j > 0 && !(ok = mbar_wait(&bars.o_done[i], (j - 1) & 1, abort_flag))) break;
+                    tc_fence_after();
+                    const uint32_t sQi = smem_u32(sQ + i * C::kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                        mma_ss(tS[i], smem_desc(sQi + off, 16, 1024, kSwizzle128B),
+                               smem_desc(sK + off, 16, 1024, kSwizzle128B), idesc_s, kk > 0);
+                    }
+                    mma_commit(&bars.s_full[i]);
+                }
+                if (!ok) break;
+                if (!(ok = mbar_wait(&bars.v_full[st], ph, abort_flag))) break;
+                for (int i = 0; i < 2 && ok; ++i) {
+                    if (j >= n_kv[i]) continue;
+                    if (!(ok = mbar_wait(&bars.p_full[i], j & 1, abort_flag))) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        mma_ts(tO[i], tS[i] + kk * 8,
+                               smem_desc(sV + kk * 2048, 16384, 1024, kSwizzle128B), idesc_o,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&bars.o_done[i]);
+                }
+                if (!ok) break;
+                mma_commit(&bars.kv_empty[st]);
+            }
+            if (!ok && !*abort_flag) raise_error(err, abort_flag);
+            // Drain: all MMAs issued by this thread complete before TMEM is freed.
+            mma_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int i = warp >> 2;                 // query tile of this warpgroup
+        const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter+32)
+        const int r = quarter * 32 + lane;       // row within the tile
+        const int t = (2 * pair + i) * kBM + r;  // query position
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const uint32_t tS = tmem + i * 128 + lane_off;
+        const uint32_t tO = tmem + 256 + i * 128 + lane_off;
+        const float sl2 = kLog2e * rsqrtf((float)D);
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        const int n = n_kv[i];
+        for (int j = 0; j < n; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[i], j & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32_sync(tS + c * 32, sr[c]);
+            const bool diag = (j == n - 1);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float x = __uint_as_float(sr[c][e]) * sl2;
+                    if (diag && (c * 32 + e) > r) x = -INFINITY;
+                    sr[c][e] = __float_as_uint(x);
+                    mx = fmaxf(mx, x);
+                }
+            const float m_new = fmaxf(m_used, mx);
+            const bool need = m_new - m_used > kRescaleThreshold;   // true on the first tile
+            float alpha = 1.f;
+            if (need) {
+                alpha = fast_exp2(m_used - m_new);
+                m_used = m_new;
+            }
+            // O rescale in TMEM (warp-uniform: tcgen05.ld/st are warp-collective)
+            if (j > 0 && __any_sync(0xffffffffu, need)) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (j - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32_sync(tO + c * 32, o);
+                }
+            }
+            float rowsum = 0.f;
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    const float p0 = fast_exp2(__uint_as_float(sr[c][e]) - m_used);
+                    const float p1 = fast_exp2(__uint_as_float(sr[c][e + 1]) - m_used);
+                    rowsum += p0 + p1;
+                    pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
+                }
+            tmem_st32_sync(tS, pk[0]);
+            tmem_st32_sync(tS + 32, pk[1]);
+            tc_fence_before();
+            mbar_arrive(&bars.p_full[i]);
+            l = l * alpha + rowsum;
+        }
+        if (ok && n > 0) {
+            // epilogue: O / l -> bf16 rows of out [B, S, H, D]; lse = (m + log2 l) ln 2
+            if (__all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (n - 1) & 1, abort_flag))) {
+                tc_fence_after();
+                const float inv_l = 1.0f / l;
+                bf16 *dst = out + (((size_t)b * S + t) * H + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32_sync(tO + c * 32, o);
+                    if (t < S) {
+#pragma unroll
+                        for (int q8 = 0; q8 < 4; ++q8) {
+                            uint4 v;
+                            v.x = pack_bf16x2(__uint_as_float(o[q8 * 8 + 0]) * inv_l, __uint_as_float(o[q8 * 8 + 1]) * inv_l);
+                            v.y = pack_bf16x2(__uint_as_float(o[q8 * 8 + 2]) * inv_l, __uint_as_float(o[q8 * 8 + 3]) * inv_l);
+                            v.z = pack_bf16x2(__uint_as_float(o[q8 * 8 + 4]) * inv_l, __uint_as_float(o[q8 * 8 + 5]) * inv_l);
+                            v.w = pack_bf16x2(__uint_as_float(o[q8 * 8 + 6]) * inv_l, __uint_as_float(o[q8 * 8 + 7]) * inv_l);
+                            *reinterpret_cast<uint4 *>(dst + c * 32 + q8 * 8) = v;
+                        }
+                    }
+                }
+                if (t < S) lse[(size_t)bh * S + t] = (m_used + __log2f(l)) * kLn2;
+            } else {
+                ok = false;
+            }
+        }
+        if (!ok && !*abort_flag) raise_error(err, abort_flag);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat, const void *v,
+                            void *out, float *lse, unsigned int *err, cudaStream_t st) {
+    using C = FwdCfg<D>;
+    CUtensorMap mq, mk, mv;
+    const uint64_t esz = 2;
+    {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.H};
+        const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
+        const uint32_t box[3] = {64, kBM, 1};
+        cudaError_t e = encode_tmap_bf16(&mq, qhat, 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.G};
+        const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
+        const uint32_t box[3] = {64, kBN, 1};
+        cudaError_t e = encode_tmap_bf16(&mk, khat, 3, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    {
+        const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)p.S, (uint64_t)p.B};
+        const uint64_t strides[3] = {D * esz, (uint64_t)p.G * D * esz, (uint64_t)p.S * p.G * D * esz};
+        const uint32_t box[4] = {64, 1, kBN, 1};
+        cudaError_t e = encode_tmap_bf16(&mv, v, 4, dims, strides, box);
+        if (e != cudaSuccess) return e;
+    }
+    const int n_qtiles = (p.S + kBM - 1) / kBM;
+    const int n_pairs = (n_qtiles + 1) / 2;
+    const long blocks = (long)p.B * p.H * n_pairs;
+    cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    k_fwd_tc<D><<<(unsigned)blocks, kThreadsFwd, C::kSmemBytes, st>>>(
+        mq, mk, mv, (bf16 *)out, lse, p.S, p.H, p.G, n_pairs, err);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
+                          void *out, float *lse, unsigned int *err, cudaStream_t st) {
+    if (p.D == 128) return launch_fwd_tc_d<128>(p, qhat, khat, v, out, lse, err, st);
+    if (p.D == 64) return launch_fwd_tc_d<64>(p, qhat, khat, v, out, lse, err, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace xt

@@ -3,6 +3,7 @@
 // arguments, lays out the workspace and times launches.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -32,6 +33,14 @@ struct Problem {
     int group() const { return H / G; }
 };
 
+// RoPE inverse frequencies theta^(-2i/D), i < D/2, formed on the host in
+// double and passed to the norm/RoPE kernels by value.
+constexpr int kMaxHalfDim = 64;
+struct RopeFreqs {
+    double inv_freq[kMaxHalfDim];
+};
+RopeFreqs rope_freqs(const Problem &p);
+
 // Error word bits raised by kernels whose bounded waits run out.
 enum : unsigned int { ERR_TIMEOUT = 1u };
 
@@ -52,6 +61,14 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
                             float *part_q, float *part_k, cudaStream_t st);
 cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
                                  int nparts, float *dgq, float *dgk, cudaStream_t st);
+
+// ---- TMA tensor maps (xt_tmap.cu) ----
+cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                             const uint64_t *strides_bytes, const uint32_t *box);
+
+// ---- bf16 tcgen05 kernels ----
+cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
+                          void *out, float *lse, unsigned int *err, cudaStream_t st);
 
 // ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
 cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,

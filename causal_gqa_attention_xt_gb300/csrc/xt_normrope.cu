@@ -36,16 +36,15 @@ __host__ __device__ inline int pow2_at_least(int x) {
 }
 
 // cos/sin of angle (s * theta^(-2i/D)) for the block's positions, i < D/2.
-// The angle is formed in double (as the pages' formula, with the inverse
-// frequency from pow) and reduced by 2*pi in double before an fp32 sincos,
-// so that large positions keep their accuracy.
-__device__ void rope_table(float *cs, float *sn, int s0, int ns, int D, double theta) {
+// The angle is formed in double (position times the host's double inverse
+// frequency, as in the pages' formula) and reduced by 2*pi in double before
+// an fp32 sincos, so that large positions keep their accuracy.
+__device__ void rope_table(float *cs, float *sn, int s0, int ns, int D, const RopeFreqs &fr) {
     const int half = D / 2;
     const double two_pi = 6.283185307179586476925;
     for (int e = threadIdx.x; e < ns * half; e += blockDim.x) {
         int si = e / half, i = e - si * half;
-        double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
-        double ang = (double)(s0 + si) * inv_freq;
+        double ang = (double)(s0 + si) * fr.inv_freq[i];
         double turns = rint(ang * (1.0 / two_pi));
         float red = (float)fma(-turns, two_pi, ang);
         float sv, cv;
@@ -60,7 +59,7 @@ __global__ void __launch_bounds__(kThreads)
 k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ gq,
            const float *__restrict__ gk, T *__restrict__ qhat, T *__restrict__ khat,
            float *__restrict__ rstd_q, float *__restrict__ rstd_k, int S, int H, int G, int D,
-           float eps, double theta) {
+           float eps, const RopeFreqs fr) {
     constexpr int VEC = 16 / sizeof(T);
     extern __shared__ float smem[];
     const int half = D / 2;
@@ -69,7 +68,7 @@ k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__rest
     const int s0 = (blockIdx.x - b * blocks_s) * kRowsPerBlock;
     const int ns = min(kRowsPerBlock, S - s0);
     float *cs = smem, *sn = smem + kRowsPerBlock * half;
-    rope_table(cs, sn, s0, ns, D, theta);
+    rope_table(cs, sn, s0, ns, D, fr);
     __syncthreads();
 
     const int chunks = half / VEC;             // lanes that carry data
@@ -162,7 +161,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
            const float *__restrict__ gk, const float *__restrict__ rstd_q,
            const float *__restrict__ rstd_k, T *__restrict__ dq, T *__restrict__ dk,
            float *__restrict__ part_q, float *__restrict__ part_k, int S, int H, int G, int D,
-           double theta) {
+           const RopeFreqs fr) {
     constexpr int VEC = 16 / sizeof(T);
     extern __shared__ float smem[];
     const int half = D / 2;
@@ -175,7 +174,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     const int tpr = pow2_at_least(chunks);
     const int rows_per_iter = kThreads / tpr;
     float *red = smem + 2 * kRowsPerBlock * half;   // [rows_per_iter][D]
-    rope_table(cs, sn, s0, ns, D, theta);
+    rope_table(cs, sn, s0, ns, D, fr);
     __syncthreads();
 
     const int c = threadIdx.x & (tpr - 1);
@@ -276,6 +275,13 @@ size_t table_smem(int D) { return sizeof(float) * 2 * kRowsPerBlock * (D / 2); }
 
 }  // namespace
 
+RopeFreqs rope_freqs(const Problem &p) {
+    RopeFreqs f;
+    for (int i = 0; i < kMaxHalfDim; ++i)
+        f.inv_freq[i] = (i < p.D / 2) ? pow(p.theta, -2.0 * (double)i / (double)p.D) : 0.0;
+    return f;
+}
+
 cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, const float *gq,
                             const float *gk, void *qhat, void *khat, float *rstd_q,
                             float *rstd_k, cudaStream_t st) {
@@ -284,11 +290,11 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
     if (p.dtype == 1)
         k_prologue<bf16><<<grid, kThreads, smem, st>>>(
             (const bf16 *)q, (const bf16 *)k, gq, gk, (bf16 *)qhat, (bf16 *)khat, rstd_q, rstd_k,
-            p.S, p.H, p.G, p.D, p.eps, p.theta);
+            p.S, p.H, p.G, p.D, p.eps, rope_freqs(p));
     else
         k_prologue<float><<<grid, kThreads, smem, st>>>(
             (const float *)q, (const float *)k, gq, gk, (float *)qhat, (float *)khat, rstd_q,
-            rstd_k, p.S, p.H, p.G, p.D, p.eps, p.theta);
+            rstd_k, p.S, p.H, p.G, p.D, p.eps, rope_freqs(p));
     return cudaGetLastError();
 }
 
@@ -317,11 +323,11 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
     if (p.dtype == 1)
         k_epilogue<bf16><<<grid, kThreads, smem, st>>>(
             dqhat, dkhat, (const bf16 *)q, (const bf16 *)k, gq, gk, rstd_q, rstd_k, (bf16 *)dq,
-            (bf16 *)dk, part_q, part_k, p.S, p.H, p.G, p.D, p.theta);
+            (bf16 *)dk, part_q, part_k, p.S, p.H, p.G, p.D, rope_freqs(p));
     else
         k_epilogue<float><<<grid, kThreads, smem, st>>>(
             dqhat, dkhat, (const float *)q, (const float *)k, gq, gk, rstd_q, rstd_k,
-            (float *)dq, (float *)dk, part_q, part_k, p.S, p.H, p.G, p.D, p.theta);
+            (float *)dq, (float *)dk, part_q, part_k, p.S, p.H, p.G, p.D, rope_freqs(p));
     return cudaGetLastError();
 }
 
