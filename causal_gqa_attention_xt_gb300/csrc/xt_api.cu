@@ -222,14 +222,27 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
 
     st = timed_launch(KID_BWD_PRE, s, [&] { return launch_bwd_pre(p, out, dout, dlt, s); });
     if (st != XT_OK) return st;
-    st = timed_launch(KID_BWD_DKDV_SIMT, s, [&] {
-        return launch_bwd_dkdv_simt(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, s);
-    });
-    if (st != XT_OK) return st;
-    st = timed_launch(KID_BWD_DQ_SIMT, s, [&] {
-        return launch_bwd_dq_simt(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, s);
-    });
-    if (st != XT_OK) return st;
+    if (dtype == XT_BF16) {
+        unsigned int *err = error_word_ptr();
+        if (!err) return cuda_fail(cudaGetLastError());
+        st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
+            return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, err, s);
+        });
+        if (st != XT_OK) return st;
+        st = timed_launch(KID_BWD_DQ_TC, s, [&] {
+            return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, err, s);
+        });
+        if (st != XT_OK) return st;
+    } else {
+        st = timed_launch(KID_BWD_DKDV_SIMT, s, [&] {
+            return launch_bwd_dkdv_simt(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, s);
+        });
+        if (st != XT_OK) return st;
+        st = timed_launch(KID_BWD_DQ_SIMT, s, [&] {
+            return launch_bwd_dq_simt(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, s);
+        });
+        if (st != XT_OK) return st;
+    }
     st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
         return launch_epilogue(p, dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q, rstd_k, dq, dk,
                                part_q, part_k, s);

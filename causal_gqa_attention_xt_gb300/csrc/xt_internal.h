@@ -69,6 +69,13 @@ cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const
 // ---- bf16 tcgen05 kernels ----
 cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                           void *out, float *lse, unsigned int *err, cudaStream_t st);
+cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
+                               const void *v, const void *dout, const float *lse,
+                               const float *dlt, float *dkhat, void *dv, unsigned int *err,
+                               cudaStream_t st);
+cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
+                             const void *dout, const float *lse, const float *dlt, float *dqhat,
+                             unsigned int *err, cudaStream_t st);
 
 // ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
 cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,
