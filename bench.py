@@ -51,6 +51,22 @@ def dist_env():
     return rank, world, local
 
 
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch of independent units (weak scaling)."""
+    return base_seed + rank
+
+
+def reduce_max(values, device=None):
+    """Element-wise max over ranks of a list of floats (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
     """Samples nvidia-smi clocks and throttle reasons during the timed region."""
@@ -216,7 +232,7 @@ def bench_ours(args, w):
     xt.lib()
 
     # each rank owns its own shard of batch units (weak scaling)
-    wr = w.with_(seed=w.seed + rank)
+    wr = w.with_(seed=shard_seed(w.seed, rank))
     cpu = make_inputs(wr)
     d = {k: v.to(dev) for k, v in cpu.items()}
     saved = xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta)
@@ -285,12 +301,7 @@ def bench_ours(args, w):
     step_ms_local = sum(fwd_ms + bwd_ms) / args.steps
     fwd_ms_local = sum(fwd_ms) / args.steps
     bwd_ms_local = sum(bwd_ms) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms_local, fwd_ms_local, bwd_ms_local], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, fwd_ms_m, bwd_ms_m = t.tolist()
-    else:
-        step_ms, fwd_ms_m, bwd_ms_m = step_ms_local, fwd_ms_local, bwd_ms_local
+    step_ms, fwd_ms_m, bwd_ms_m = reduce_max([step_ms_local, fwd_ms_local, bwd_ms_local], dev)
 
     # ---- end to end through the public API: pinned host buffers in and out
     pin = {k: v.pin_memory() for k, v in cpu.items()}
@@ -320,11 +331,7 @@ def bench_ours(args, w):
         e2e_step()
         e2e_ev[i][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = reduce_max([sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps], dev)[0]
 
     flops_step = w.fwd_flops + w.bwd_flops
     value = world * flops_step / (step_ms * 1e-3) / 1e12
@@ -406,6 +413,26 @@ def bench_ours(args, w):
     return 0
 
 
+def profile_run(w):
+    """One warm-up and one measured-shape fwd+bwd step (launch order: prologue,
+    fwd, bwd_pre, dkdv, dq, epilogue, dgamma_reduce, twice), for ncu."""
+    import torch
+
+    from causal_gqa_attention_xt_gb300 import build as xbuild
+    from causal_gqa_attention_xt_gb300 import xt
+    from causal_gqa_attention_xt_gb300.inputs import make_inputs
+    xbuild.build()
+    d = {k: v.cuda() for k, v in make_inputs(w).items()}
+    for _ in range(2):
+        f = xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta)
+        xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], f, d["dout"], w.eps,
+                       w.theta)
+    torch.cuda.synchronize()
+    st = xt.xt_attn_check()
+    print(f"profile run {w.name}: status {xt.xt_status_str(st)}")
+    return 0 if st == xt.XT_OK else 1
+
+
 def source_hash() -> str:
     """Hash of the CUDA sources, to tie stored ncu traffic to the kernels it measured."""
     import glob
@@ -427,11 +454,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=1024,
                     help="sequence length of the oracle's per-step sample (reference arm)")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="one warm-up and one fwd+bwd step, no timing (for ncu captures)")
     args = ap.parse_args(argv)
-    if args.warmup < 3:
-        ap.error("--warmup must be >= 3")
     from causal_gqa_attention_xt_gb300.inputs import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        w = w.with_(B=args.batch, name=f"{w.name}_B{args.batch}")
+    if args.profile_run:
+        return profile_run(w)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_ours(args, w)
