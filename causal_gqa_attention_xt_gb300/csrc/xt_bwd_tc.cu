@@ -20,10 +20,15 @@
 // TMEM buffers; the softmax warps (thread = one owned row) turn them into P
 // and dS, written back as bf16 over the columns they have read, and the MMA
 // warp consumes those as the A operand of TS MMAs. With two buffers the S/dP
-// MMAs of tile t+1 overlap the softmax of tile t.
+// MMAs of tile t+1 overlap the softmax of tile t. The MMA warp never waits for
+// its own MMAs: one thread's tcgen05.mma operations execute in issue order, so
+// the S/dP MMAs of tile t+2 (issued after the MMAs that read P/dS of tile t)
+// cannot overwrite that buffer early.
 //
-// Warps: 0-3 softmax + epilogue (thread = owned row = TMEM lane), 4 TMA
-// producer, 5 TMEM allocator + MMA issuer.
+// Warps: 0-3 and 4-7 two softmax warpgroups (thread = owned row = TMEM lane);
+// warpgroup w takes the tiles t with t % 2 == w, i.e. TMEM buffer w, so two
+// tiles' softmax run at once; they split the epilogue. Warp 8 TMA producer,
+// warp 9 TMEM allocator + MMA issuer.
 // TMEM (512 columns): buffer b at [128b, 128b+128) with S (or S^T) in its
 // first 64 columns and dP (or dP^T) in the next 64; accumulators at 256
 // (and 384).
@@ -39,8 +44,8 @@ using namespace tc;
 
 constexpr int kOwn = 128;          // owned rows per CTA (MMA M)
 constexpr int kStream = 64;        // rows per streamed tile (N of the S / dP MMAs)
-constexpr int kThreadsBwd = 192;
-constexpr int kStages = 3;
+constexpr int kThreadsBwd = 320;   // 2 softmax warpgroups, TMA warp, MMA warp
+constexpr int kStages = 4;
 
 template <int D> struct BwdCfg {
     static constexpr int kChunks = D / 64;
@@ -54,7 +59,7 @@ template <int D> struct BwdCfg {
 struct BwdBarriers {
     uint64_t own_full;
     uint64_t st_full[kStages], st_empty[kStages];
-    uint64_t s_full[2], p_full[2], s_free[2];
+    uint64_t s_full[2], p_full[2];
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -66,34 +71,27 @@ __device__ __forceinline__ void raise_error_b(unsigned int *err, volatile int *a
     *abort_flag = 1;
 }
 
-__device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t st_full_count) {
+__device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t own_count,
+                                                  uint32_t st_full_count) {
     bars.abort_flag = 0;
-    mbar_init(&bars.own_full, 1);
+    mbar_init(&bars.own_full, own_count);
     for (int s = 0; s < kStages; ++s) {
         mbar_init(&bars.st_full[s], st_full_count);
         mbar_init(&bars.st_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
         mbar_init(&bars.s_full[i], 1);
-        mbar_init(&bars.p_full[i], 128);
-        mbar_init(&bars.s_free[i], 1);
+        mbar_init(&bars.p_full[i], 128);   // one warpgroup per buffer
     }
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
 }
 
-// K-major operand descriptors (128B swizzle, 8-row groups 1024 B apart):
-// k-step kk of 16 elements inside 64-column chunks of `chunk_bytes`.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk, uint32_t chunk_bytes) {
-    return smem_desc(base + (kk >> 2) * chunk_bytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
-}
-
-// MN-major B operand: k-step kk of 16 rows (2048 B), N spread over 64-column
-// chunks `chunk_bytes` apart.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk, uint32_t chunk_bytes) {
-    return smem_desc(base + kk * 2048, chunk_bytes, 1024, kSwizzle128B);
-}
+// Operand descriptors (128B swizzle, 8-row groups 1024 B apart): a K-major
+// operand advances 16 elements by +32 B inside a 64-column chunk (chunks are
+// 16 KB for 128 rows, 8 KB for 64 rows); an MN-major B operand advances 16
+// rows by +2048 B, its 64-column N chunks `LBO` bytes apart.
 
 // ---------------------------------------------------------------------------
 // dKhat, dV
@@ -124,8 +122,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const int T = group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 2);
-    if (warp == 5) {
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2);
+    if (warp == 9) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
     }
@@ -133,7 +131,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&map_k);
@@ -187,49 +185,61 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             for (int t = max(0, issued - kStages); t < issued; ++t)
                 mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kOwn, kStream, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kOwn, D, 0, 1);
-            const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+            // descriptors built once; per MMA only compile-time offsets are added
+            const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
+            const uint64_t dV = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128B);
+            const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
+            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kStreamTile), 16, 1024, kSwizzle128B);
+            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
+            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kStreamTile), 8192, 1024, kSwizzle128B);
+            constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
+            // S^T and dP^T of tile t into TMEM buffer t % 2
+            auto issue_sp = [&](int t) {
+                const int st = t % kStages, buf = t & 1;
+                const uint64_t so = (uint64_t)st * kStep;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {    // S^T = Khat Qhat^T
+                    const uint64_t oo = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + 128 * buf, dK + oo, dQk0 + so + os, idesc_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {    // dP^T = V dO^T
+                    const uint64_t oo = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_ss(tmem + 128 * buf + 64, dV + oo, dDOk0 + so + os, idesc_s, kk > 0);
+                }
+                mma_commit(&bars.s_full[buf]);
+            };
+            // The MMA thread waits once per tile, on P/dS of that tile. The softmax
+            // warps check that the operands of tile t+2 have landed before they signal
+            // P/dS of tile t, so S/dP of tile t+2 can be issued right behind dV/dK of t.
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag);
-            for (int t = 0; ok && t <= T; ++t) {
-                if (t < T) {
-                    const int st = t % kStages, buf = t & 1;
-                    if (!(ok = mbar_wait(&bars.st_full[st], (t / kStages) & 1, abort_flag))) break;
-                    if (t >= 2 && !(ok = mbar_wait(&bars.s_free[buf], ((t >> 1) - 1) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t aQ = smem_u32(sStage + st * C::kStageBytes);
-                    const uint32_t aDO = aQ + C::kStreamTile;
+            for (int t = 0; ok && t < 2 && t < T; ++t) {
+                if (!(ok = mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_sp(t);
+            }
+            for (int t = 0; ok && t < T; ++t) {
+                const int buf = t & 1, st = t % kStages;
+                if (!(ok = mbar_wait(&bars.p_full[buf], (t >> 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)      // S^T = Khat Qhat^T
-                        mma_ss(tmem + 128 * buf, kmajor_desc(aK, kk, 16384),
-                               kmajor_desc(aQ, kk, 8192), idesc_s, kk > 0);
+                for (int kk = 0; kk < kStream / 16; ++kk)   // dV += P^T dO
+                    mma_ts(tmem + 256, tmem + 128 * buf + kk * 8, dDOm0 + so + ((kk * 2048) >> 4),
+                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)      // dP^T = V dO^T
-                        mma_ss(tmem + 128 * buf + 64, kmajor_desc(aV, kk, 16384),
-                               kmajor_desc(aDO, kk, 8192), idesc_s, kk > 0);
-                    mma_commit(&bars.s_full[buf]);
-                }
-                if (t >= 1) {
-                    const int tp = t - 1, bp = tp & 1, stp = tp % kStages;
-                    if (!(ok = mbar_wait(&bars.p_full[bp], (tp >> 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    const uint32_t aQ = smem_u32(sStage + stp * C::kStageBytes);
-                    const uint32_t aDO = aQ + C::kStreamTile;
-#pragma unroll
-                    for (int kk = 0; kk < kStream / 16; ++kk)   // dV += P^T dO
-                        mma_ts(tmem + 256, tmem + 128 * bp + kk * 8,
-                               mnmajor_desc(aDO, kk, 8192), idesc_acc, (tp > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                    for (int kk = 0; kk < kStream / 16; ++kk)   // dKhat += dS^T Qhat
-                        mma_ts(tmem + 384, tmem + 128 * bp + 64 + kk * 8,
-                               mnmajor_desc(aQ, kk, 8192), idesc_acc, (tp > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars.s_free[bp]);
-                    mma_commit(&bars.st_empty[stp]);
-                }
+                for (int kk = 0; kk < kStream / 16; ++kk)   // dKhat += dS^T Qhat
+                    mma_ts(tmem + 384, tmem + 128 * buf + 64 + kk * 8, dQm0 + so + ((kk * 2048) >> 4),
+                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars.st_empty[st]);
+                if (t + 2 < T) issue_sp(t + 2);
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -238,13 +248,14 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int r = warp * 32 + lane;                 // owned key row = TMEM lane
+        const int wg = warp >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;              // owned key row = TMEM lane
         const int kp = j * kOwn + r;                    // key position
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int buf = t & 1, st = t % kStages;
+        for (int t = wg; t < T; t += 2) {
+            const int buf = wg, st = t % kStages;
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (t >> 1) & 1, abort_flag) &&
                                              mbar_wait(&bars.st_full[st], (t / kStages) & 1, abort_flag));
             if (!ok) break;
@@ -254,29 +265,41 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const float *sl = reinterpret_cast<const float *>(sStage + st * C::kStageBytes +
                                                               2 * C::kStreamTile);
             const uint32_t tS = tmem + 128 * buf + lane_off;
+            // interior tile: every query of the tile is at/after every owned key and < S
+            const bool interior = (q0 >= j * kOwn + kOwn - 1) && (q0 + kStream <= S);
+            uint32_t pp[32], dd[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t s[32], dp[32], pp[16], dd[16];
-                tmem_ld32_sync(tS + 32 * c, s);
-                tmem_ld32_sync(tS + 64 + 32 * c, dp);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t sv[32], dpv[32];        // S^T and dP^T columns [32 hf, 32 hf + 32)
+                tmem_ld32x2_sync(tS + 32 * hf, sv, tS + 64 + 32 * hf, dpv);
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float pv[2], dsv[2];
+                for (int e = 0; e < 32; e += 4) {
+                    const int col = 32 * hf + e;
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + col);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sl + 64 + col);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                    const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
+                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int col = 32 * c + e + x, q = q0 + col;
-                        const float p = (q >= kp && q < S)
-                                            ? fast_exp2(__uint_as_float(s[e + x]) * sl2 - sl[col])
-                                            : 0.f;
+                    for (int x = 0; x < 4; ++x) {
+                        const int q = q0 + col + x;
+                        float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lv[x]));
+                        if (!interior && !(q >= kp && q < S)) p = 0.f;
                         pv[x] = p;
-                        dsv[x] = p * (__uint_as_float(dp[e + x]) - sl[64 + col]);
+                        dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlv[x]);
                     }
-                    pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                    pp[col >> 1] = pack_bf16x2(pv[0], pv[1]);
+                    pp[(col >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+                    dd[col >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                    dd[(col >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
-                tmem_st16_sync(tS + 16 * c, pp);
-                tmem_st16_sync(tS + 64 + 16 * c, dd);
             }
+            if (t + 2 < T) {   // operands of tile t+2 (issued right after this tile's dV/dK)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 2) % kStages],
+                                                       ((t + 2) / kStages) & 1, abort_flag));
+                if (!ok) break;
+            }
+            tmem_st32x2_sync(tS, pp, tS + 64, dd);
             tc_fence_before();
             mbar_arrive(&bars.p_full[buf]);
         }
@@ -284,34 +307,41 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
             if (ok) {
                 tc_fence_after();
-                const float scale = rsqrtf((float)D);
-                bf16 *dvrow = dv + (((size_t)b * S + kp) * G + g) * D;
-                float *dkrow = dkhat + ((size_t)bg * S + kp) * D;
+                if (wg == 0) {      // dV row -> bf16
+                    bf16 *dvrow = dv + (((size_t)b * S + kp) * G + g) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t a[32];
-                    tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
-                    if (kp < S) {
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t a[32];
+                        tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
+                        if (kp < S) {
 #pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            uint4 v4;
-                            v4.x = pack_bf16x2(__uint_as_float(a[q8 * 8 + 0]), __uint_as_float(a[q8 * 8 + 1]));
-                            v4.y = pack_bf16x2(__uint_as_float(a[q8 * 8 + 2]), __uint_as_float(a[q8 * 8 + 3]));
-                            v4.z = pack_bf16x2(__uint_as_float(a[q8 * 8 + 4]), __uint_as_float(a[q8 * 8 + 5]));
-                            v4.w = pack_bf16x2(__uint_as_float(a[q8 * 8 + 6]), __uint_as_float(a[q8 * 8 + 7]));
-                            *reinterpret_cast<uint4 *>(dvrow + 32 * c + 8 * q8) = v4;
+                            for (int q8 = 0; q8 < 4; ++q8) {
+                                uint4 v4;
+                                v4.x = pack_bf16x2(__uint_as_float(a[q8 * 8 + 0]), __uint_as_float(a[q8 * 8 + 1]));
+                                v4.y = pack_bf16x2(__uint_as_float(a[q8 * 8 + 2]), __uint_as_float(a[q8 * 8 + 3]));
+                                v4.z = pack_bf16x2(__uint_as_float(a[q8 * 8 + 4]), __uint_as_float(a[q8 * 8 + 5]));
+                                v4.w = pack_bf16x2(__uint_as_float(a[q8 * 8 + 6]), __uint_as_float(a[q8 * 8 + 7]));
+                                *reinterpret_cast<uint4 *>(dvrow + 32 * c + 8 * q8) = v4;
+                            }
                         }
                     }
-                    tmem_ld32_sync(tmem + 384 + lane_off + 32 * c, a);
-                    if (kp < S) {
+                } else {            // dKhat row (scaled) -> fp32
+                    const float scale = rsqrtf((float)D);
+                    float *dkrow = dkhat + ((size_t)bg * S + kp) * D;
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            float4 f;
-                            f.x = __uint_as_float(a[q4 * 4 + 0]) * scale;
-                            f.y = __uint_as_float(a[q4 * 4 + 1]) * scale;
-                            f.z = __uint_as_float(a[q4 * 4 + 2]) * scale;
-                            f.w = __uint_as_float(a[q4 * 4 + 3]) * scale;
-                            *reinterpret_cast<float4 *>(dkrow + 32 * c + 4 * q4) = f;
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t a[32];
+                        tmem_ld32_sync(tmem + 384 + lane_off + 32 * c, a);
+                        if (kp < S) {
+#pragma unroll
+                            for (int q4 = 0; q4 < 8; ++q4) {
+                                float4 f;
+                                f.x = __uint_as_float(a[q4 * 4 + 0]) * scale;
+                                f.y = __uint_as_float(a[q4 * 4 + 1]) * scale;
+                                f.z = __uint_as_float(a[q4 * 4 + 2]) * scale;
+                                f.w = __uint_as_float(a[q4 * 4 + 3]) * scale;
+                                *reinterpret_cast<float4 *>(dkrow + 32 * c + 4 * q4) = f;
+                            }
                         }
                     }
                 }
@@ -321,7 +351,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -332,17 +362,17 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
-k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
-            const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+            const bf16 *__restrict__ qhat, const bf16 *__restrict__ dout,
             const float *__restrict__ lse, const float *__restrict__ dlt,
             float *__restrict__ dqhat, int S, int H, int G, int n_qt, unsigned int *err) {
     using C = BwdCfg<D>;
+    // TMEM columns of the resident A operands (D/2 packed columns each)
+    constexpr uint32_t kTQ = 384, kTDO = 448;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sQ = smem;
-    uint8_t *sDO = smem + C::kOwnTile;
-    uint8_t *sStage = smem + 2 * C::kOwnTile;
+    uint8_t *sStage = smem;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = gridDim.x / n_qt;
@@ -353,8 +383,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     const int T = min(2 * i + 2, n_k64);               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 1);
-    if (warp == 5) {
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1);
+    if (warp == 9) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
     }
@@ -362,18 +392,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            tma_prefetch_desc(&map_q);
-            tma_prefetch_desc(&map_do);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
-            mbar_expect_tx(&bars.own_full, 2 * C::kOwnTile);
-            for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(sQ + c * 16384, &map_q, &bars.own_full, c * 64, i * kOwn, bh);
-                tma_load_4d(sDO + c * 16384, &map_do, &bars.own_full, c * 64, h, i * kOwn, b);
-            }
             int issued = 0;
             for (int t = 0; t < T; ++t) {
                 const int st = t % kStages;
@@ -392,48 +415,55 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 }
                 issued = t + 1;
             }
-            mbar_wait(&bars.own_full, 0, nullptr);
             for (int t = max(0, issued - kStages); t < issued; ++t)
                 mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, nullptr);
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kOwn, kStream, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kOwn, D, 0, 1);
-            const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
+            // descriptors built once; per MMA only compile-time offsets are added
+            const uint64_t dKk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
+            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kStreamTile), 16, 1024, kSwizzle128B);
+            const uint64_t dKm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
+            constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
+            // S and dP of tile t into TMEM buffer t % 2
+            auto issue_sp = [&](int t) {
+                const int st = t % kStages, buf = t & 1;
+                const uint64_t so = (uint64_t)st * kStep;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {    // S = Qhat Khat^T (Qhat in TMEM)
+                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_ts(tmem + 128 * buf, tmem + kTQ + kk * 8, dKk0 + so + os, idesc_s, kk > 0);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {    // dP = dO V^T (dO in TMEM)
+                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+                    mma_ts(tmem + 128 * buf + 64, tmem + kTDO + kk * 8, dVk0 + so + os, idesc_s,
+                           kk > 0);
+                }
+                mma_commit(&bars.s_full[buf]);
+            };
+            // One wait per tile (dS of tile t); the softmax warps check the operands of
+            // tile t+2 before signalling, so S/dP of t+2 follow dQ of t immediately.
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag);
-            for (int t = 0; ok && t <= T; ++t) {
-                if (t < T) {
-                    const int st = t % kStages, buf = t & 1;
-                    if (!(ok = mbar_wait(&bars.st_full[st], (t / kStages) & 1, abort_flag))) break;
-                    if (t >= 2 && !(ok = mbar_wait(&bars.s_free[buf], ((t >> 1) - 1) & 1, abort_flag)))
-                        break;
-                    tc_fence_after();
-                    const uint32_t aK = smem_u32(sStage + st * C::kStageBytes);
-                    const uint32_t aV = aK + C::kStreamTile;
+            for (int t = 0; ok && t < 2 && t < T; ++t) {
+                if (!(ok = mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, abort_flag))) break;
+                tc_fence_after();
+                issue_sp(t);
+            }
+            for (int t = 0; ok && t < T; ++t) {
+                const int buf = t & 1, st = t % kStages;
+                if (!(ok = mbar_wait(&bars.p_full[buf], (t >> 1) & 1, abort_flag))) break;
+                tc_fence_after();
+                const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)      // S = Qhat Khat^T
-                        mma_ss(tmem + 128 * buf, kmajor_desc(aQ, kk, 16384),
-                               kmajor_desc(aK, kk, 8192), idesc_s, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)      // dP = dO V^T
-                        mma_ss(tmem + 128 * buf + 64, kmajor_desc(aDO, kk, 16384),
-                               kmajor_desc(aV, kk, 8192), idesc_s, kk > 0);
-                    mma_commit(&bars.s_full[buf]);
-                }
-                if (t >= 1) {
-                    const int tp = t - 1, bp = tp & 1, stp = tp % kStages;
-                    if (!(ok = mbar_wait(&bars.p_full[bp], (tp >> 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    const uint32_t aK = smem_u32(sStage + stp * C::kStageBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kStream / 16; ++kk)   // dQhat += dS Khat
-                        mma_ts(tmem + 256, tmem + 128 * bp + kk * 8, mnmajor_desc(aK, kk, 8192),
-                               idesc_acc, (tp > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars.s_free[bp]);
-                    mma_commit(&bars.st_empty[stp]);
-                }
+                for (int kk = 0; kk < kStream / 16; ++kk)   // dQhat += dS Khat
+                    mma_ts(tmem + 256, tmem + 128 * buf + kk * 8, dKm0 + so + ((kk * 2048) >> 4),
+                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&bars.st_empty[st]);
+                if (t + 2 < T) issue_sp(t + 2);
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -442,40 +472,66 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
-        const int r = warp * 32 + lane;                // owned query row = TMEM lane
+        const int wg = warp >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;             // owned query row = TMEM lane
         const int tq = i * kOwn + r;                   // query position
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         const float lse2 = tq < S ? lse[(size_t)bh * S + tq] * kLog2e : 0.f;
         const float dl = tq < S ? dlt[(size_t)bh * S + tq] : 0.f;
+        {
+            // the owned Qhat (warpgroup 0) and dO (warpgroup 1) rows become TMEM-resident
+            // A operands (lane = row; a 32-bit column holds two consecutive bf16, the lower
+            // index in the low half)
+            uint32_t xa[D / 2];
+            const uint4 *src = wg == 0
+                ? reinterpret_cast<const uint4 *>(qhat + ((size_t)bh * S + tq) * D)
+                : reinterpret_cast<const uint4 *>(dout + (((size_t)b * S + tq) * H + h) * D);
+#pragma unroll
+            for (int c = 0; c < D / 8; ++c) {
+                const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
+                xa[4 * c] = z.x; xa[4 * c + 1] = z.y; xa[4 * c + 2] = z.z; xa[4 * c + 3] = z.w;
+            }
+            const uint32_t dst = tmem + (wg == 0 ? kTQ : kTDO) + lane_off;
+            if constexpr (D == 128) tmem_st64_sync(dst, xa);
+            else tmem_st32_sync(dst, xa);
+            tc_fence_before();
+            mbar_arrive(&bars.own_full);
+        }
         bool ok = true;
-        for (int t = 0; t < T; ++t) {
-            const int buf = t & 1;
+        for (int t = wg; t < T; t += 2) {
+            const int buf = wg;
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (t >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int k0 = t * kStream;
             const uint32_t tS = tmem + 128 * buf + lane_off;
+            // interior tile: every key of the tile is at/before every owned query
+            const bool interior = (k0 + kStream - 1 <= i * kOwn);
+            uint32_t dd[32];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t s[32], dp[32], dd[16];
-                tmem_ld32_sync(tS + 32 * c, s);
-                tmem_ld32_sync(tS + 64 + 32 * c, dp);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t sv[32], dpv[32];        // S and dP columns [32 hf, 32 hf + 32)
+                tmem_ld32x2_sync(tS + 32 * hf, sv, tS + 64 + 32 * hf, dpv);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float dsv[2];
 #pragma unroll
                     for (int x = 0; x < 2; ++x) {
-                        const int kpos = k0 + 32 * c + e + x;
-                        const float p = (kpos <= tq)
-                                            ? fast_exp2(__uint_as_float(s[e + x]) * sl2 - lse2)
-                                            : 0.f;
-                        dsv[x] = p * (__uint_as_float(dp[e + x]) - dl);
+                        const int kpos = k0 + 32 * hf + e + x;
+                        float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lse2));
+                        if (!interior && kpos > tq) p = 0.f;
+                        dsv[x] = p * (__uint_as_float(dpv[e + x]) - dl);
                     }
-                    dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                    dd[(32 * hf + e) >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                 }
-                tmem_st16_sync(tS + 16 * c, dd);
             }
+            if (t + 2 < T) {   // operands of tile t+2 (issued right after this tile's dQ)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 2) % kStages],
+                                                       ((t + 2) / kStages) & 1, abort_flag));
+                if (!ok) break;
+            }
+            tmem_st32_sync(tS, dd);
             tc_fence_before();
             mbar_arrive(&bars.p_full[buf]);
         }
@@ -485,8 +541,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
                 tc_fence_after();
                 const float scale = rsqrtf((float)D);
                 float *dst = dqhat + ((size_t)bh * S + tq) * D;
+                // the two warpgroups split the D columns of the dQhat row
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
+                for (int cc = 0; cc < D / 64; ++cc) {
+                    const int c = wg * (D / 64) + cc;
                     uint32_t a[32];
                     tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
                     if (tq < S) {
@@ -507,7 +565,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -584,8 +642,8 @@ cudaError_t launch_dq_d(const Problem &p, const void *qhat, const void *khat, co
     if ((e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   C::kSmemBytes)) != cudaSuccess)
         return e;
-    k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemBytes, st>>>(
-        m.q, m.dout, m.k, m.v, lse, dlt, dqhat, p.S, p.H, p.G, n_qt, err);
+    k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemBytes - 2 * C::kOwnTile, st>>>(
+        m.k, m.v, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, dqhat, p.S, p.H, p.G, n_qt, err);
     return cudaGetLastError();
 }
 

@@ -152,44 +152,64 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
+        // Issue order per key tile j: PV_{j,0}, S_{j+1,0}, PV_{j,1}, S_{j+1,1}, so the
+        // next S of query tile 0 queues right behind its PV while tile 1's softmax runs.
+        // The MMA warp waits for data (TMA) and for P (softmax), never for its own
+        // MMAs: the tensor pipe executes one thread's MMAs in issue order.
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
             const uint32_t tS[2] = {tmem, tmem + 128};
             const uint32_t tO[2] = {tmem + 256, tmem + 384};
-            bool ok = mbar_wait(&bars.q_full, 0, abort_flag);
-            for (int j = 0; ok && j < n_iter; ++j) {
-                const int st = j % C::kStages;
-                const uint32_t ph = (j / C::kStages) & 1;
-                const uint32_t sK = smem_u32(sKV + (2 * st) * C::kTileBytes);
-                const uint32_t sV = smem_u32(sKV + (2 * st + 1) * C::kTileBytes);
-                if (!(ok = mbar_wait(&bars.k_full[st], ph, abort_flag))) break;
-                for (int i = 0; i < 2 && ok; ++i) {
-                    if (j >= n_kv[i]) continue;
-                    // S_i is free once PV_{j-1,i} (which read P_i from it) completed
-                    if (j > 0 && !(ok = mbar_wait(&bars.o_done[i], (j - 1) & 1, abort_flag))) break;
-                    tc_fence_after();
-                    const uint32_t sQi = smem_u32(sQ + i * C::kTileBytes);
+            // Descriptors are built once; per MMA only a compile-time offset (>> 4, the
+            // start-address field) is added, which keeps the single issuing thread fast.
+            const uint64_t dQ0 = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
+            const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024, kSwizzle128B);
+            const uint64_t dV0 = smem_desc(smem_u32(sKV + C::kTileBytes), 16384, 1024, kSwizzle128B);
+            constexpr uint64_t kStageStep = (uint64_t)(2 * C::kTileBytes) >> 4;
+            constexpr uint64_t kQStep = (uint64_t)C::kTileBytes >> 4;
+            auto issue_s = [&](int i, int st) {
+                const uint64_t dQ = dQ0 + (uint64_t)i * kQStep;
+                const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        mma_ss(tS[i], smem_desc(sQi + off, 16, 1024, kSwizzle128B),
-                               smem_desc(sK + off, 16, 1024, kSwizzle128B), idesc_s, kk > 0);
-                    }
-                    mma_commit(&bars.s_full[i]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    mma_ss(tS[i], dQ + off, dK + off, idesc_s, kk > 0);
                 }
-                if (!ok) break;
-                if (!(ok = mbar_wait(&bars.v_full[st], ph, abort_flag))) break;
+                mma_commit(&bars.s_full[i]);
+            };
+            bool ok = mbar_wait(&bars.q_full, 0, abort_flag) &&
+                      mbar_wait(&bars.k_full[0], 0, abort_flag);
+            if (ok) {
+                tc_fence_after();
+                for (int i = 0; i < 2; ++i)
+                    if (n_kv[i] > 0) issue_s(i, 0);
+            }
+            for (int j = 0; ok && j < n_iter; ++j) {
+                const int st = j % C::kStages, st1 = (j + 1) % C::kStages;
+                const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
+                if (!(ok = mbar_wait(&bars.v_full[st], (j / C::kStages) & 1, abort_flag))) break;
+                bool k_next = false;
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (j >= n_kv[i]) continue;
                     if (!(ok = mbar_wait(&bars.p_full[i], j & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tO[i], tS[i] + kk * 8,
-                               smem_desc(sV + kk * 2048, 16384, 1024, kSwizzle128B), idesc_o,
+                        mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)((kk * 2048) >> 4), idesc_o,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&bars.o_done[i]);
+                    if (j + 1 < n_kv[i]) {
+                        if (!k_next) {
+                            if (!(ok = mbar_wait(&bars.k_full[st1], ((j + 1) / C::kStages) & 1,
+                                                 abort_flag)))
+                                break;
+                            k_next = true;
+                        }
+                        // No wait for PV_{j,i} to finish reading P_i: tcgen05.mma operations
+                        // issued by one thread execute in issue order.
+                        issue_s(i, st1);
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&bars.kv_empty[st]);
@@ -216,20 +236,21 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[i], j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[4][32];
+            uint32_t sr[128];
+            tmem_ld128_sync(tS, sr);
+            if (j == n - 1) {
+                // diagonal tile: key column c is visible to row r iff c <= r
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32_sync(tS + c * 32, sr[c]);
-            const bool diag = (j == n - 1);
-            float mx = -INFINITY;
+                for (int e = 0; e < 128; ++e)
+                    if (e > r) sr[e] = __float_as_uint(-INFINITY);
+            }
+            float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float x = __uint_as_float(sr[c][e]) * sl2;
-                    if (diag && (c * 32 + e) > r) x = -INFINITY;
-                    sr[c][e] = __float_as_uint(x);
-                    mx = fmaxf(mx, x);
-                }
+            for (int e = 0; e < 128; e += 4) {
+                m0 = fmax3(m0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                m1 = fmax3(m1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+            }
+            const float mx = fmaxf(m0, m1) * sl2;
             const float m_new = fmaxf(m_used, mx);
             const bool need = m_new - m_used > kRescaleThreshold;   // true on the first tile
             float alpha = 1.f;
@@ -251,19 +272,21 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                     tmem_st32_sync(tO + c * 32, o);
                 }
             }
-            float rowsum = 0.f;
-            uint32_t pk[2][32];
+            const float neg_m = -m_used;
+            float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    const float p0 = fast_exp2(__uint_as_float(sr[c][e]) - m_used);
-                    const float p1 = fast_exp2(__uint_as_float(sr[c][e + 1]) - m_used);
-                    rowsum += p0 + p1;
-                    pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(p0, p1);
-                }
-            tmem_st32_sync(tS, pk[0]);
-            tmem_st32_sync(tS + 32, pk[1]);
+            for (int e = 0; e < 128; e += 4) {
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), sl2, neg_m));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), sl2, neg_m));
+                const float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), sl2, neg_m));
+                const float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), sl2, neg_m));
+                rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
+                pk[e >> 1] = pack_bf16x2(p0, p1);
+                pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+            }
+            const float rowsum = (rs0 + rs1) + (rs2 + rs3);
+            tmem_st64_sync(tS, pk);
             tc_fence_before();
             mbar_arrive(&bars.p_full[i]);
             l = l * alpha + rowsum;
