@@ -10,28 +10,31 @@
 //
 // Two kernels, both deterministic:
 //  * k_bwd_dkdv_tc: a CTA owns 128 key rows of one (batch, kv head) and walks
-//    the group's query heads r = 0..group-1 in order, each over the 64-row
+//    the group's query heads r = 0..group-1 in order, each over the 128-row
 //    query tiles at or after its keys, accumulating dV += P^T dO and
 //    dKhat += dS^T Qhat in TMEM: the group sum happens inside the CTA.
 //  * k_bwd_dq_tc: a CTA owns 128 query rows of one (batch, head) and walks
-//    the 64-row key tiles at or before them, accumulating dQhat += dS Khat.
-// Both recompute S from the saved Qhat, Khat and lse. For each streamed
-// 64-row tile the MMA warp issues S (or S^T) and dP (or dP^T) into one of two
-// TMEM buffers; the softmax warps (thread = one owned row) turn them into P
-// and dS, written back as bf16 over the columns they have read, and the MMA
-// warp consumes those as the A operand of TS MMAs. With two buffers the S/dP
-// MMAs of tile t+1 overlap the softmax of tile t. The MMA warp never waits for
-// its own MMAs: one thread's tcgen05.mma operations execute in issue order, so
-// the S/dP MMAs of tile t+2 (issued after the MMAs that read P/dS of tile t)
-// cannot overwrite that buffer early.
+//    the 128-row key tiles at or before them, accumulating dQhat += dS Khat.
+// Both recompute S from the saved Qhat, Khat and lse.
 //
-// Warps: 0-3 and 4-7 two softmax warpgroups (thread = owned row = TMEM lane);
-// warpgroup w takes the tiles t with t % 2 == w, i.e. TMEM buffer w, so two
-// tiles' softmax run at once; they split the epilogue. Warp 8 TMA producer,
-// warp 9 TMEM allocator + MMA issuer.
-// TMEM (512 columns): buffer b at [128b, 128b+128) with S (or S^T) in its
-// first 64 columns and dP (or dP^T) in the next 64; accumulators at 256
-// (and 384).
+// Per streamed tile the MMA warp issues S (or S^T) into TMEM columns
+// [0,128) and dP (or dP^T) into [128,256) (M=128, N=128: full-rate MMA
+// shapes); two softmax warpgroups split the 128 columns (warpgroup w takes
+// columns [64w, 64w+64)), form P and dS, and write them back as packed bf16
+// over the columns they themselves read (P at [64w, 64w+32), dS at
+// [128+64w, 128+64w+32)), so the two halves never race. The accumulating MMAs
+// (TS form, A from TMEM) read those halves k-step by k-step.
+//
+// Pipeline: the MMA thread polls one mbarrier per tile (P/dS of tile t) and
+// then issues the accumulating MMAs of t followed by S/dP of t+1, which
+// reuse the TMEM buffer: one thread's tcgen05.mma operations execute in issue
+// order, so t+1 cannot overwrite P/dS of t before they are read. An mbarrier
+// poll right after tcgen05.commit stalls the issuing thread until earlier
+// MMAs drain, so the TMA-arrival check for tile t+1 is done by the softmax
+// warps before they signal tile t.
+//
+// Warps: 0-3 and 4-7 the softmax warpgroups (thread = owned row = TMEM
+// lane); 8 TMA producer; 9 TMEM allocator + MMA issuer.
 #include "xt_common.cuh"
 #include "xt_internal.h"
 #include "xt_tc.cuh"
@@ -42,24 +45,24 @@ namespace {
 
 using namespace tc;
 
-constexpr int kOwn = 128;          // owned rows per CTA (MMA M)
-constexpr int kStream = 64;        // rows per streamed tile (N of the S / dP MMAs)
-constexpr int kThreadsBwd = 320;   // 2 softmax warpgroups, TMA warp, MMA warp
-constexpr int kStages = 4;
+constexpr int kTile = 128;         // owned rows (MMA M) and streamed rows (MMA N of S/dP)
+constexpr int kThreadsBwd = 320;
+constexpr int kMaxStages = 4;
 
 template <int D> struct BwdCfg {
     static constexpr int kChunks = D / 64;
-    static constexpr int kOwnTile = kChunks * 16384;     // 128 rows x D bf16
-    static constexpr int kStreamTile = kChunks * 8192;   // 64 rows x D bf16
-    // a stage holds two streamed tiles and (dK/dV kernel) 2 x 64 row statistics
-    static constexpr int kStageBytes = 2 * kStreamTile + 1024;
-    static constexpr int kSmemBytes = 2 * kOwnTile + kStages * kStageBytes + 1024;
+    static constexpr int kTileBytes = kChunks * 16384;   // 128 rows x D bf16
+    static constexpr int kStages = (D == 128) ? 2 : 4;
+    // a stage: two 128-row tiles and (dK/dV kernel) 2 x 128 row statistics
+    static constexpr int kStageBytes = 2 * kTileBytes + 1024;
+    static constexpr int kSmemA = 2 * kTileBytes + kStages * kStageBytes + 1024;
+    static constexpr int kSmemB = kStages * kStageBytes + 1024;
 };
 
 struct BwdBarriers {
     uint64_t own_full;
-    uint64_t st_full[kStages], st_empty[kStages];
-    uint64_t s_full[2], p_full[2];
+    uint64_t st_full[kMaxStages], st_empty[kMaxStages];
+    uint64_t s_full, p_full;
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -72,26 +75,33 @@ __device__ __forceinline__ void raise_error_b(unsigned int *err, volatile int *a
 }
 
 __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t own_count,
-                                                  uint32_t st_full_count) {
+                                                  uint32_t st_full_count, int stages) {
     bars.abort_flag = 0;
     mbar_init(&bars.own_full, own_count);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
         mbar_init(&bars.st_full[s], st_full_count);
         mbar_init(&bars.st_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars.s_full[i], 1);
-        mbar_init(&bars.p_full[i], 128);   // one warpgroup per buffer
-    }
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 256);     // both softmax warpgroups
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
 }
 
+// TMEM column of the packed-bf16 A operand (P or dS) for k-step kk of 16 rows:
+// warpgroup 0 wrote rows 0..63 at columns [0,32), warpgroup 1 rows 64..127 at
+// [64,96) (relative to the S or dP region).
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+    return kk < 4 ? (uint32_t)(kk * 8) : (uint32_t)(64 + (kk - 4) * 8);
+}
+
 // Operand descriptors (128B swizzle, 8-row groups 1024 B apart): a K-major
-// operand advances 16 elements by +32 B inside a 64-column chunk (chunks are
-// 16 KB for 128 rows, 8 KB for 64 rows); an MN-major B operand advances 16
-// rows by +2048 B, its 64-column N chunks `LBO` bytes apart.
+// operand advances 16 elements by +32 B inside a 64-column chunk of 16 KB;
+// an MN-major B operand advances 16 rows by +2048 B, its 64-column N chunks
+// 16 KB apart.
+constexpr uint64_t kmajor_off(int kk) { return (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; }
+constexpr uint64_t mnmajor_off(int kk) { return (uint64_t)(kk * 2048) >> 4; }
 
 // ---------------------------------------------------------------------------
 // dKhat, dV
@@ -104,25 +114,25 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
               float *__restrict__ dkhat, bf16 *__restrict__ dv, int S, int H, int G,
               int n_kvt, unsigned int *err) {
     using C = BwdCfg<D>;
+    constexpr int ST = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sK = smem;
-    uint8_t *sV = smem + C::kOwnTile;
-    uint8_t *sStage = smem + 2 * C::kOwnTile;
+    uint8_t *sV = smem + C::kTileBytes;
+    uint8_t *sStage = smem + 2 * C::kTileBytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BG = gridDim.x / n_kvt;
     const int j = (int)(blockIdx.x / BG);          // key tile, longest first
     const int bg = blockIdx.x % BG;
     const int b = bg / G, g = bg - b * G, group = H / G;
-    const int n_q64 = (S + kStream - 1) / kStream;
-    const int u0 = 2 * j;                           // first query tile at/after the keys
-    const int nU = n_q64 - u0;
+    const int n_q = (S + kTile - 1) / kTile;
+    const int nU = n_q - j;                         // query tiles at/after the keys, per head
     const int T = group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, ST);
     if (warp == 9) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -138,42 +148,42 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             tma_prefetch_desc(&map_v);
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_do);
-            mbar_expect_tx(&bars.own_full, 2 * C::kOwnTile);
+            mbar_expect_tx(&bars.own_full, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(sK + c * 16384, &map_k, &bars.own_full, c * 64, j * kOwn, bg);
-                tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g, j * kOwn, b);
+                tma_load_3d(sK + c * 16384, &map_k, &bars.own_full, c * 64, j * kTile, bg);
+                tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g, j * kTile, b);
             }
         }
         int issued = 0;
         for (int t = 0; t < T; ++t) {
-            const int st = t % kStages;
+            const int st = t % ST;
             bool ok = true;
-            if (t >= kStages && lane == 0)
-                ok = mbar_wait(&bars.st_empty[st], ((t / kStages) - 1) & 1, abort_flag);
+            if (t >= ST && lane == 0)
+                ok = mbar_wait(&bars.st_empty[st], ((t / ST) - 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
                 break;
             }
-            const int r = t / nU, u = u0 + (t - r * nU);
+            const int r = t / nU, u = j + (t - r * nU);
             const int h = g * group + r;
             uint8_t *base = sStage + st * C::kStageBytes;
             if (lane == 0) {
-                mbar_expect_tx(&bars.st_full[st], 2 * C::kStreamTile);
+                mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 8192, &map_q, &bars.st_full[st], c * 64, u * kStream,
+                    tma_load_3d(base + c * 16384, &map_q, &bars.st_full[st], c * 64, u * kTile,
                                 b * H + h);
-                    tma_load_4d(base + C::kStreamTile + c * 8192, &map_do, &bars.st_full[st],
-                                c * 64, h, u * kStream, b);
+                    tma_load_4d(base + C::kTileBytes + c * 16384, &map_do, &bars.st_full[st],
+                                c * 64, h, u * kTile, b);
                 }
             }
-            float *sl = reinterpret_cast<float *>(base + 2 * C::kStreamTile);
+            float *sl = reinterpret_cast<float *>(base + 2 * C::kTileBytes);
             const size_t row0 = ((size_t)b * H + h) * S;
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int k = lane + 32 * e, q = u * kStream + k;
+            for (int e = 0; e < 4; ++e) {
+                const int k = lane + 32 * e, q = u * kTile + k;
                 sl[k] = q < S ? lse[row0 + q] * kLog2e : 0.f;
-                sl[64 + k] = q < S ? dlt[row0 + q] : 0.f;
+                sl[128 + k] = q < S ? dlt[row0 + q] : 0.f;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.st_full[st]);
@@ -182,64 +192,53 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         if (lane == 0) {
             // drain: every copy issued by this CTA lands before it exits
             mbar_wait(&bars.own_full, 0, nullptr);
-            for (int t = max(0, issued - kStages); t < issued; ++t)
-                mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, nullptr);
+            for (int t = max(0, issued - ST); t < issued; ++t)
+                mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(kOwn, kStream, 0, 0);
-            const uint32_t idesc_acc = idesc_bf16_f32(kOwn, D, 0, 1);
-            // descriptors built once; per MMA only compile-time offsets are added
+            const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
+            const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
             const uint64_t dV = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128B);
             const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
-            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kStreamTile), 16, 1024, kSwizzle128B);
-            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
-            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kStreamTile), 8192, 1024, kSwizzle128B);
+            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, 1024, kSwizzle128B);
+            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
+            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16384, 1024, kSwizzle128B);
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
-            // S^T and dP^T of tile t into TMEM buffer t % 2
-            auto issue_sp = [&](int t) {
-                const int st = t % kStages, buf = t & 1;
-                const uint64_t so = (uint64_t)st * kStep;
+            auto issue_sp = [&](int t) {            // S^T = Khat Qhat^T, dP^T = V dO^T
+                const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {    // S^T = Khat Qhat^T
-                    const uint64_t oo = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + 128 * buf, dK + oo, dQk0 + so + os, idesc_s, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem, dK + kmajor_off(kk), dQk0 + so + kmajor_off(kk), idesc_s, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {    // dP^T = V dO^T
-                    const uint64_t oo = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ss(tmem + 128 * buf + 64, dV + oo, dDOk0 + so + os, idesc_s, kk > 0);
-                }
-                mma_commit(&bars.s_full[buf]);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128, dV + kmajor_off(kk), dDOk0 + so + kmajor_off(kk), idesc_s,
+                           kk > 0);
+                mma_commit(&bars.s_full);
             };
-            // The MMA thread waits once per tile, on P/dS of that tile. The softmax
-            // warps check that the operands of tile t+2 have landed before they signal
-            // P/dS of tile t, so S/dP of tile t+2 can be issued right behind dV/dK of t.
-            bool ok = mbar_wait(&bars.own_full, 0, abort_flag);
-            for (int t = 0; ok && t < 2 && t < T; ++t) {
-                if (!(ok = mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, abort_flag))) break;
+            bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
+                      mbar_wait(&bars.st_full[0], 0, abort_flag);
+            if (ok) {
                 tc_fence_after();
-                issue_sp(t);
+                issue_sp(0);
             }
             for (int t = 0; ok && t < T; ++t) {
-                const int buf = t & 1, st = t % kStages;
-                if (!(ok = mbar_wait(&bars.p_full[buf], (t >> 1) & 1, abort_flag))) break;
+                const int st = t % ST;
+                if (!(ok = mbar_wait(&bars.p_full, t & 1, abort_flag))) break;
                 tc_fence_after();
                 const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
-                for (int kk = 0; kk < kStream / 16; ++kk)   // dV += P^T dO
-                    mma_ts(tmem + 256, tmem + 128 * buf + kk * 8, dDOm0 + so + ((kk * 2048) >> 4),
+                for (int kk = 0; kk < kTile / 16; ++kk)   // dV += P^T dO
+                    mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-                for (int kk = 0; kk < kStream / 16; ++kk)   // dKhat += dS^T Qhat
-                    mma_ts(tmem + 384, tmem + 128 * buf + 64 + kk * 8, dQm0 + so + ((kk * 2048) >> 4),
+                for (int kk = 0; kk < kTile / 16; ++kk)   // dKhat += dS^T Qhat
+                    mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars.st_empty[st]);
-                if (t + 2 < T) issue_sp(t + 2);
+                if (t + 1 < T) issue_sp(t + 1);       // operands checked by the softmax warps
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -250,33 +249,35 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         // ------------------------------------------------------------ softmax + epilogue
         const int wg = warp >> 2, quarter = warp & 3;
         const int r = quarter * 32 + lane;              // owned key row = TMEM lane
-        const int kp = j * kOwn + r;                    // key position
+        const int kp = j * kTile + r;                   // key position
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         bool ok = true;
-        for (int t = wg; t < T; t += 2) {
-            const int buf = wg, st = t % kStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (t >> 1) & 1, abort_flag) &&
-                                             mbar_wait(&bars.st_full[st], (t / kStages) & 1, abort_flag));
+        for (int t = 0; t < T; ++t) {
+            const int st = t % ST;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, t & 1, abort_flag) &&
+                                             mbar_wait(&bars.st_full[st], (t / ST) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int u = u0 + (t % nU);
-            const int q0 = u * kStream;
+            const int u = j + (t % nU);
+            const int c0 = wg * 64;                     // this warpgroup's columns
+            const int q0 = u * kTile + c0;
             const float *sl = reinterpret_cast<const float *>(sStage + st * C::kStageBytes +
-                                                              2 * C::kStreamTile);
-            const uint32_t tS = tmem + 128 * buf + lane_off;
-            // interior tile: every query of the tile is at/after every owned key and < S
-            const bool interior = (q0 >= j * kOwn + kOwn - 1) && (q0 + kStream <= S);
+                                                              2 * C::kTileBytes);
+            const uint32_t tS = tmem + lane_off + c0;         // S^T columns
+            const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
+            // no masking when every query of these columns is at/after every owned key and < S
+            const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + 64 <= S);
             uint32_t pp[32], dd[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                uint32_t sv[32], dpv[32];        // S^T and dP^T columns [32 hf, 32 hf + 32)
-                tmem_ld32x2_sync(tS + 32 * hf, sv, tS + 64 + 32 * hf, dpv);
+                uint32_t sv[32], dpv[32];
+                tmem_ld32x2_sync(tS + 32 * hf, sv, tP + 32 * hf, dpv);
 #pragma unroll
                 for (int e = 0; e < 32; e += 4) {
-                    const int col = 32 * hf + e;
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + col);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(sl + 64 + col);
+                    const int col = 32 * hf + e;              // within this warpgroup's 64
+                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + c0 + col);
+                    const float4 d4 = *reinterpret_cast<const float4 *>(sl + 128 + c0 + col);
                     const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
                     const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
                     float pv[4], dsv[4];
@@ -294,14 +295,14 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                     dd[(col >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                 }
             }
-            if (t + 2 < T) {   // operands of tile t+2 (issued right after this tile's dV/dK)
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 2) % kStages],
-                                                       ((t + 2) / kStages) & 1, abort_flag));
+            if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dV/dK
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
+                                                       ((t + 1) / ST) & 1, abort_flag));
                 if (!ok) break;
             }
-            tmem_st32x2_sync(tS, pp, tS + 64, dd);
+            tmem_st32x2_sync(tS, pp, tP, dd);
             tc_fence_before();
-            mbar_arrive(&bars.p_full[buf]);
+            mbar_arrive(&bars.p_full);
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
@@ -367,7 +368,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const float *__restrict__ lse, const float *__restrict__ dlt,
             float *__restrict__ dqhat, int S, int H, int G, int n_qt, unsigned int *err) {
     using C = BwdCfg<D>;
-    // TMEM columns of the resident A operands (D/2 packed columns each)
+    constexpr int ST = C::kStages;
+    // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), and the
+    // resident A operands Qhat at 384 and dO at 448 (D/2 packed columns each)
     constexpr uint32_t kTQ = 384, kTDO = 448;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
@@ -379,11 +382,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int i = n_qt - 1 - (int)(blockIdx.x / BH);   // query tile, longest first
     const int bh = blockIdx.x % BH;
     const int b = bh / H, h = bh - b * H, g = h / (H / G);
-    const int n_k64 = (S + kStream - 1) / kStream;
-    const int T = min(2 * i + 2, n_k64);               // key tiles at or before the rows
+    const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST);
     if (warp == 9) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -399,71 +401,61 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_v);
             int issued = 0;
             for (int t = 0; t < T; ++t) {
-                const int st = t % kStages;
-                if (t >= kStages &&
-                    !mbar_wait(&bars.st_empty[st], ((t / kStages) - 1) & 1, abort_flag)) {
+                const int st = t % ST;
+                if (t >= ST && !mbar_wait(&bars.st_empty[st], ((t / ST) - 1) & 1, abort_flag)) {
                     if (!*abort_flag) raise_error_b(err, abort_flag);
                     break;
                 }
                 uint8_t *base = sStage + st * C::kStageBytes;
-                mbar_expect_tx(&bars.st_full[st], 2 * C::kStreamTile);
+                mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 8192, &map_k, &bars.st_full[st], c * 64, t * kStream,
+                    tma_load_3d(base + c * 16384, &map_k, &bars.st_full[st], c * 64, t * kTile,
                                 b * G + g);
-                    tma_load_4d(base + C::kStreamTile + c * 8192, &map_v, &bars.st_full[st],
-                                c * 64, g, t * kStream, b);
+                    tma_load_4d(base + C::kTileBytes + c * 16384, &map_v, &bars.st_full[st],
+                                c * 64, g, t * kTile, b);
                 }
                 issued = t + 1;
             }
-            for (int t = max(0, issued - kStages); t < issued; ++t)
-                mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, nullptr);
+            for (int t = max(0, issued - ST); t < issued; ++t)
+                mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(kOwn, kStream, 0, 0);
-            const uint32_t idesc_acc = idesc_bf16_f32(kOwn, D, 0, 1);
-            // descriptors built once; per MMA only compile-time offsets are added
+            const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
+            const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             const uint64_t dKk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
-            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kStreamTile), 16, 1024, kSwizzle128B);
-            const uint64_t dKm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
+            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, 1024, kSwizzle128B);
+            const uint64_t dKm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
-            // S and dP of tile t into TMEM buffer t % 2
-            auto issue_sp = [&](int t) {
-                const int st = t % kStages, buf = t & 1;
-                const uint64_t so = (uint64_t)st * kStep;
+            auto issue_sp = [&](int t) {            // S = Qhat Khat^T, dP = dO V^T (A in TMEM)
+                const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {    // S = Qhat Khat^T (Qhat in TMEM)
-                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ts(tmem + 128 * buf, tmem + kTQ + kk * 8, dKk0 + so + os, idesc_s, kk > 0);
-                }
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ts(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off(kk), idesc_s, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {    // dP = dO V^T (dO in TMEM)
-                    const uint64_t os = (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-                    mma_ts(tmem + 128 * buf + 64, tmem + kTDO + kk * 8, dVk0 + so + os, idesc_s,
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off(kk), idesc_s,
                            kk > 0);
-                }
-                mma_commit(&bars.s_full[buf]);
+                mma_commit(&bars.s_full);
             };
-            // One wait per tile (dS of tile t); the softmax warps check the operands of
-            // tile t+2 before signalling, so S/dP of t+2 follow dQ of t immediately.
-            bool ok = mbar_wait(&bars.own_full, 0, abort_flag);
-            for (int t = 0; ok && t < 2 && t < T; ++t) {
-                if (!(ok = mbar_wait(&bars.st_full[t % kStages], (t / kStages) & 1, abort_flag))) break;
+            bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
+                      mbar_wait(&bars.st_full[0], 0, abort_flag);
+            if (ok) {
                 tc_fence_after();
-                issue_sp(t);
+                issue_sp(0);
             }
             for (int t = 0; ok && t < T; ++t) {
-                const int buf = t & 1, st = t % kStages;
-                if (!(ok = mbar_wait(&bars.p_full[buf], (t >> 1) & 1, abort_flag))) break;
+                const int st = t % ST;
+                if (!(ok = mbar_wait(&bars.p_full, t & 1, abort_flag))) break;
                 tc_fence_after();
                 const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
-                for (int kk = 0; kk < kStream / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts(tmem + 256, tmem + 128 * buf + kk * 8, dKm0 + so + ((kk * 2048) >> 4),
+                for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
+                    mma_ts(tmem + 256, tmem + packed_col(kk), dKm0 + so + mnmajor_off(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars.st_empty[st]);
-                if (t + 2 < T) issue_sp(t + 2);
+                if (t + 1 < T) issue_sp(t + 1);       // operands checked by the softmax warps
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -474,7 +466,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         // ------------------------------------------------------------ softmax + epilogue
         const int wg = warp >> 2, quarter = warp & 3;
         const int r = quarter * 32 + lane;             // owned query row = TMEM lane
-        const int tq = i * kOwn + r;                   // query position
+        const int tq = i * kTile + r;                  // query position
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         const float lse2 = tq < S ? lse[(size_t)bh * S + tq] * kLog2e : 0.f;
@@ -499,20 +491,21 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             mbar_arrive(&bars.own_full);
         }
         bool ok = true;
-        for (int t = wg; t < T; t += 2) {
-            const int buf = wg;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[buf], (t >> 1) & 1, abort_flag));
+        for (int t = 0; t < T; ++t) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, t & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int k0 = t * kStream;
-            const uint32_t tS = tmem + 128 * buf + lane_off;
-            // interior tile: every key of the tile is at/before every owned query
-            const bool interior = (k0 + kStream - 1 <= i * kOwn);
+            const int c0 = wg * 64;
+            const int k0 = t * kTile + c0;
+            const uint32_t tS = tmem + lane_off + c0;
+            const uint32_t tP = tmem + lane_off + 128 + c0;
+            // no masking when every key of these columns is at/before every owned query
+            const bool interior = (k0 + 63 <= i * kTile);
             uint32_t dd[32];
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                uint32_t sv[32], dpv[32];        // S and dP columns [32 hf, 32 hf + 32)
-                tmem_ld32x2_sync(tS + 32 * hf, sv, tS + 64 + 32 * hf, dpv);
+                uint32_t sv[32], dpv[32];
+                tmem_ld32x2_sync(tS + 32 * hf, sv, tP + 32 * hf, dpv);
 #pragma unroll
                 for (int e = 0; e < 32; e += 2) {
                     float dsv[2];
@@ -526,14 +519,14 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                     dd[(32 * hf + e) >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                 }
             }
-            if (t + 2 < T) {   // operands of tile t+2 (issued right after this tile's dQ)
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 2) % kStages],
-                                                       ((t + 2) / kStages) & 1, abort_flag));
+            if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dQ
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
+                                                       ((t + 1) / ST) & 1, abort_flag));
                 if (!ok) break;
             }
             tmem_st32_sync(tS, dd);
             tc_fence_before();
-            mbar_arrive(&bars.p_full[buf]);
+            mbar_arrive(&bars.p_full);
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
@@ -579,70 +572,63 @@ struct BwdMaps {
 };
 
 // Qhat [B*H, S, D] / Khat [B*G, S, D] as 3-D maps; V [B, S, G, D] and
-// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of 64 columns x rows.
+// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of 64 columns x 128 rows.
 cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, const void *v,
-                      const void *dout, int q_rows, int k_rows, BwdMaps &m) {
+                      const void *dout, BwdMaps &m) {
     const uint64_t esz = 2, D = (uint64_t)p.D;
     cudaError_t e;
     {
         const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, (uint32_t)q_rows, 1};
+        const uint32_t box[3] = {64, (uint32_t)kTile, 1};
         if ((e = encode_tmap_bf16(&m.q, qhat, 3, dims, strides, box)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.G};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, (uint32_t)k_rows, 1};
+        const uint32_t box[3] = {64, (uint32_t)kTile, 1};
         if ((e = encode_tmap_bf16(&m.k, khat, 3, dims, strides, box)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[4] = {D, (uint64_t)p.G, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.G * D * esz, (uint64_t)p.S * p.G * D * esz};
-        const uint32_t box[4] = {64, 1, (uint32_t)k_rows, 1};
+        const uint32_t box[4] = {64, 1, (uint32_t)kTile, 1};
         if ((e = encode_tmap_bf16(&m.v, v, 4, dims, strides, box)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[4] = {D, (uint64_t)p.H, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.H * D * esz, (uint64_t)p.S * p.H * D * esz};
-        const uint32_t box[4] = {64, 1, (uint32_t)q_rows, 1};
+        const uint32_t box[4] = {64, 1, (uint32_t)kTile, 1};
         if ((e = encode_tmap_bf16(&m.dout, dout, 4, dims, strides, box)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 template <int D>
-cudaError_t launch_dkdv_d(const Problem &p, const void *qhat, const void *khat, const void *v,
-                          const void *dout, const float *lse, const float *dlt, float *dkhat,
-                          void *dv, unsigned int *err, cudaStream_t st) {
+cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, const float *dlt,
+                          float *dkhat, void *dv, unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
-    BwdMaps m;
-    cudaError_t e = make_maps(p, qhat, khat, v, dout, kStream, kOwn, m);
-    if (e != cudaSuccess) return e;
-    const int n_kvt = (p.S + kOwn - 1) / kOwn;
+    const int n_kvt = (p.S + kTile - 1) / kTile;
     const long blocks = (long)p.B * p.G * n_kvt;
-    if ((e = cudaFuncSetAttribute(k_bwd_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  C::kSmemBytes)) != cudaSuccess)
-        return e;
-    k_bwd_dkdv_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemBytes, st>>>(
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemA);
+    if (e != cudaSuccess) return e;
+    k_bwd_dkdv_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
         m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, p.S, p.H, p.G, n_kvt, err);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_dq_d(const Problem &p, const void *qhat, const void *khat, const void *v,
-                        const void *dout, const float *lse, const float *dlt, float *dqhat,
-                        unsigned int *err, cudaStream_t st) {
+cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, const void *dout,
+                        const float *lse, const float *dlt, float *dqhat, unsigned int *err,
+                        cudaStream_t st) {
     using C = BwdCfg<D>;
-    BwdMaps m;
-    cudaError_t e = make_maps(p, qhat, khat, v, dout, kOwn, kStream, m);
-    if (e != cudaSuccess) return e;
-    const int n_qt = (p.S + kOwn - 1) / kOwn;
+    const int n_qt = (p.S + kTile - 1) / kTile;
     const long blocks = (long)p.B * p.H * n_qt;
-    if ((e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  C::kSmemBytes)) != cudaSuccess)
-        return e;
-    k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemBytes - 2 * C::kOwnTile, st>>>(
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemB);
+    if (e != cudaSuccess) return e;
+    k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
         m.k, m.v, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, dqhat, p.S, p.H, p.G, n_qt, err);
     return cudaGetLastError();
 }
@@ -653,16 +639,22 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *k
                                const void *v, const void *dout, const float *lse,
                                const float *dlt, float *dkhat, void *dv, unsigned int *err,
                                cudaStream_t st) {
-    if (p.D == 128) return launch_dkdv_d<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
-    if (p.D == 64) return launch_dkdv_d<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
+    BwdMaps m;
+    cudaError_t e = make_maps(p, qhat, khat, v, dout, m);
+    if (e != cudaSuccess) return e;
+    if (p.D == 128) return launch_dkdv_d<128>(p, m, lse, dlt, dkhat, dv, err, st);
+    if (p.D == 64) return launch_dkdv_d<64>(p, m, lse, dlt, dkhat, dv, err, st);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                              const void *dout, const float *lse, const float *dlt, float *dqhat,
                              unsigned int *err, cudaStream_t st) {
-    if (p.D == 128) return launch_dq_d<128>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
-    if (p.D == 64) return launch_dq_d<64>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
+    BwdMaps m;
+    cudaError_t e = make_maps(p, qhat, khat, v, dout, m);
+    if (e != cudaSuccess) return e;
+    if (p.D == 128) return launch_dq_d<128>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
+    if (p.D == 64) return launch_dq_d<64>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
     return cudaErrorInvalidValue;
 }
 
