@@ -52,6 +52,9 @@ def lib():
     L.xt_attn_bwd.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, i, vp, vp, vp, vp, vp, vp,
                               vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.xt_attn_bwd.restype = i
+    L.xt_attn_bwd_noalloc.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
+                                      vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    L.xt_attn_bwd_noalloc.restype = i
     L.xt_attn_check.argtypes = [vp]
     L.xt_attn_check.restype = i
     L.xt_status_str.argtypes = [i]
@@ -157,6 +160,31 @@ def xt_attn_bwd(q, k, v, gamma_q, gamma_k, saved, dout, eps, theta, *, dq=None, 
                            wbytes, _stream(stream))
     if st != XT_OK:
         raise XtError(st, "xt_attn_bwd")
+    return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
+
+
+def xt_attn_bwd_noalloc(q, k, v, gamma_q, gamma_k, saved, dout, eps, theta, *, dq=None, dk=None,
+                        dv=None, dgamma_q=None, dgamma_k=None, stream=None):
+    """xt_attn_bwd without a workspace: the library's fixed 16 MiB device array is
+    its scratch (for callers that cannot allocate). Outputs are the caller's,
+    allocated here only when not passed in. Raises XtError(XT_EWORKSPACE) for
+    problems that need more scratch than the array holds."""
+    B, S, H, D = q.shape
+    G = k.shape[2]
+    dev = q.device
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    dgamma_q = dgamma_q if dgamma_q is not None else torch.empty(D, device=dev, dtype=torch.float32)
+    dgamma_k = dgamma_k if dgamma_k is not None else torch.empty(D, device=dev, dtype=torch.float32)
+    st = lib().xt_attn_bwd_noalloc(B, S, H, G, D, float(eps), float(theta), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _dtype_code(q.dtype),
+                                   _ptr(saved["out"]), _ptr(saved["lse"]), _ptr(saved["q_hat"]),
+                                   _ptr(saved["k_hat"]), _ptr(saved["rstd_q"]),
+                                   _ptr(saved["rstd_k"]), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                                   _ptr(dgamma_q), _ptr(dgamma_k), _stream(stream))
+    if st != XT_OK:
+        raise XtError(st, "xt_attn_bwd_noalloc")
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
 
 

@@ -106,6 +106,33 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                 void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
                 void *workspace, size_t workspace_bytes, void *stream);
 
+/* Backward without a workspace: identical in arguments and results to
+ * xt_attn_bwd, but its scratch memory is a fixed 16 MiB array that this
+ * library keeps in device memory (no counterpart on the pages: it exists for
+ * callers that cannot allocate device memory themselves, e.g. a host
+ * application whose own memory pool exposes no allocation hook to plugins, or
+ * a latency-critical loop where cudaMalloc is not allowed). The call itself
+ * allocates and frees nothing.
+ *  - Limit: problems whose xt_attn_workspace_bytes(..., backward=1) exceeds
+ *    16 MiB (16777216 bytes) are refused with XT_EWORKSPACE before any launch.
+ *  - Every GPU that loads the library holds the 16 MiB array until the
+ *    process exits.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, on the current device); make that first call
+ *    before any stream capture begins.
+ *  - All calls share the one array, which keeps the previous call's contents
+ *    (the backward writes every scratch byte it reads, so nothing needs
+ *    clearing). Calls whose GPU work overlaps in time -- on different streams,
+ *    or from different host threads -- race on the array: serialize them. */
+int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                        double eps, double theta,
+                        const void *q, const void *k, const void *v,
+                        const float *gamma_q, const float *gamma_k, int dtype,
+                        const void *out, const float *lse, const void *q_hat, const void *k_hat,
+                        const float *rstd_q, const float *rstd_k, const void *dout,
+                        void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
+                        void *stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the
  * current device: XT_OK, XT_ETIMEOUT (a bounded wait ran out) or XT_ECUDA. */
 int xt_attn_check(void *stream);
