@@ -246,7 +246,8 @@ def bench_ours(args, w):
     def step():
         xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
                        out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
-                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"])
+                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"],
+                       workspace=ws)
         xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
                        w.eps, w.theta, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
                        dgamma_q=grads["dgamma_q"], dgamma_k=grads["dgamma_k"], workspace=ws)
@@ -254,7 +255,8 @@ def bench_ours(args, w):
     def fwd_only():
         xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
                        out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
-                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"])
+                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"],
+                       workspace=ws)
 
     def bwd_only():
         xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],

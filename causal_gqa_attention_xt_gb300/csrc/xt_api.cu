@@ -42,7 +42,8 @@ struct Timing {
 const char *kKernelNames[KID_COUNT] = {
     "prologue_qknorm_rope", "fwd_simt_f32", "fwd_tcgen05_bf16", "bwd_pre_dlt",
     "bwd_dq_simt_f32",      "bwd_dkdv_simt_f32", "bwd_dq_tcgen05_bf16",
-    "bwd_dkdv_tcgen05_bf16", "bwd_epilogue_rope_norm", "bwd_dgamma_reduce"};
+    "bwd_dkdv_tcgen05_bf16", "bwd_epilogue_rope_norm", "bwd_dgamma_reduce",
+    "rope_table"};
 
 void drain_locked() {
     for (auto &p : g_timing.pending) {
@@ -110,20 +111,24 @@ int validate_scalars(double eps, double theta) {
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
+// Forward scratch: the RoPE cos/sin table.
+size_t fwd_workspace(const Problem &p) { return align_up(rope_table_bytes(p)); }
+
+// Backward scratch: the RoPE cos/sin table, Dlt, fp32 dQhat and dKhat, and the
+// epilogue's per-CTA dgamma partials (at most kMaxNormParts rows each).
 struct BwdWorkspace {
-    size_t off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, total;
-    int nparts;
+    size_t off_tab, off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, total;
 };
 
 BwdWorkspace bwd_layout(const Problem &p) {
-    BwdWorkspace w;
+    BwdWorkspace w = {};
     size_t o = 0;
+    w.off_tab = o;    o = align_up(o + rope_table_bytes(p));
     w.off_dlt = o;    o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S);
     w.off_dqhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S * p.D);
     w.off_dkhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.G * p.S * p.D);
-    w.nparts = normrope_blocks(p);
-    w.off_part_q = o; o = align_up(o + sizeof(float) * (size_t)w.nparts * p.D);
-    w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)w.nparts * p.D);
+    w.off_part_q = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
+    w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
     w.total = o;
     return w;
 }
@@ -160,8 +165,8 @@ extern "C" {
 size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                                int dtype, int backward) {
     if (validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
-    if (!backward) return 0;
-    return bwd_layout(make_problem(B, S, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype)).total;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype);
+    return backward ? bwd_layout(p).total : fwd_workspace(p);
 }
 
 int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
@@ -175,16 +180,21 @@ int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     const void *ptrs[] = {q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k};
     for (const void *ptr : ptrs)
         if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
-    (void)workspace; (void)workspace_bytes;
     const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < fwd_workspace(p))
+        return XT_EWORKSPACE;
+    void *tab = workspace;
     cudaStream_t s = (cudaStream_t)stream;
+    unsigned int *err = error_word_ptr();
+    if (!err) return cuda_fail(cudaGetLastError());
+    st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, s); });
+    if (st != XT_OK) return st;
     st = timed_launch(KID_PROLOGUE, s, [&] {
-        return launch_prologue(p, q, k, gamma_q, gamma_k, q_hat, k_hat, rstd_q, rstd_k, s);
+        return launch_prologue(p, q, k, gamma_q, gamma_k, tab, q_hat, k_hat, rstd_q, rstd_k, err,
+                               s);
     });
     if (st != XT_OK) return st;
     if (dtype == XT_BF16) {
-        unsigned int *err = error_word_ptr();
-        if (!err) return cuda_fail(cudaGetLastError());
         return timed_launch(KID_FWD_TC, s, [&] {
             return launch_fwd_tc(p, q_hat, k_hat, v, out, lse, err, s);
         });
@@ -213,18 +223,23 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < w.total)
         return XT_EWORKSPACE;
     char *ws = (char *)workspace;
+    void *tab = ws + w.off_tab;
     float *dlt = (float *)(ws + w.off_dlt);
     float *dqhat = (float *)(ws + w.off_dqhat);
     float *dkhat = (float *)(ws + w.off_dkhat);
     float *part_q = (float *)(ws + w.off_part_q);
     float *part_k = (float *)(ws + w.off_part_k);
     cudaStream_t s = (cudaStream_t)stream;
+    unsigned int *err = error_word_ptr();
+    if (!err) return cuda_fail(cudaGetLastError());
 
-    st = timed_launch(KID_BWD_PRE, s, [&] { return launch_bwd_pre(p, out, dout, dlt, s); });
+    st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, s); });
+    if (st != XT_OK) return st;
+    st = timed_launch(KID_BWD_PRE, s, [&] {
+        return launch_bwd_pre(p, out, dout, dlt, err, s);
+    });
     if (st != XT_OK) return st;
     if (dtype == XT_BF16) {
-        unsigned int *err = error_word_ptr();
-        if (!err) return cuda_fail(cudaGetLastError());
         st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
             return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, err, s);
         });
@@ -243,13 +258,14 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
         });
         if (st != XT_OK) return st;
     }
+    int nparts = 0;
     st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
-        return launch_epilogue(p, dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q, rstd_k, dq, dk,
-                               part_q, part_k, s);
+        return launch_epilogue(p, dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q, rstd_k, tab, dq,
+                               dk, part_q, part_k, &nparts, err, s);
     });
     if (st != XT_OK) return st;
     return timed_launch(KID_DGAMMA_REDUCE, s, [&] {
-        return launch_dgamma_reduce(p, part_q, part_k, w.nparts, dgamma_q, dgamma_k, s);
+        return launch_dgamma_reduce(p, part_q, part_k, nparts, nparts, dgamma_q, dgamma_k, s);
     });
 }
 

@@ -22,6 +22,7 @@ enum KernelId {
     KID_BWD_DKDV_TC,      // bf16 tcgen05 dKhat, dV (group sum in-block)
     KID_BWD_EPILOGUE,     // RoPE^-1 + RMSNorm backward, dgamma partials
     KID_DGAMMA_REDUCE,    // fixed-order sum of dgamma partials
+    KID_ROPE_TABLE,       // cos/sin table of the RoPE angles
     KID_COUNT
 };
 
@@ -33,34 +34,31 @@ struct Problem {
     int group() const { return H / G; }
 };
 
-// RoPE inverse frequencies theta^(-2i/D), i < D/2, formed on the host in
-// double and passed to the norm/RoPE kernels by value.
-constexpr int kMaxHalfDim = 64;
-struct RopeFreqs {
-    double inv_freq[kMaxHalfDim];
-};
-RopeFreqs rope_freqs(const Problem &p);
-
 // Error word bits raised by kernels whose bounded waits run out.
 enum : unsigned int { ERR_TIMEOUT = 1u };
 
 // ---- norm / RoPE kernels (xt_normrope.cu) ----
-// Rows of positions handled by one prologue / epilogue block.
-constexpr int kRowsPerBlock = 16;
-inline int normrope_blocks(const Problem &p) {
-    return ((p.S + kRowsPerBlock - 1) / kRowsPerBlock) * p.B;
-}
+// Persistent grids: at most this many CTAs, which bounds the number of
+// per-CTA dgamma partials the backward epilogue writes.
+constexpr int kMaxNormParts = 1024;
+// cos/sin table [S][D/2] of (cos, sin) float pairs, filled by launch_rope_table
+// and read by the prologue and the epilogue.
+size_t rope_table_bytes(const Problem &p);
+cudaError_t launch_rope_table(const Problem &p, void *tab, cudaStream_t st);
 cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, const float *gq,
-                            const float *gk, void *qhat, void *khat, float *rstd_q,
-                            float *rstd_k, cudaStream_t st);
+                            const float *gk, const void *tab, void *qhat, void *khat,
+                            float *rstd_q, float *rstd_k, unsigned int *err, cudaStream_t st);
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, float *dlt,
-                           cudaStream_t st);
+                           unsigned int *err, cudaStream_t st);
+// Writes the number of dgamma partial rows it produced (<= kMaxNormParts) to *nparts.
 cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *dkhat,
                             const void *q, const void *k, const float *gq, const float *gk,
-                            const float *rstd_q, const float *rstd_k, void *dq, void *dk,
-                            float *part_q, float *part_k, cudaStream_t st);
+                            const float *rstd_q, const float *rstd_k, const void *tab, void *dq,
+                            void *dk, float *part_q, float *part_k, int *nparts,
+                            unsigned int *err, cudaStream_t st);
 cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
-                                 int nparts, float *dgq, float *dgk, cudaStream_t st);
+                                 int nparts_q, int nparts_k, float *dgq, float *dgk,
+                                 cudaStream_t st);
 
 // ---- TMA tensor maps (xt_tmap.cu) ----
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,

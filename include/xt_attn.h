@@ -75,15 +75,18 @@ typedef enum {
 } xt_status;
 
 /* Bytes of scratch the forward (backward = 0) or backward (backward != 0)
- * call needs for this problem; 0 on invalid arguments or when none is
- * needed. */
+ * call needs for this problem; 0 on invalid arguments. The forward's scratch
+ * is the RoPE table, S * head_dim/2 (cos, sin) fp32 pairs (rounded up to 256
+ * bytes); the backward's holds that table too, plus Dlt [B, H, S], fp32 dQhat
+ * and dKhat, and 2 * 1024 * head_dim floats of dgamma partials. */
 size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                                int dtype, int backward);
 
 /* Forward: out = causal GQA SDPA(rope(norm(q)), rope(norm(k)), v) with scale
  * 1/sqrt(head_dim). Also writes what the backward needs: lse, q_hat, k_hat,
  * rstd_q, rstd_k. `eps` is the RMSNorm epsilon (added to mean(x^2) inside the
- * square root), `theta` the RoPE base. */
+ * square root), `theta` the RoPE base. `workspace` must hold at least
+ * xt_attn_workspace_bytes(..., backward = 0) bytes (else XT_EWORKSPACE). */
 int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                 double eps, double theta,
                 const void *q, const void *k, const void *v,

@@ -66,11 +66,21 @@ def test_forward_validation_rejects_before_launch(L, kw, code):
     assert _fwd(L, **kw) == code
 
 
+def test_forward_needs_its_workspace(L):
+    p = ctypes.c_void_p(16)
+    need = xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, False)
+    args = [1, 16, 2, 2, 16, 1e-5, 1e4] + [p] * 5 + [0] + [p] * 6
+    assert L.xt_attn_fwd(*args, None, need, None) == xt.XT_EWORKSPACE
+    assert L.xt_attn_fwd(*args, p, need - 1, None) == xt.XT_EWORKSPACE
+    assert L.xt_attn_fwd(*args, ctypes.c_void_p(24), need, None) == xt.XT_EWORKSPACE
+
+
 def test_backward_validation_and_workspace(L):
     p = ctypes.c_void_p(16)
     need = xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, True)
     assert need > 0 and need % 256 == 0
-    assert xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, False) == 0
+    fneed = xt.xt_attn_workspace_bytes(1, 16, 2, 2, 16, 0, False)
+    assert 16 * 8 * 8 <= fneed <= need   # the [S][D/2] (cos, sin) table; the backward holds it too
     assert xt.xt_attn_workspace_bytes(1, 16, 3, 2, 16, 0, True) == 0
     args = [1, 16, 2, 2, 16, 1e-5, 1e4] + [p] * 5 + [0] + [p] * 7 + [p] * 5
     assert L.xt_attn_bwd(*args, p, need - 1, None) == xt.XT_EWORKSPACE
