@@ -15,20 +15,21 @@
 // backward, dgamma summed over rows); xtrain "Phase T12: bf16 mixed
 // precision" (norm and RoPE computed in fp32 on bf16 activations).
 //
-// Data movement. The three row kernels are persistent grids (two CTAs per
-// SM) that walk "units": P consecutive positions of one batch element times a
-// chunk of HC heads, all q heads or all k heads. P makes a head's run in the
-// [B, heads, S, D] tensors about kRunBytes long, HC fills the stage budget.
-// A producer warp copies each unit's inputs -- one run per position from the
-// [B, S, heads, D] tensors, one run per head from the [B, heads, S, D] ones,
-// the unit's rows of the cos/sin table -- into a ring of kStages shared-memory
-// buffers with bulk asynchronous copies (cp.async.bulk, byte count on a
-// "full" mbarrier). Eight consumer warps read the staged rows, compute in
-// fp32, store results with 16-byte stores and release the buffer on an
-// "empty" mbarrier; no CTA-wide barrier is taken per unit. A row of D
-// elements is handled by tpr lanes, each owning VEC elements of the first
-// half of the row and the VEC matching elements of the second half (the RoPE
-// pair); gamma for those elements stays in registers for the whole unit.
+// Data movement. The three row kernels are persistent grids (two CTAs of
+// eight warps per SM). Every warp runs its own pipeline over "units": one
+// position of one batch element times a chunk of HC heads, all q heads or all
+// k heads (for bwd_pre: of O and dO). Warp w of the grid takes units w,
+// w + W, w + 2W, ... (W = warps in the grid). A unit's inputs are a few
+// contiguous runs of global memory -- the chunk's rows from the
+// [B, S, heads, D] tensors, one row per head from the [B, heads, S, D] ones,
+// the position's cos/sin row, the rows' rstd words -- which the warp's lanes
+// copy with bulk asynchronous copies (cp.async.bulk; 4-byte cp.async for the
+// rstd words) into one of its NS shared-memory stages, completion counted on
+// that stage's mbarrier. While the warp computes one unit from shared memory,
+// the copies of its next NS - 1 units are in flight; no barrier couples the
+// warps. A row of D elements is handled by tpr lanes, each owning VEC
+// elements of the first half of the row and the VEC matching elements of the
+// second half (the RoPE pair); a warp-iteration covers 32 / tpr heads.
 //
 // RoPE angles (rope_table): for positions below 2^21 the product pos * f is
 // formed in fp32 with f = theta^(-2i/D) split as hi + lo and the rounding
@@ -47,18 +48,13 @@ namespace {
 using tc::bulk_load;
 using tc::cp_async4;
 using tc::cp_async_mbar_arrive;
-using tc::mbar_arrive;
 using tc::mbar_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
 
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = 32 * kConsumerWarps;
-constexpr int kThreads = kConsumers + 32;    // + the producer warp
-constexpr int kStages = 3;                   // ring depth
+constexpr int kWarps = 8;                    // warps per CTA, each its own pipeline
+constexpr int kThreads = 32 * kWarps;
 constexpr int kCtasPerSm = 2;
-constexpr size_t kStageBudget = 28 * 1024;   // staged bytes per unit (rows + table)
-constexpr size_t kRunBytes = 2048;           // target run per head in [B, heads, S, D]
 constexpr int kRopeFp32Limit = 1 << 21;      // positions with the fp32 angle path
 
 // 2*pi = kC1 + kC2 + kC3 (Cody-Waite): kC1 has 5 significant bits, so k * kC1
@@ -78,6 +74,25 @@ __host__ __device__ inline int pow2_at_least(int x) {
 constexpr size_t align128(size_t x) { return (x + 127) & ~(size_t)127; }
 constexpr size_t align16(size_t x) { return (x + 15) & ~(size_t)15; }
 
+// n / d for 0 <= n < 2^31 by a multiply-high and a shift (Granlund and
+// Montgomery, division by run-time invariant integers, round-up multiplier).
+struct FastDiv {
+    uint32_t d, m, s;
+};
+
+FastDiv make_fastdiv(uint32_t d) {
+    FastDiv f;
+    f.d = d;
+    f.s = 0;
+    while ((1ull << f.s) < d) ++f.s;
+    f.m = (uint32_t)((((1ull << 32) * ((1ull << f.s) - d)) / d) + 1);
+    return f;
+}
+
+__device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
+    return (__umulhi(f.m, n) + n) >> f.s;
+}
+
 // ---------------------------------------------------------------- RoPE table
 // Inverse frequencies theta^(-2i/D), formed on the host in double; fhi + flo
 // is that double to ~48 bits.
@@ -90,6 +105,14 @@ struct RopeConsts {
 // tab[s * half + i] = (cos, sin) of s * theta^(-2i/D), s < S, i < half.
 __global__ void __launch_bounds__(256)
 k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ RopeConsts rc) {
+    __shared__ float fhi[kMaxHalf], flo[kMaxHalf];
+    __shared__ double fd[kMaxHalf];
+    for (int i = threadIdx.x; i < half; i += blockDim.x) {
+        fhi[i] = rc.fhi[i];
+        flo[i] = rc.flo[i];
+        fd[i] = rc.fd[i];
+    }
+    __syncthreads();
     const long n = (long)S * half;
     for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long)gridDim.x * blockDim.x) {
@@ -97,15 +120,15 @@ k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ 
         float red;
         if (s < kRopeFp32Limit) {
             const float fs = (float)s;   // exact
-            const float hi = rc.fhi[i];
+            const float hi = fhi[i];
             const float p = __fmul_rn(fs, hi);
-            const float tail = fmaf(fs, rc.flo[i], fmaf(fs, hi, -p));   // s * f - p
+            const float tail = fmaf(fs, flo[i], fmaf(fs, hi, -p));   // s * f - p
             const float k = rintf(p * kInvTwoPi);
             float r = fmaf(-k, kC1, p);   // exact
             r = fmaf(-k, kC2, r);
             red = __fadd_rn(r, fmaf(-k, kC3, tail));
         } else {
-            const double ang = (double)s * rc.fd[i];
+            const double ang = (double)s * fd[i];
             red = (float)fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
         }
         float sv, cv;
@@ -115,106 +138,82 @@ k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ 
 }
 
 // ---------------------------------------------------------------- units
-// How the rows of a problem are cut into units.
+// Units: u = (b * S + s) * (nqc + nkc) + chunk; chunk < nqc are q-head chunks
+// of HC heads, the rest k-head chunks.
 struct UnitGeo {
-    int P;            // positions per unit
-    int HC;           // heads per unit (all q or all k)
-    int nsb;          // position blocks per batch element
-    int nqc, nkc;     // head chunks over the q heads and over the k heads
-    int units;        // B * nsb * (nqc + nkc)
-    int y_off;        // ring-buffer offset of the second input
-    int r_off;        // ring-buffer offset of the staged rstd values
-    int t_off;        // ring-buffer offset of the cos/sin rows
-    int stage_bytes;  // one ring buffer
+    int HC;           // heads per unit
+    int nqc, nkc;     // chunks over the q heads and over the k heads
+    int units;        // B * S * (nqc + nkc)
+    FastDiv fd_chunks, fd_S;
+    int y_off;        // stage offset of the second input's rows
+    int r_off;        // stage offset of the rstd words
+    int t_off;        // stage offset of the cos/sin row
+    int stage_bytes;
 };
 
 struct Unit {
-    int b, s0, np;    // batch element, first position, number of positions
+    int b, s;         // batch element, position
     int h0, nh;       // heads [h0, h0 + nh) of q (isq) or of k
     bool isq;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const UnitGeo &g, int S, int H, int G) {
+__device__ __forceinline__ Unit decode_unit(uint32_t u, const UnitGeo &g, int H, int G) {
     Unit t;
-    const int nhc = g.nqc + g.nkc;
-    const int ch = u % nhc;
-    const int r = u / nhc;
-    const int sb = r % g.nsb;
-    t.b = r / g.nsb;
-    t.s0 = sb * g.P;
-    t.np = min(g.P, S - t.s0);
+    const uint32_t bs = fdiv(u, g.fd_chunks);
+    const int ch = (int)(u - bs * (uint32_t)(g.nqc + g.nkc));
+    t.b = (int)fdiv(bs, g.fd_S);
+    t.s = (int)(bs - (uint32_t)t.b * g.fd_S.d);
     t.isq = ch < g.nqc;
     t.h0 = (t.isq ? ch : ch - g.nqc) * g.HC;
     t.nh = min(g.HC, (t.isq ? H : G) - t.h0);
     return t;
 }
 
-// Shared memory: [RingCtl][ring: kStages buffers]
-struct alignas(16) RingCtl {
-    uint64_t full[kStages];    // producer's copies landed (1 arrival + bytes)
-    uint64_t empty[kStages];   // consumer warps done with the buffer (kConsumerWarps)
-    int abort_flag;
-};
-
-__device__ __forceinline__ void ring_init(RingCtl *c) {
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < kStages; ++st) {
-            mbar_init(&c->full[st], 1);
-            mbar_init(&c->empty[st], kConsumerWarps);
-        }
-        c->abort_flag = 0;
-        tc::fence_barrier_init();
-    }
-    __syncthreads();
-}
-
-__device__ __forceinline__ void raise_timeout(RingCtl *c, unsigned int *err) {
-    atomicOr(err, ERR_TIMEOUT);
-    *(volatile int *)&c->abort_flag = 1;
-}
-
-// Producer warp: units blockIdx.x, blockIdx.x + gridDim.x, ... ; issue(u, buf,
-// bar) is run by all 32 lanes and starts the copies of unit u into buf.
-template <class Issue>
-__device__ void produce(RingCtl *c, unsigned char *ring, int stage_bytes, int units,
-                        unsigned int *err, Issue issue) {
+// Per-warp pipeline over units first, first + stride, ... < units through NS
+// stages of `stage_bytes` at `ring`, with one mbarrier per stage in `full`.
+// issue(u, buf, bar) is run by all 32 lanes and starts the copies of unit u;
+// process(u, buf) computes it once they have landed. Returns false if a wait
+// ran out (the error word is raised and the copies in flight are let land).
+template <int NS, class Issue, class Process>
+__device__ bool warp_pipeline(uint64_t *full, unsigned char *ring, int stage_bytes, uint32_t first,
+                              uint32_t stride, uint32_t units, unsigned int *err, Issue issue,
+                              Process process) {
     const int lane = threadIdx.x & 31;
-    int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-        const int st = it % kStages;
-        if (it >= kStages) {
-            const bool ok = mbar_wait(&c->empty[st], (uint32_t)(((it / kStages) - 1) & 1),
-                                      &c->abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) {
-                if (lane == 0 && !*(volatile int *)&c->abort_flag) raise_timeout(c, err);
-                break;
-            }
-        }
-        issue(u, ring + (size_t)st * stage_bytes, &c->full[st]);
+    if (lane == 0)
+        for (int k = 0; k < NS; ++k) mbar_init(&full[k], 1);
+    __syncwarp();
+    if (lane == 0) tc::fence_barrier_init();
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+        const uint32_t u = first + k * stride;
+        if (u < units) issue(u, ring + (size_t)k * stage_bytes, &full[k]);
     }
-    // After an abort, let the copies still in flight land before the CTA exits.
-    if (lane == 0 && *(volatile int *)&c->abort_flag)
-        for (int k = 1; k <= kStages && it - k >= 0; ++k)
-            mbar_wait(&c->full[(it - k) % kStages], (uint32_t)(((it - k) / kStages) & 1), nullptr);
-}
-
-// Consumer warps: process(u, buf) on every unit of this CTA, then release.
-template <class Process>
-__device__ void consume(RingCtl *c, unsigned char *ring, int stage_bytes, int units,
-                        unsigned int *err, Process process) {
-    const int lane = threadIdx.x & 31;
     int it = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++it) {
-        const int st = it % kStages;
-        const bool ok = mbar_wait(&c->full[st], (uint32_t)((it / kStages) & 1), &c->abort_flag);
+    for (uint32_t u = first; u < units; u += stride, ++it) {
+        const int st = it % NS;
+        const bool ok = mbar_wait(&full[st], (uint32_t)((it / NS) & 1), nullptr);
         if (!__all_sync(0xffffffffu, ok)) {
-            if (lane == 0 && !*(volatile int *)&c->abort_flag) raise_timeout(c, err);
-            break;
+            if (lane == 0) {
+                atomicOr(err, ERR_TIMEOUT);
+                for (int k = 0; k < NS; ++k)
+                    if (u + k * stride < units)
+                        mbar_wait(&full[(it + k) % NS], (uint32_t)(((it + k) / NS) & 1), nullptr);
+            }
+            __syncwarp();
+            return false;
         }
         process(u, ring + (size_t)st * stage_bytes);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&c->empty[st]);
+        const uint32_t un = u + NS * stride;
+        if (un < units) {
+            // the reads of this stage (generic proxy) come before the copies
+            // that overwrite it (async proxy)
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(un, ring + (size_t)st * stage_bytes, &full[st]);
+        }
     }
+    return true;
 }
 
 template <int N>
@@ -235,7 +234,7 @@ __device__ __forceinline__ void ldg_f32(const float *p, float *dst) {
     }
 }
 
-// cos/sin of the N pairs starting at tb (N even): c[e], s[e].
+// cos/sin of the N pairs starting at tb (N even): cv[e], sv[e].
 template <int N>
 __device__ __forceinline__ void load_cs(const float2 *tb, float *cv, float *sv) {
 #pragma unroll
@@ -245,26 +244,14 @@ __device__ __forceinline__ void load_cs(const float2 *tb, float *cv, float *sv) 
     }
 }
 
-// Copies of a unit's x rows from a [B, S, heads, D] tensor (one run of nh rows
-// per position, into buf rows [pos][lh]) and of its cos/sin rows; copy j is
-// issued by lane j % 32.
-template <typename T>
-__device__ __forceinline__ void issue_x_and_table(const Unit &t, const T *x, int S, int NH,
-                                                  int D, const float2 *tab, int t_off,
-                                                  unsigned char *buf, uint64_t *bar, int lane) {
-    const uint32_t xrow = (uint32_t)D * sizeof(T);
-    const uint32_t trow = (uint32_t)(D / 2) * sizeof(float2);
-    for (int j = lane; j <= t.np; j += 32) {
-        if (j < t.np)
-            bulk_load(buf + (size_t)j * t.nh * xrow,
-                      x + (((size_t)t.b * S + t.s0 + j) * NH + t.h0) * D, t.nh * xrow, bar);
-        else
-            bulk_load(buf + t_off, tab + (size_t)t.s0 * (D / 2), t.np * trow, bar);
-    }
-}
+// Shared memory of a CTA: [kWarps * NS mbarriers][kWarps rings of NS stages]
+template <int NS>
+constexpr size_t ring_offset() { return align128(sizeof(uint64_t) * kWarps * NS); }
 
 // ---------------------------------------------------------------- prologue
 // q_hat = rope(rmsnorm(q) * gamma_q), k_hat likewise; rstd saved.
+constexpr int kStagesPro = 3;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__restrict__ gq,
@@ -272,151 +259,139 @@ k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__rest
            T *__restrict__ khat, float *__restrict__ rstd_q, float *__restrict__ rstd_k, int S,
            int H, int G, int D, float eps, const UnitGeo geo, unsigned int *err) {
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int NS = kStagesPro;
     extern __shared__ __align__(128) unsigned char smem[];
-    RingCtl *ctl = reinterpret_cast<RingCtl *>(smem);
-    unsigned char *ring = smem + align128(sizeof(RingCtl));
-    ring_init(ctl);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem) + warp * NS;
+    unsigned char *ring = smem + ring_offset<NS>() + (size_t)warp * NS * geo.stage_bytes;
     const int half = D / 2;
     const uint32_t xrow = (uint32_t)D * sizeof(T);
-
-    if (threadIdx.x >= kConsumers) {
-        const int lane = threadIdx.x & 31;
-        produce(ctl, ring, geo.stage_bytes, geo.units, err,
-                [&](int u, unsigned char *buf, uint64_t *bar) {
-                    const Unit t = decode_unit(u, geo, S, H, G);
-                    if (lane == 0)
-                        mbar_expect_tx(bar, (uint32_t)(t.np * t.nh) * xrow +
-                                                (uint32_t)t.np * half * sizeof(float2));
-                    __syncwarp();
-                    issue_x_and_table<T>(t, t.isq ? q : k, S, t.isq ? H : G, D, tab, geo.t_off,
-                                         buf, bar, lane);
-                });
-        return;
-    }
-
+    const uint32_t trow = (uint32_t)half * sizeof(float2);
     const int chunks = half / VEC;
     const int tpr = pow2_at_least(chunks);
-    const int c = threadIdx.x & (tpr - 1);
-    const int slot = threadIdx.x / tpr, nslots = kConsumers / tpr;
+    const int c = lane & (tpr - 1);
+    const int sub = lane / tpr, rpi = 32 / tpr;   // row within an iteration, rows per iteration
     const bool lane_has = c < chunks;
+    const int cc = lane_has ? c : 0;              // clamped column group for the loads
     const float inv_d = 1.0f / (float)D;
 
-    consume(ctl, ring, geo.stage_bytes, geo.units, err, [&](int u, const unsigned char *buf) {
-        const Unit t = decode_unit(u, geo, S, H, G);
-        const int NH = t.isq ? H : G;
-        float glo[VEC], ghi[VEC];
-        if (lane_has) {
-            const float *gamma = t.isq ? gq : gk;
-            ldg_f32<VEC>(gamma + c * VEC, glo);
-            ldg_f32<VEC>(gamma + half + c * VEC, ghi);
+    auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
+        const Unit t = decode_unit(u, geo, H, G);
+        const uint32_t xb = (uint32_t)t.nh * xrow;
+        if (lane == 0) {
+            mbar_expect_tx(bar, xb + trow);
+            const T *x = t.isq ? q + (((size_t)t.b * S + t.s) * H + t.h0) * D
+                               : k + (((size_t)t.b * S + t.s) * G + t.h0) * D;
+            bulk_load(buf, x, xb, bar);
+            bulk_load(buf + geo.t_off, tab + (size_t)t.s * half, trow, bar);
         }
-        T *obase = (t.isq ? qhat : khat) + (((size_t)t.b * NH + t.h0) * S + t.s0) * D;
-        float *rbase = (t.isq ? rstd_q : rstd_k) + ((size_t)t.b * S + t.s0) * NH + t.h0;
-        const float2 *tb0 = reinterpret_cast<const float2 *>(buf + geo.t_off) + c * VEC;
-        const int nrows = t.np * t.nh;
-        const int lim = ((nrows + nslots - 1) / nslots) * nslots;   // warp-uniform trip count
-        int pos = slot / t.nh, lh = slot - pos * t.nh;
-        const int dpos = nslots / t.nh, dlh = nslots - dpos * t.nh;
-        for (int rr = slot; rr < lim; rr += nslots) {
-            const bool row_ok = rr < nrows;
-            const bool lane_ok = row_ok && lane_has;
+    };
+    auto process = [&](uint32_t u, const unsigned char *buf) {
+        const Unit t = decode_unit(u, geo, H, G);
+        const int NH = t.isq ? H : G;
+        float glo[VEC], ghi[VEC], cv[VEC], sv[VEC];
+        const float *gamma = t.isq ? gq : gk;
+        ldg_f32<VEC>(gamma + cc * VEC, glo);
+        ldg_f32<VEC>(gamma + half + cc * VEC, ghi);
+        load_cs<VEC>(reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC, cv, sv);
+        T *obase = (t.isq ? qhat : khat) + (((size_t)t.b * NH + t.h0) * S + t.s) * D;
+        float *rbase = (t.isq ? rstd_q : rstd_k) + ((size_t)t.b * S + t.s) * NH + t.h0;
+        for (int lh0 = 0; lh0 < t.nh; lh0 += rpi) {
+            const int lh = lh0 + sub;
+            const bool ok = lh < t.nh && lane_has;
+            const T *x = reinterpret_cast<const T *>(buf + (size_t)min(lh, t.nh - 1) * xrow);
             float lo[VEC], hi[VEC];
-            float ss = 0.f;
-            if (lane_ok) {
-                const T *x = reinterpret_cast<const T *>(buf + (size_t)rr * xrow);
-                load16<T>(x + c * VEC, lo);
-                load16<T>(x + half + c * VEC, hi);
+            load16<T>(x + cc * VEC, lo);
+            load16<T>(x + half + cc * VEC, hi);
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) ss = fmaf(lo[e], lo[e], fmaf(hi[e], hi[e], ss));
+            for (int e = 0; e < VEC; e += 2) {
+                s0 = fmaf(lo[e], lo[e], fmaf(hi[e], hi[e], s0));
+                s1 = fmaf(lo[e + 1], lo[e + 1], fmaf(hi[e + 1], hi[e + 1], s1));
             }
-            ss = group_sum(ss, tpr);
+            const float ss = group_sum(lane_has ? s0 + s1 : 0.f, tpr);
             const float r = rsqrtf(fmaf(ss, inv_d, eps));
-            if (lane_ok) {
-                float cv[VEC], sv[VEC];
-                load_cs<VEC>(tb0 + pos * half, cv, sv);
-                float olo[VEC], ohi[VEC];
+            float olo[VEC], ohi[VEC];
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float ylo = lo[e] * (r * glo[e]);
-                    const float yhi = hi[e] * (r * ghi[e]);
-                    olo[e] = ylo * cv[e] - yhi * sv[e];
-                    ohi[e] = ylo * sv[e] + yhi * cv[e];
-                }
-                T *y = obase + ((size_t)lh * S + pos) * D;
+            for (int e = 0; e < VEC; ++e) {
+                const float ylo = lo[e] * (r * glo[e]);
+                const float yhi = hi[e] * (r * ghi[e]);
+                olo[e] = ylo * cv[e] - yhi * sv[e];
+                ohi[e] = ylo * sv[e] + yhi * cv[e];
+            }
+            if (ok) {
+                T *y = obase + (size_t)lh * S * D;
                 store16<T>(y + c * VEC, olo);
                 store16<T>(y + half + c * VEC, ohi);
-                if (c == 0) rbase[(size_t)pos * NH + lh] = r;
+                if (c == 0) rbase[lh] = r;
             }
-            lh += dlh;
-            pos += dpos;
-            if (lh >= t.nh) { lh -= t.nh; ++pos; }
         }
-    });
+    };
+    const uint32_t gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+    warp_pipeline<NS>(full, ring, geo.stage_bytes, gw, nw, (uint32_t)geo.units, err, issue,
+                      process);
 }
 
 // ---------------------------------------------------------------- bwd_pre
-// Dlt[b, h, s] = sum_d dO[b, s, h, d] * O[b, s, h, d]. Units are whole
-// positions (or one position and a chunk of heads), contiguous in O and dO.
+// Dlt[b, h, s] = sum_d dO[b, s, h, d] * O[b, s, h, d].
+constexpr int kStagesPre = 3;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 k_bwd_pre(const T *__restrict__ out, const T *__restrict__ dout, float *__restrict__ dlt, int S,
           int H, int D, const UnitGeo geo, unsigned int *err) {
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int NS = kStagesPre;
     extern __shared__ __align__(128) unsigned char smem[];
-    RingCtl *ctl = reinterpret_cast<RingCtl *>(smem);
-    unsigned char *ring = smem + align128(sizeof(RingCtl));
-    ring_init(ctl);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem) + warp * NS;
+    unsigned char *ring = smem + ring_offset<NS>() + (size_t)warp * NS * geo.stage_bytes;
     const uint32_t xrow = (uint32_t)D * sizeof(T);
-
-    if (threadIdx.x >= kConsumers) {
-        const int lane = threadIdx.x & 31;
-        produce(ctl, ring, geo.stage_bytes, geo.units, err,
-                [&](int u, unsigned char *buf, uint64_t *bar) {
-                    if (lane != 0) return;
-                    const Unit t = decode_unit(u, geo, S, H, 0);
-                    const uint32_t nb = (uint32_t)(t.np * t.nh) * xrow;
-                    const size_t off = (((size_t)t.b * S + t.s0) * H + t.h0) * D;
-                    mbar_expect_tx(bar, 2 * nb);
-                    bulk_load(buf, out + off, nb, bar);
-                    bulk_load(buf + geo.y_off, dout + off, nb, bar);
-                });
-        return;
-    }
-
     const int chunks = D / VEC;
     const int tpr = pow2_at_least(chunks);
-    const int c = threadIdx.x & (tpr - 1);
-    const int slot = threadIdx.x / tpr, nslots = kConsumers / tpr;
+    const int c = lane & (tpr - 1);
+    const int sub = lane / tpr, rpi = 32 / tpr;
+    const bool lane_has = c < chunks;
+    const int cc = lane_has ? c : 0;
 
-    consume(ctl, ring, geo.stage_bytes, geo.units, err, [&](int u, const unsigned char *buf) {
-        const Unit t = decode_unit(u, geo, S, H, 0);
-        const int nrows = t.np * t.nh;
-        const int lim = ((nrows + nslots - 1) / nslots) * nslots;
-        float *dbase = dlt + ((size_t)t.b * H + t.h0) * S + t.s0;
-        int pos = slot / t.nh, lh = slot - pos * t.nh;
-        const int dpos = nslots / t.nh, dlh = nslots - dpos * t.nh;
-        for (int rr = slot; rr < lim; rr += nslots) {
-            const bool row_ok = rr < nrows;
-            float acc = 0.f;
-            if (row_ok && c < chunks) {
-                float a[VEC], g[VEC];
-                load16<T>(reinterpret_cast<const T *>(buf + (size_t)rr * xrow) + c * VEC, a);
-                load16<T>(reinterpret_cast<const T *>(buf + geo.y_off + (size_t)rr * xrow) +
-                              c * VEC, g);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) acc = fmaf(a[e], g[e], acc);
-            }
-            acc = group_sum(acc, tpr);
-            if (row_ok && c == 0) dbase[(size_t)lh * S + pos] = acc;
-            lh += dlh;
-            pos += dpos;
-            if (lh >= t.nh) { lh -= t.nh; ++pos; }
+    auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
+        const Unit t = decode_unit(u, geo, H, 0);
+        const uint32_t nb = (uint32_t)t.nh * xrow;
+        const size_t off = (((size_t)t.b * S + t.s) * H + t.h0) * D;
+        if (lane == 0) {
+            mbar_expect_tx(bar, 2 * nb);
+            bulk_load(buf, out + off, nb, bar);
+            bulk_load(buf + geo.y_off, dout + off, nb, bar);
         }
-    });
+    };
+    auto process = [&](uint32_t u, const unsigned char *buf) {
+        const Unit t = decode_unit(u, geo, H, 0);
+        float *dbase = dlt + ((size_t)t.b * H + t.h0) * S + t.s;
+        for (int lh0 = 0; lh0 < t.nh; lh0 += rpi) {
+            const int lh = lh0 + sub;
+            const size_t ro = (size_t)min(lh, t.nh - 1) * xrow;
+            float a[VEC], g[VEC];
+            load16<T>(reinterpret_cast<const T *>(buf + ro) + cc * VEC, a);
+            load16<T>(reinterpret_cast<const T *>(buf + geo.y_off + ro) + cc * VEC, g);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int e = 0; e < VEC; e += 2) {
+                a0 = fmaf(a[e], g[e], a0);
+                a1 = fmaf(a[e + 1], g[e + 1], a1);
+            }
+            const float acc = group_sum(lane_has ? a0 + a1 : 0.f, tpr);
+            if (lh < t.nh && c == 0) dbase[(size_t)lh * S] = acc;
+        }
+    };
+    const uint32_t gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+    warp_pipeline<NS>(full, ring, geo.stage_bytes, gw, nw, (uint32_t)geo.units, err, issue,
+                      process);
 }
 
 // ---------------------------------------------------------------- epilogue
 // dq = RMSNorm_bwd(RoPE_bwd(dqhat)), likewise dk; one dgamma partial per CTA.
+constexpr int kStagesEpi = 2;
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
@@ -427,132 +402,123 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
            float *__restrict__ part_k, int S, int H, int G, int D, const UnitGeo geo,
            unsigned int *err) {
     constexpr int VEC = 16 / sizeof(T);
+    constexpr int NS = kStagesEpi;
     extern __shared__ __align__(128) unsigned char smem[];
-    RingCtl *ctl = reinterpret_cast<RingCtl *>(smem);
-    unsigned char *ring = smem + align128(sizeof(RingCtl));
-    ring_init(ctl);
+    __shared__ int any_failed;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem) + warp * NS;
+    unsigned char *ring = smem + ring_offset<NS>() + (size_t)warp * NS * geo.stage_bytes;
     const int half = D / 2;
     const uint32_t xrow = (uint32_t)D * sizeof(T);
     const uint32_t yrow = (uint32_t)D * sizeof(float);
-
+    const uint32_t trow = (uint32_t)half * sizeof(float2);
     const int chunks = half / VEC;
     const int tpr = pow2_at_least(chunks);
-    const int c = threadIdx.x & (tpr - 1);
-    const int slot = threadIdx.x / tpr, nslots = kConsumers / tpr;
+    const int c = lane & (tpr - 1);
+    const int sub = lane / tpr, rpi = 32 / tpr;
     const bool lane_has = c < chunks;
+    const int cc = lane_has ? c : 0;
+    const float inv_d = 1.0f / (float)D;
+    if (threadIdx.x == 0) any_failed = 0;
     float accq[2 * VEC], acck[2 * VEC];
 #pragma unroll
     for (int e = 0; e < 2 * VEC; ++e) { accq[e] = 0.f; acck[e] = 0.f; }
 
-    // Ring buffer: x rows [pos][lh], then dyhat rows [lh][pos] (one run per
-    // head: dqhat/dkhat are [B, heads, S, D]), rstd [pos][lh], cos/sin rows.
-    if (threadIdx.x >= kConsumers) {
-        const int lane = threadIdx.x & 31;
-        produce(ctl, ring, geo.stage_bytes, geo.units, err,
-                [&](int u, unsigned char *buf, uint64_t *bar) {
-                    const Unit t = decode_unit(u, geo, S, H, G);
-                    const int NH = t.isq ? H : G;
-                    const float *rs = (t.isq ? rstd_q : rstd_k) +
-                                      ((size_t)t.b * S + t.s0) * NH + t.h0;
-                    float *rbuf = reinterpret_cast<float *>(buf + geo.r_off);
-                    for (int rr = lane; rr < t.np * t.nh; rr += 32) {
-                        const int pos = rr / t.nh;
-                        cp_async4(rbuf + rr, rs + (size_t)pos * NH + (rr - pos * t.nh));
-                    }
-                    cp_async_mbar_arrive(bar);   // one pending arrival until this lane's copies land
-                    __syncwarp();
-                    const uint32_t hb = (uint32_t)t.np * yrow;
-                    if (lane == 0)
-                        mbar_expect_tx(bar, (uint32_t)(t.np * t.nh) * xrow + (uint32_t)t.nh * hb +
-                                                (uint32_t)t.np * half * sizeof(float2));
-                    __syncwarp();
-                    issue_x_and_table<T>(t, t.isq ? q : k, S, NH, D, tab, geo.t_off, buf, bar,
-                                         lane);
-                    const float *dy = (t.isq ? dqhat : dkhat) +
-                                      (((size_t)t.b * NH + t.h0) * S + t.s0) * D;
-                    for (int lh = lane; lh < t.nh; lh += 32)
-                        bulk_load(buf + geo.y_off + (size_t)lh * hb, dy + (size_t)lh * S * D, hb,
-                                  bar);
-                });
-    } else {
-        const float inv_d = 1.0f / (float)D;
-        consume(ctl, ring, geo.stage_bytes, geo.units, err, [&](int u, const unsigned char *buf) {
-            const Unit t = decode_unit(u, geo, S, H, G);
-            const int NH = t.isq ? H : G;
-            float gml[VEC], gmh[VEC];
-            if (lane_has) {
-                const float *gamma = t.isq ? gq : gk;
-                ldg_f32<VEC>(gamma + c * VEC, gml);
-                ldg_f32<VEC>(gamma + half + c * VEC, gmh);
-            }
-            T *obase = (t.isq ? dq : dk) + (((size_t)t.b * S + t.s0) * NH + t.h0) * D;
-            const float *rbuf = reinterpret_cast<const float *>(buf + geo.r_off);
-            const float2 *tb0 = reinterpret_cast<const float2 *>(buf + geo.t_off) + c * VEC;
-            const int nrows = t.np * t.nh;
-            const int lim = ((nrows + nslots - 1) / nslots) * nslots;
-            int pos = slot / t.nh, lh = slot - pos * t.nh;
-            const int dpos = nslots / t.nh, dlh = nslots - dpos * t.nh;
-            for (int rr = slot; rr < lim; rr += nslots) {
-                const bool row_ok = rr < nrows;
-                const bool lane_ok = row_ok && lane_has;
-                float xl[VEC], xh[VEC], dyl[VEC], dyh[VEC];
-                float r = 0.f, dot = 0.f;
-                if (lane_ok) {
-                    const T *xr = reinterpret_cast<const T *>(buf + (size_t)rr * xrow);
-                    load16<T>(xr + c * VEC, xl);
-                    load16<T>(xr + half + c * VEC, xh);
-                    const float *yr = reinterpret_cast<const float *>(
-                        buf + geo.y_off + (size_t)(lh * t.np + pos) * yrow);
-                    float gl[VEC], gh[VEC], cv[VEC], sv[VEC];
-                    load_f32<VEC>(yr + c * VEC, gl);
-                    load_f32<VEC>(yr + half + c * VEC, gh);
-                    load_cs<VEC>(tb0 + pos * half, cv, sv);
-                    r = rbuf[rr];
+    // Stage: x rows [lh], dyhat rows [lh] (one copy per head: dqhat/dkhat are
+    // [B, heads, S, D]), rstd [lh], the position's cos/sin row.
+    auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
+        const Unit t = decode_unit(u, geo, H, G);
+        const int NH = t.isq ? H : G;
+        const size_t bs = (size_t)t.b * S + t.s;
+        if (lane < t.nh)
+            cp_async4(reinterpret_cast<float *>(buf + geo.r_off) + lane,
+                      (t.isq ? rstd_q : rstd_k) + bs * NH + t.h0 + lane);
+        cp_async_mbar_arrive(bar);   // one pending arrival until this lane's copy lands
+        __syncwarp();
+        const uint32_t xb = (uint32_t)t.nh * xrow;
+        if (lane == 0) {
+            mbar_expect_tx(bar, xb + (uint32_t)t.nh * yrow + trow);
+            bulk_load(buf, (t.isq ? q : k) + (bs * NH + t.h0) * D, xb, bar);
+            bulk_load(buf + geo.t_off, tab + (size_t)t.s * half, trow, bar);
+        }
+        __syncwarp();
+        const float *dy = (t.isq ? dqhat : dkhat) + (((size_t)t.b * NH + t.h0) * S + t.s) * D;
+        if (lane < t.nh)
+            bulk_load(buf + geo.y_off + (size_t)lane * yrow, dy + (size_t)lane * S * D, yrow, bar);
+    };
+    auto process = [&](uint32_t u, const unsigned char *buf) {
+        const Unit t = decode_unit(u, geo, H, G);
+        const int NH = t.isq ? H : G;
+        float gml[VEC], gmh[VEC], cv[VEC], sv[VEC];
+        const float *gamma = t.isq ? gq : gk;
+        ldg_f32<VEC>(gamma + cc * VEC, gml);
+        ldg_f32<VEC>(gamma + half + cc * VEC, gmh);
+        load_cs<VEC>(reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC, cv, sv);
+        T *obase = (t.isq ? dq : dk) + (((size_t)t.b * S + t.s) * NH + t.h0) * D;
+        const float *rbuf = reinterpret_cast<const float *>(buf + geo.r_off);
+        for (int lh0 = 0; lh0 < t.nh; lh0 += rpi) {
+            const int lh = lh0 + sub;
+            const bool ok = lh < t.nh && lane_has;
+            const int lr = min(lh, t.nh - 1);
+            const T *xr = reinterpret_cast<const T *>(buf + (size_t)lr * xrow);
+            const float *yr = reinterpret_cast<const float *>(buf + geo.y_off + (size_t)lr * yrow);
+            float xl[VEC], xh[VEC], gl[VEC], gh[VEC];
+            load16<T>(xr + cc * VEC, xl);
+            load16<T>(xr + half + cc * VEC, xh);
+            load_f32<VEC>(yr + cc * VEC, gl);
+            load_f32<VEC>(yr + half + cc * VEC, gh);
+            const float r = rbuf[lr];
+            float dyl[VEC], dyh[VEC];
+            float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        // rotation by the negative angle
-                        dyl[e] = gl[e] * cv[e] + gh[e] * sv[e];
-                        dyh[e] = gh[e] * cv[e] - gl[e] * sv[e];
-                        dot += gml[e] * dyl[e] * xl[e] + gmh[e] * dyh[e] * xh[e];
+            for (int e = 0; e < VEC; ++e) {
+                // rotation by the negative angle
+                dyl[e] = gl[e] * cv[e] + gh[e] * sv[e];
+                dyh[e] = gh[e] * cv[e] - gl[e] * sv[e];
+                d0 = fmaf(gml[e] * dyl[e], xl[e], d0);
+                d1 = fmaf(gmh[e] * dyh[e], xh[e], d1);
+            }
+            const float dot = group_sum(lane_has ? d0 + d1 : 0.f, tpr);
+            const float corr = dot * r * r * r * inv_d;
+            float ol[VEC], oh[VEC];
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                ol[e] = gml[e] * dyl[e] * r - xl[e] * corr;
+                oh[e] = gmh[e] * dyh[e] * r - xh[e] * corr;
+            }
+            if (ok) {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    if (t.isq) {   // uniform per unit; keeps both arrays in registers
+                        accq[e] += dyl[e] * xl[e] * r;
+                        accq[VEC + e] += dyh[e] * xh[e] * r;
+                    } else {
+                        acck[e] += dyl[e] * xl[e] * r;
+                        acck[VEC + e] += dyh[e] * xh[e] * r;
                     }
                 }
-                dot = group_sum(dot, tpr);
-                if (lane_ok) {
-                    const float corr = dot * r * r * r * inv_d;
-                    float ol[VEC], oh[VEC];
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        ol[e] = gml[e] * dyl[e] * r - xl[e] * corr;
-                        oh[e] = gmh[e] * dyh[e] * r - xh[e] * corr;
-                        if (t.isq) {   // uniform per unit; keeps both arrays in registers
-                            accq[e] += dyl[e] * xl[e] * r;
-                            accq[VEC + e] += dyh[e] * xh[e] * r;
-                        } else {
-                            acck[e] += dyl[e] * xl[e] * r;
-                            acck[VEC + e] += dyh[e] * xh[e] * r;
-                        }
-                    }
-                    T *dst = obase + ((size_t)pos * NH + lh) * D;
-                    store16<T>(dst + c * VEC, ol);
-                    store16<T>(dst + half + c * VEC, oh);
-                }
-                lh += dlh;
-                pos += dpos;
-                if (lh >= t.nh) { lh -= t.nh; ++pos; }
+                T *dst = obase + (size_t)lh * D;
+                store16<T>(dst + c * VEC, ol);
+                store16<T>(dst + half + c * VEC, oh);
             }
-        });
-    }
+        }
+    };
+    const uint32_t gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
+    const bool ok = warp_pipeline<NS>(full, ring, geo.stage_bytes, gw, nw, (uint32_t)geo.units,
+                                      err, issue, process);
+    if (!ok && lane == 0) any_failed = 1;
 
-    // Fixed-order reduction of the dgamma terms over the consumer row slots.
-    // Every copy has landed once all threads are here (the consumers waited
-    // for each unit), so the ring can hold the [nslots][D] scratch.
+    // Fixed-order reduction of the dgamma terms: over the rows a thread slot
+    // (warp, sub) handled, then over the slots in order. Every copy has landed
+    // once all warps are here, so the rings can hold the [slots][D] scratch.
     __syncthreads();
-    if (*(volatile int *)&ctl->abort_flag) return;
-    float *red = reinterpret_cast<float *>(ring);
+    if (any_failed) return;
+    float *red = reinterpret_cast<float *>(smem + ring_offset<NS>());
+    const int nslots = kWarps * rpi, slot = warp * rpi + sub;
     for (int pass = 0; pass < 2; ++pass) {
         const float *acc = pass == 0 ? accq : acck;
         if (pass) __syncthreads();
-        if (threadIdx.x < kConsumers && lane_has) {
+        if (lane_has) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
                 red[slot * D + c * VEC + e] = acc[e];
@@ -604,64 +570,31 @@ RopeConsts rope_consts(const Problem &p) {
     return f;
 }
 
-int gcd_int(int a, int b) {
-    while (b) { const int t = a % b; a = b; b = t; }
-    return a;
-}
-
-// Units over H q heads and G k heads (G = 0: q only). Per row the ring stages
-// x_row bytes of the first input, y_row of the second and r_row of rstd; with
-// a table, each unit also stages its positions' cos/sin rows.
-//  run_row > 0: each head's P rows are also a run of P * run_row bytes in a
-//    [B, heads, S, D] tensor: P makes that run about kRunBytes, HC fills the
-//    budget, rounded down to a divisor of gcd(H, G) when that loses at most
-//    half of it (equal units).
-//  run_row == 0: units are whole positions (all H heads, contiguous in the
-//    [B, S, H, D] inputs), or one position and a chunk of its heads when a
-//    position alone exceeds the budget.
+// Units over H q heads and G k heads (G = 0: q only), one position each. A
+// stage holds HC rows of x_row + y_row + r_row bytes (and a cos/sin row with
+// a table); HC is the largest multiple of `rpi` (rows per warp-iteration)
+// whose rows fit `row_budget` bytes, at most max(H, G) rounded up to rpi, and
+// at most 32 (one copy per lane).
 UnitGeo make_geo(const Problem &p, int H, int G, size_t x_row, size_t y_row, size_t r_row,
-                 size_t run_row, bool table) {
+                 bool table, int rpi, size_t row_budget) {
     UnitGeo g = {};
     const size_t row = x_row + y_row + r_row;
-    const size_t trow = table ? (size_t)(p.D / 2) * sizeof(float2) : 0;
     const int hmax = H > G ? H : G;
-    size_t P = 1, HC = 1;
-    if (run_row > 0) {
-        P = kRunBytes / run_row;
-        if (P > (size_t)p.S) P = (size_t)p.S;
-        if (P < 1) P = 1;
-        while (P > 1 && P * (row + trow) > kStageBudget) P /= 2;
-        size_t hc_max = (kStageBudget - P * trow) / (P * row);
-        if (hc_max < 1) hc_max = 1;
-        if (hc_max > (size_t)hmax) hc_max = (size_t)hmax;
-        HC = hc_max;
-        const int hdiv = G > 0 ? gcd_int(H, G) : H;
-        size_t d = hc_max < (size_t)hdiv ? hc_max : (size_t)hdiv;
-        while (d > 1 && hdiv % d != 0) --d;
-        if (2 * d >= hc_max) HC = d;
-    } else {
-        const size_t per_pos = (size_t)H * row;
-        if (per_pos <= kStageBudget) {
-            P = kStageBudget / per_pos;
-            if (P > (size_t)p.S) P = (size_t)p.S;
-            HC = (size_t)H;
-        } else {
-            P = 1;
-            HC = kStageBudget / row;
-            if (HC < 1) HC = 1;
-        }
-    }
-    g.P = (int)P;
-    g.HC = (int)HC;
-    g.nsb = (p.S + g.P - 1) / g.P;
-    g.nqc = (H + g.HC - 1) / g.HC;
-    g.nkc = G > 0 ? (G + g.HC - 1) / g.HC : 0;
-    g.units = p.B * g.nsb * (g.nqc + g.nkc);
-    const size_t rows = P * HC;
-    g.y_off = (int)align16(rows * x_row);
-    g.r_off = (int)align16(g.y_off + rows * y_row);
-    g.t_off = (int)align16(g.r_off + rows * r_row);
-    g.stage_bytes = (int)align128(g.t_off + P * trow);
+    int hc = (int)(row_budget / row) / rpi * rpi;
+    if (hc < rpi) hc = rpi;
+    const int cap = (hmax + rpi - 1) / rpi * rpi;
+    if (hc > cap) hc = cap;
+    if (hc > 32) hc = 32;
+    g.HC = hc;
+    g.nqc = (H + hc - 1) / hc;
+    g.nkc = G > 0 ? (G + hc - 1) / hc : 0;
+    g.units = p.B * p.S * (g.nqc + g.nkc);
+    g.fd_chunks = make_fastdiv((uint32_t)(g.nqc + g.nkc));
+    g.fd_S = make_fastdiv((uint32_t)p.S);
+    g.y_off = (int)align16((size_t)hc * x_row);
+    g.r_off = (int)align16(g.y_off + (size_t)hc * y_row);
+    g.t_off = (int)align16(g.r_off + (size_t)hc * r_row);
+    g.stage_bytes = (int)align128(g.t_off + (table ? (size_t)(p.D / 2) * sizeof(float2) : 0));
     return g;
 }
 
@@ -672,7 +605,8 @@ int persistent_grid(int units) {
         sms = 1;
     int g = kCtasPerSm * sms;
     if (g > kMaxNormParts) g = kMaxNormParts;
-    return units < g ? units : g;
+    const int need = (units + kWarps - 1) / kWarps;
+    return need < g ? need : g;
 }
 
 template <typename K>
@@ -680,10 +614,10 @@ cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-size_t ring_smem(const UnitGeo &g, size_t min_ring) {
-    size_t ring = (size_t)kStages * g.stage_bytes;
-    if (ring < min_ring) ring = min_ring;
-    return align128(sizeof(RingCtl)) + ring;
+int rows_per_iter(int D, int dtype, bool halves) {
+    const int vec = dtype == 1 ? 8 : 4;
+    const int chunks = (halves ? D / 2 : D) / vec;
+    return 32 / pow2_at_least(chunks);
 }
 
 }  // namespace
@@ -702,9 +636,9 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
                             const float *gk, const void *tab, void *qhat, void *khat,
                             float *rstd_q, float *rstd_k, unsigned int *err, cudaStream_t st) {
     const size_t es = p.dtype == 1 ? 2 : 4;
-    const size_t xrow = (size_t)p.D * es;
-    const UnitGeo geo = make_geo(p, p.H, p.G, xrow, 0, 0, xrow, true);
-    const size_t smem = ring_smem(geo, 0);
+    const UnitGeo geo = make_geo(p, p.H, p.G, (size_t)p.D * es, 0, 0, true,
+                                 rows_per_iter(p.D, p.dtype, true), 4096);
+    const size_t smem = ring_offset<kStagesPro>() + (size_t)kWarps * kStagesPro * geo.stage_bytes;
     const int grid = persistent_grid(geo.units);
     cudaError_t e;
     if (p.dtype == 1) {
@@ -725,8 +659,9 @@ cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, 
                            unsigned int *err, cudaStream_t st) {
     const size_t es = p.dtype == 1 ? 2 : 4;
     const size_t xrow = (size_t)p.D * es;
-    const UnitGeo geo = make_geo(p, p.H, 0, xrow, xrow, 0, 0, false);
-    const size_t smem = ring_smem(geo, 0);
+    const UnitGeo geo = make_geo(p, p.H, 0, xrow, xrow, 0, false,
+                                 rows_per_iter(p.D, p.dtype, false), 4096);
+    const size_t smem = ring_offset<kStagesPre>() + (size_t)kWarps * kStagesPre * geo.stage_bytes;
     const int grid = persistent_grid(geo.units);
     cudaError_t e;
     if (p.dtype == 1) {
@@ -747,13 +682,13 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
                             void *dk, float *part_q, float *part_k, int *nparts,
                             unsigned int *err, cudaStream_t st) {
     const size_t es = p.dtype == 1 ? 2 : 4;
-    const size_t xrow = (size_t)p.D * es;
-    const size_t yrow = (size_t)p.D * sizeof(float);
-    const UnitGeo geo = make_geo(p, p.H, p.G, xrow, yrow, sizeof(float), yrow, true);
-    const int vec = p.dtype == 1 ? 8 : 4;
-    const int tpr = pow2_at_least((p.D / 2) / vec);
-    const size_t red_bytes = (size_t)(kConsumers / tpr) * p.D * sizeof(float);
-    const size_t smem = ring_smem(geo, red_bytes);
+    const int rpi = rows_per_iter(p.D, p.dtype, true);
+    const UnitGeo geo = make_geo(p, p.H, p.G, (size_t)p.D * es, (size_t)p.D * sizeof(float),
+                                 sizeof(float), true, rpi, 6400);
+    size_t ring = (size_t)kWarps * kStagesEpi * geo.stage_bytes;
+    const size_t red = (size_t)kWarps * rpi * p.D * sizeof(float);
+    if (ring < red) ring = red;
+    const size_t smem = ring_offset<kStagesEpi>() + ring;
     const int grid = persistent_grid(geo.units);
     *nparts = grid;
     cudaError_t e;
