@@ -100,6 +100,7 @@ int validate_shape(int B, int S, int H, int G, int D, int dtype) {
     if (big >= 2147483648.0) return XT_EINVAL;
     if (dtype == XT_BF16 && D != 64 && D != 128) return XT_EUNSUPPORTED;
     if (dtype == XT_F32 && (D % 8 != 0 || D > 128)) return XT_EUNSUPPORTED;
+    if (H + G > kMaxHeads) return XT_EUNSUPPORTED;
     return XT_OK;
 }
 

@@ -41,6 +41,9 @@ enum : unsigned int { ERR_TIMEOUT = 1u };
 // Persistent grids: at most this many CTAs, which bounds the number of
 // per-CTA dgamma partials the backward epilogue writes.
 constexpr int kMaxNormParts = 1024;
+// n_heads + n_kv_heads limit: every warp of those grids (8 per CTA) must be
+// able to own one head chunk of a position.
+constexpr int kMaxHeads = 8 * kMaxNormParts;
 // cos/sin table [S][D/2] of (cos, sin) float pairs, filled by launch_rope_table
 // and read by the prologue and the epilogue.
 size_t rope_table_bytes(const Problem &p);

@@ -169,6 +169,19 @@ __device__ __forceinline__ Unit decode_unit(uint32_t u, const UnitGeo &g, int H,
     return t;
 }
 
+// Fixed-chunk assignment: warp w of the grid takes units w, w + nw,
+// w + 2 nw, ... with nw the number of warps rounded down to a multiple of the
+// chunks per position, so that all of a warp's units have the same chunk
+// (same tensor, same heads); warps at or past nw take none. Balanced when the
+// chunks are of equal size.
+__device__ __forceinline__ void warp_units_fixed(const UnitGeo &g, uint32_t &first,
+                                                 uint32_t &stride) {
+    const uint32_t nch = (uint32_t)(g.nqc + g.nkc);
+    stride = (gridDim.x * kWarps) / nch * nch;
+    first = blockIdx.x * kWarps + (threadIdx.x >> 5);
+    if (first >= stride) first = 0xffffffffu;   // idle warp
+}
+
 // Per-warp pipeline over units first, first + stride, ... < units through NS
 // stages of `stage_bytes` at `ring`, with one mbarrier per stage in `full`.
 // issue(u, buf, bar) is run by all 32 lanes and starts the copies of unit u;
@@ -179,6 +192,7 @@ __device__ bool warp_pipeline(uint64_t *full, unsigned char *ring, int stage_byt
                               uint32_t stride, uint32_t units, unsigned int *err, Issue issue,
                               Process process) {
     const int lane = threadIdx.x & 31;
+    if (first >= units) return true;
     if (lane == 0)
         for (int k = 0; k < NS; ++k) mbar_init(&full[k], 1);
     __syncwarp();
@@ -420,9 +434,17 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     const int cc = lane_has ? c : 0;
     const float inv_d = 1.0f / (float)D;
     if (threadIdx.x == 0) any_failed = 0;
-    float accq[2 * VEC], acck[2 * VEC];
+    uint32_t gw, nw;
+    warp_units_fixed(geo, gw, nw);
+    // every unit of this warp has the same chunk: one gamma, one set of
+    // dgamma accumulators (for that tensor)
+    const bool wq = gw < nw && (int)(gw % (uint32_t)(geo.nqc + geo.nkc)) < geo.nqc;
+    float gml[VEC], gmh[VEC];
+    ldg_f32<VEC>((wq ? gq : gk) + cc * VEC, gml);
+    ldg_f32<VEC>((wq ? gq : gk) + half + cc * VEC, gmh);
+    float acc[2 * VEC];
 #pragma unroll
-    for (int e = 0; e < 2 * VEC; ++e) { accq[e] = 0.f; acck[e] = 0.f; }
+    for (int e = 0; e < 2 * VEC; ++e) acc[e] = 0.f;
 
     // Stage: x rows [lh], dyhat rows [lh] (one copy per head: dqhat/dkhat are
     // [B, heads, S, D]), rstd [lh], the position's cos/sin row.
@@ -449,10 +471,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     auto process = [&](uint32_t u, const unsigned char *buf) {
         const Unit t = decode_unit(u, geo, H, G);
         const int NH = t.isq ? H : G;
-        float gml[VEC], gmh[VEC], cv[VEC], sv[VEC];
-        const float *gamma = t.isq ? gq : gk;
-        ldg_f32<VEC>(gamma + cc * VEC, gml);
-        ldg_f32<VEC>(gamma + half + cc * VEC, gmh);
+        float cv[VEC], sv[VEC];
         load_cs<VEC>(reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC, cv, sv);
         T *obase = (t.isq ? dq : dk) + (((size_t)t.b * S + t.s) * NH + t.h0) * D;
         const float *rbuf = reinterpret_cast<const float *>(buf + geo.r_off);
@@ -489,13 +508,8 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
             if (ok) {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    if (t.isq) {   // uniform per unit; keeps both arrays in registers
-                        accq[e] += dyl[e] * xl[e] * r;
-                        accq[VEC + e] += dyh[e] * xh[e] * r;
-                    } else {
-                        acck[e] += dyl[e] * xl[e] * r;
-                        acck[VEC + e] += dyh[e] * xh[e] * r;
-                    }
+                    acc[e] += dyl[e] * xl[e] * r;
+                    acc[VEC + e] += dyh[e] * xh[e] * r;
                 }
                 T *dst = obase + (size_t)lh * D;
                 store16<T>(dst + c * VEC, ol);
@@ -503,7 +517,6 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
             }
         }
     };
-    const uint32_t gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
     const bool ok = warp_pipeline<NS>(full, ring, geo.stage_bytes, gw, nw, (uint32_t)geo.units,
                                       err, issue, process);
     if (!ok && lane == 0) any_failed = 1;
@@ -515,14 +528,14 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     if (any_failed) return;
     float *red = reinterpret_cast<float *>(smem + ring_offset<NS>());
     const int nslots = kWarps * rpi, slot = warp * rpi + sub;
-    for (int pass = 0; pass < 2; ++pass) {
-        const float *acc = pass == 0 ? accq : acck;
+    for (int pass = 0; pass < 2; ++pass) {   // pass 0: q, pass 1: k
+        const bool mine = (pass == 0) == wq;
         if (pass) __syncthreads();
         if (lane_has) {
 #pragma unroll
             for (int e = 0; e < VEC; ++e) {
-                red[slot * D + c * VEC + e] = acc[e];
-                red[slot * D + half + c * VEC + e] = acc[VEC + e];
+                red[slot * D + c * VEC + e] = mine ? acc[e] : 0.f;
+                red[slot * D + half + c * VEC + e] = mine ? acc[VEC + e] : 0.f;
             }
         }
         __syncthreads();
@@ -598,15 +611,19 @@ UnitGeo make_geo(const Problem &p, int H, int G, size_t x_row, size_t y_row, siz
     return g;
 }
 
-int persistent_grid(int units) {
+// CTAs: enough warps for the units, at most kCtasPerSm per SM and
+// kMaxNormParts, at least one warp per head chunk of a position.
+int persistent_grid(const UnitGeo &geo) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         sms = 1;
     int g = kCtasPerSm * sms;
     if (g > kMaxNormParts) g = kMaxNormParts;
-    const int need = (units + kWarps - 1) / kWarps;
-    return need < g ? need : g;
+    const int need = (geo.units + kWarps - 1) / kWarps;
+    if (need < g) g = need;
+    const int min_ctas = (geo.nqc + geo.nkc + kWarps - 1) / kWarps;
+    return g < min_ctas ? min_ctas : g;
 }
 
 template <typename K>
@@ -639,7 +656,7 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
     const UnitGeo geo = make_geo(p, p.H, p.G, (size_t)p.D * es, 0, 0, true,
                                  rows_per_iter(p.D, p.dtype, true), 4096);
     const size_t smem = ring_offset<kStagesPro>() + (size_t)kWarps * kStagesPro * geo.stage_bytes;
-    const int grid = persistent_grid(geo.units);
+    const int grid = persistent_grid(geo);
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = set_smem(k_prologue<bf16>, smem)) != cudaSuccess) return e;
@@ -662,7 +679,7 @@ cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, 
     const UnitGeo geo = make_geo(p, p.H, 0, xrow, xrow, 0, false,
                                  rows_per_iter(p.D, p.dtype, false), 4096);
     const size_t smem = ring_offset<kStagesPre>() + (size_t)kWarps * kStagesPre * geo.stage_bytes;
-    const int grid = persistent_grid(geo.units);
+    const int grid = persistent_grid(geo);
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = set_smem(k_bwd_pre<bf16>, smem)) != cudaSuccess) return e;
@@ -689,7 +706,7 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
     const size_t red = (size_t)kWarps * rpi * p.D * sizeof(float);
     if (ring < red) ring = red;
     const size_t smem = ring_offset<kStagesEpi>() + ring;
-    const int grid = persistent_grid(geo.units);
+    const int grid = persistent_grid(geo);
     *nparts = grid;
     cudaError_t e;
     if (p.dtype == 1) {

@@ -42,10 +42,10 @@
  * overwritten, not accumulated. Forward and backward are deterministic:
  * identical inputs give bitwise identical outputs.
  *
- * Supported shapes: B, S, H, G >= 1, H % G == 0; dtype XT_BF16 with
- * head_dim 64 or 128 (tensor-core path), dtype XT_F32 with head_dim a
- * multiple of 8 up to 128 (fp32 CUDA-core path). Every tensor must hold
- * fewer than 2^31 elements.
+ * Supported shapes: B, S, H, G >= 1, H % G == 0, H + G <= 8192; dtype
+ * XT_BF16 with head_dim 64 or 128 (tensor-core path), dtype XT_F32 with
+ * head_dim a multiple of 8 up to 128 (fp32 CUDA-core path). Every tensor must
+ * hold fewer than 2^31 elements.
  *
  * Errors: calls validate their arguments on the host before any launch and
  * return an xt_status; no call aborts the process. XT_ECUDA reports a launch

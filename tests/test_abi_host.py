@@ -94,3 +94,8 @@ def test_timing_hooks_without_launches(L):
     xt.xt_timing_reset()
     assert xt.xt_timing_query() == {}
     assert L.xt_kernel_count() >= 5
+
+
+def test_head_count_limit(L):
+    # n_heads + n_kv_heads above 8192 is refused before any launch
+    assert _fwd(L, H=8192, G=1) == xt.XT_EUNSUPPORTED
