@@ -51,6 +51,7 @@ using tc::cp_async_mbar_arrive;
 using tc::mbar_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
+using tc::mbar_wait_sleep;
 
 constexpr int kWarps = 8;                    // warps per CTA, each its own pipeline
 constexpr int kThreads = 32 * kWarps;
@@ -206,7 +207,7 @@ __device__ bool warp_pipeline(uint64_t *full, unsigned char *ring, int stage_byt
     int it = 0;
     for (uint32_t u = first; u < units; u += stride, ++it) {
         const int st = it % NS;
-        const bool ok = mbar_wait(&full[st], (uint32_t)((it / NS) & 1), nullptr);
+        const bool ok = mbar_wait_sleep(&full[st], (uint32_t)((it / NS) & 1));
         if (!__all_sync(0xffffffffu, ok)) {
             if (lane == 0) {
                 atomicOr(err, ERR_TIMEOUT);

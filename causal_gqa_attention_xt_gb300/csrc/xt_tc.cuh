@@ -66,6 +66,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// Bounded wait whose polls carry a suspend-time hint: a thread whose phase is
+// not complete is parked by the hardware until the phase completes or about
+// kSuspendHintNs pass, so a waiting warp spends no issue slots spinning. Used
+// by the streaming kernels, where waiting warps share the SM with computing
+// ones; the tensor-core kernels poll without the hint (lower wake-up latency
+// on their critical path).
+constexpr uint32_t kSuspendHintNs = 200000;   // 0.2 ms
+
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait_hint(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_hint(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
