@@ -35,6 +35,8 @@
 //
 // Warps: 0-3 and 4-7 the softmax warpgroups (thread = owned row = TMEM
 // lane); 8 TMA producer; 9 TMEM allocator + MMA issuer.
+#include <type_traits>
+
 #include "xt_common.cuh"
 #include "xt_internal.h"
 #include "xt_tc.cuh"
@@ -46,7 +48,10 @@ namespace {
 using namespace tc;
 
 constexpr int kTile = 128;         // owned rows (MMA M) and streamed rows (MMA N of S/dP)
-constexpr int kThreadsBwd = 320;
+constexpr int kSoftmaxWGs = 4;     // softmax warpgroups; WG w takes columns [32w, 32w+32)
+constexpr int kWgCols = kTile / kSoftmaxWGs;
+constexpr int kWarpTma = 4 * kSoftmaxWGs, kWarpMma = kWarpTma + 1;
+constexpr int kThreadsBwd = 32 * (kWarpMma + 1);
 constexpr int kMaxStages = 4;
 
 template <int D> struct BwdCfg {
@@ -83,17 +88,17 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
         mbar_init(&bars.st_empty[s], 1);
     }
     mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 256);     // both softmax warpgroups
+    mbar_init(&bars.p_full, 32 * 4 * kSoftmaxWGs);   // every softmax thread
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
 }
 
 // TMEM column of the packed-bf16 A operand (P or dS) for k-step kk of 16 rows:
-// warpgroup 0 wrote rows 0..63 at columns [0,32), warpgroup 1 rows 64..127 at
-// [64,96) (relative to the S or dP region).
+// warpgroup w wrote rows [32w, 32w+32) packed two per column at columns
+// [32w, 32w+16) (relative to the S or dP region).
 __device__ __forceinline__ uint32_t packed_col(int kk) {
-    return kk < 4 ? (uint32_t)(kk * 8) : (uint32_t)(64 + (kk - 4) * 8);
+    return (uint32_t)((kk >> 1) * kWgCols + (kk & 1) * 8);
 }
 
 // Operand descriptors (128B swizzle, 8-row groups 1024 B apart): a K-major
@@ -133,7 +138,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, ST);
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
     }
@@ -141,7 +146,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 8) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&map_k);
@@ -195,7 +200,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             for (int t = max(0, issued - ST); t < issued; ++t)
                 mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
         }
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
@@ -260,47 +265,53 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             if (!ok) break;
             tc_fence_after();
             const int u = j + (t % nU);
-            const int c0 = wg * 64;                     // this warpgroup's columns
+            const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
             const float *sl = reinterpret_cast<const float *>(sStage + st * C::kStageBytes +
                                                               2 * C::kTileBytes);
             const uint32_t tS = tmem + lane_off + c0;         // S^T columns
             const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
             // no masking when every query of these columns is at/after every owned key and < S
-            const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + 64 <= S);
-            uint32_t pp[32], dd[32];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + kWgCols <= S);
+            uint32_t pp[kWgCols / 2], dd[kWgCols / 2];
+            {
                 uint32_t sv[32], dpv[32];
-                tmem_ld32x2_sync(tS + 32 * hf, sv, tP + 32 * hf, dpv);
+                tmem_ld32x2_sync(tS, sv, tP, dpv);
+                // masked columns (the diagonal tile, the ragged end) take the select;
+                // interior tiles (all but about one in n_q) run without it
+                auto body = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const int col = 32 * hf + e;              // within this warpgroup's 64
-                    const float4 l4 = *reinterpret_cast<const float4 *>(sl + c0 + col);
-                    const float4 d4 = *reinterpret_cast<const float4 *>(sl + 128 + c0 + col);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                    const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    float pv[4], dsv[4];
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4 *>(sl + c0 + e);
+                        const float4 d4 = *reinterpret_cast<const float4 *>(sl + 128 + c0 + e);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+                        const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        float pv[4], dsv[4];
 #pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int q = q0 + col + x;
-                        float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lv[x]));
-                        if (!interior && !(q >= kp && q < S)) p = 0.f;
-                        pv[x] = p;
-                        dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlv[x]);
+                        for (int x = 0; x < 4; ++x) {
+                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lv[x]));
+                            if constexpr (decltype(masked)::value) {
+                                const int q = q0 + e + x;
+                                if (!(q >= kp && q < S)) p = 0.f;
+                            }
+                            pv[x] = p;
+                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlv[x]);
+                        }
+                        pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                        pp[(e >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
+                        dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        dd[(e >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
-                    pp[col >> 1] = pack_bf16x2(pv[0], pv[1]);
-                    pp[(col >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
-                    dd[col >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                    dd[(col >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
-                }
+                };
+                if (interior) body(std::false_type{});
+                else body(std::true_type{});
             }
             if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dV/dK
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
                                                        ((t + 1) / ST) & 1, abort_flag));
                 if (!ok) break;
             }
-            tmem_st32x2_sync(tS, pp, tP, dd);
+            tmem_st16x2_sync(tS, pp, tP, dd);
             tc_fence_before();
             mbar_arrive(&bars.p_full);
         }
@@ -308,13 +319,19 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
             if (ok) {
                 tc_fence_after();
-                if (wg == 0) {      // dV row -> bf16
-                    bf16 *dvrow = dv + (((size_t)b * S + kp) * G + g) * D;
+                // 32-column chunks: dV (bf16) chunks 0..D/32-1, then dKhat (fp32, scaled);
+                // warpgroup w writes chunks w, w + kSoftmaxWGs, ...
+                const float scale = rsqrtf((float)D);
+                bf16 *dvrow = dv + (((size_t)b * S + kp) * G + g) * D;
+                float *dkrow = dkhat + ((size_t)bg * S + kp) * D;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t a[32];
-                        tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
-                        if (kp < S) {
+                for (int cc = wg; cc < 2 * (D / 32); cc += kSoftmaxWGs) {
+                    const bool isv = cc < D / 32;
+                    const int c = isv ? cc : cc - D / 32;
+                    uint32_t a[32];
+                    tmem_ld32_sync(tmem + (isv ? 256 : 384) + lane_off + 32 * c, a);
+                    if (kp < S) {
+                        if (isv) {
 #pragma unroll
                             for (int q8 = 0; q8 < 4; ++q8) {
                                 uint4 v4;
@@ -324,16 +341,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                                 v4.w = pack_bf16x2(__uint_as_float(a[q8 * 8 + 6]), __uint_as_float(a[q8 * 8 + 7]));
                                 *reinterpret_cast<uint4 *>(dvrow + 32 * c + 8 * q8) = v4;
                             }
-                        }
-                    }
-                } else {            // dKhat row (scaled) -> fp32
-                    const float scale = rsqrtf((float)D);
-                    float *dkrow = dkhat + ((size_t)bg * S + kp) * D;
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t a[32];
-                        tmem_ld32_sync(tmem + 384 + lane_off + 32 * c, a);
-                        if (kp < S) {
+                        } else {
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4) {
                                 float4 f;
@@ -352,7 +360,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -386,7 +394,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST);
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
     }
@@ -394,7 +402,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 8) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&map_k);
@@ -419,7 +427,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             for (int t = max(0, issued - ST); t < issued; ++t)
                 mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
         }
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
@@ -471,7 +479,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         const float sl2 = kLog2e * rsqrtf((float)D);
         const float lse2 = tq < S ? lse[(size_t)bh * S + tq] * kLog2e : 0.f;
         const float dl = tq < S ? dlt[(size_t)bh * S + tq] : 0.f;
-        {
+        if (wg < 2) {
             // the owned Qhat (warpgroup 0) and dO (warpgroup 1) rows become TMEM-resident
             // A operands (lane = row; a 32-bit column holds two consecutive bf16, the lower
             // index in the low half)
@@ -495,36 +503,41 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, t & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int c0 = wg * 64;
+            const int c0 = wg * kWgCols;
             const int k0 = t * kTile + c0;
             const uint32_t tS = tmem + lane_off + c0;
             const uint32_t tP = tmem + lane_off + 128 + c0;
             // no masking when every key of these columns is at/before every owned query
-            const bool interior = (k0 + 63 <= i * kTile);
-            uint32_t dd[32];
-#pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
+            const bool interior = (k0 + kWgCols - 1 <= i * kTile);
+            uint32_t dd[kWgCols / 2];
+            {
                 uint32_t sv[32], dpv[32];
-                tmem_ld32x2_sync(tS + 32 * hf, sv, tP + 32 * hf, dpv);
+                tmem_ld32x2_sync(tS, sv, tP, dpv);
+                // only tiles that reach past the owned rows' diagonal take the select
+                auto body = [&](auto masked) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    float dsv[2];
+                    for (int e = 0; e < 32; e += 2) {
+                        float dsv[2];
 #pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int kpos = k0 + 32 * hf + e + x;
-                        float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lse2));
-                        if (!interior && kpos > tq) p = 0.f;
-                        dsv[x] = p * (__uint_as_float(dpv[e + x]) - dl);
+                        for (int x = 0; x < 2; ++x) {
+                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lse2));
+                            if constexpr (decltype(masked)::value) {
+                                if (k0 + e + x > tq) p = 0.f;
+                            }
+                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dl);
+                        }
+                        dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
                     }
-                    dd[(32 * hf + e) >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                }
+                };
+                if (interior) body(std::false_type{});
+                else body(std::true_type{});
             }
             if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dQ
                 ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
                                                        ((t + 1) / ST) & 1, abort_flag));
                 if (!ok) break;
             }
-            tmem_st32_sync(tS, dd);
+            tmem_st16_sync(tS, dd);
             tc_fence_before();
             mbar_arrive(&bars.p_full);
         }
@@ -534,10 +547,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 tc_fence_after();
                 const float scale = rsqrtf((float)D);
                 float *dst = dqhat + ((size_t)bh * S + tq) * D;
-                // the two warpgroups split the D columns of the dQhat row
+                // warpgroup w writes the 32-column chunks w, w + kSoftmaxWGs, ... of the row
 #pragma unroll
-                for (int cc = 0; cc < D / 64; ++cc) {
-                    const int c = wg * (D / 64) + cc;
+                for (int c = wg; c < D / 32; c += kSoftmaxWGs) {
                     uint32_t a[32];
                     tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
                     if (tq < S) {
@@ -558,7 +570,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }

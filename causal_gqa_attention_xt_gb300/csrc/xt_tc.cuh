@@ -326,6 +326,18 @@ __device__ __forceinline__ void tmem_st32x2_sync(uint32_t ta, const uint32_t (&a
 }
 
 
+// Two 16-column stores (to two TMEM addresses) and one wait.
+__device__ __forceinline__ void tmem_st16x2_sync(uint32_t ta, const uint32_t (&a)[16], uint32_t tb,
+                                                 const uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17};\n"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};\n"
+        "tcgen05.wait::st.sync.aligned;"
+        :: "r"(ta), "r"(tb), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]), "r"(b[8]), "r"(b[9]), "r"(b[10]), "r"(b[11]), "r"(b[12]), "r"(b[13]), "r"(b[14]), "r"(b[15])
+        : "memory");
+}
+
+
 // Two 32-column loads (from two TMEM addresses) and one wait.
 __device__ __forceinline__ void tmem_ld32x2_sync(uint32_t ta, uint32_t (&a)[32], uint32_t tb,
                                                  uint32_t (&b)[32]) {
