@@ -17,24 +17,31 @@
 //    the 128-row key tiles at or before them, accumulating dQhat += dS Khat.
 // Both recompute S from the saved Qhat, Khat and lse.
 //
-// Per streamed tile the MMA warp issues S (or S^T) into TMEM columns
-// [0,128) and dP (or dP^T) into [128,256) (M=128, N=128: full-rate MMA
-// shapes); two softmax warpgroups split the 128 columns (warpgroup w takes
-// columns [64w, 64w+64)), form P and dS, and write them back as packed bf16
-// over the columns they themselves read (P at [64w, 64w+32), dS at
-// [128+64w, 128+64w+32)), so the two halves never race. The accumulating MMAs
-// (TS form, A from TMEM) read those halves k-step by k-step.
+// TMEM: S (or S^T) in columns [0,128), dP (or dP^T) in [128,256), the
+// accumulators from 256. Four softmax warpgroups split the streamed tile's 128
+// columns (warpgroup w takes [32w, 32w+32)), form P and dS, and write them back
+// as packed bf16 over the first 16 of the columns they themselves read, so no
+// two warpgroups race. The accumulating MMAs (TS form, A from TMEM) read those
+// packed columns k-step by k-step; the causal-mask select runs only on tiles
+// that cross the diagonal or the end of the sequence.
 //
-// Pipeline: the MMA thread polls one mbarrier per tile (P/dS of tile t) and
-// then issues the accumulating MMAs of t followed by S/dP of t+1, which
-// reuse the TMEM buffer: one thread's tcgen05.mma operations execute in issue
-// order, so t+1 cannot overwrite P/dS of t before they are read. An mbarrier
-// poll right after tcgen05.commit stalls the issuing thread until earlier
-// MMAs drain, so the TMA-arrival check for tile t+1 is done by the softmax
-// warps before they signal tile t.
+// dK/dV pipeline: S^T and dP^T are issued per half of the streamed tile
+// (queries [64h, 64h+64), N = 64), each half with its own "S ready" and "P
+// ready" mbarriers, warpgroups 2h and 2h+1 being that half's. Once half h's P/dS
+// are in TMEM, the MMA thread issues that half's 4 k-steps of dV and dKhat and
+// then S^T/dP^T of the same half of the next tile: the tensor core works on one
+// half while the other half's softmax runs. One thread's tcgen05.mma
+// operations execute in issue order, so the next tile's S/dP cannot overwrite
+// P/dS before they are read. (In the dQ kernel the S/dP MMAs are TS-form, which
+// at N = 64 runs well below the full rate: it keeps full 128-key tiles and one
+// "P ready" barrier for all four warpgroups.)
 //
-// Warps: 0-3 and 4-7 the softmax warpgroups (thread = owned row = TMEM
-// lane); 8 TMA producer; 9 TMEM allocator + MMA issuer.
+// An mbarrier poll right after tcgen05.commit stalls the issuing thread until
+// earlier MMAs drain, so the TMA-arrival check for the next tile is done by the
+// softmax warps before they signal the current one.
+//
+// Warps: 0-15 the four softmax warpgroups (thread = owned row = TMEM lane of
+// its warp's quarter); 16 TMA producer; 17 TMEM allocator + MMA issuer.
 #include <type_traits>
 
 #include "xt_common.cuh"
@@ -67,7 +74,7 @@ template <int D> struct BwdCfg {
 struct BwdBarriers {
     uint64_t own_full;
     uint64_t st_full[kMaxStages], st_empty[kMaxStages];
-    uint64_t s_full, p_full;
+    uint64_t s_full[2], p_full[2];   // per half of the streamed tile (columns [64h, 64h+64))
     uint64_t acc_done;
     uint64_t drain;
     uint32_t tmem_base;
@@ -79,16 +86,22 @@ __device__ __forceinline__ void raise_error_b(unsigned int *err, volatile int *a
     *abort_flag = 1;
 }
 
+// split_p: one p_full barrier per half of the streamed tile (the dK/dV kernel);
+// otherwise p_full[0] collects every softmax thread.
 __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t own_count,
-                                                  uint32_t st_full_count, int stages) {
+                                                  uint32_t st_full_count, int stages,
+                                                  bool split_p) {
     bars.abort_flag = 0;
     mbar_init(&bars.own_full, own_count);
     for (int s = 0; s < stages; ++s) {
         mbar_init(&bars.st_full[s], st_full_count);
         mbar_init(&bars.st_empty[s], 1);
     }
-    mbar_init(&bars.s_full, 1);
-    mbar_init(&bars.p_full, 32 * 4 * kSoftmaxWGs);   // every softmax thread
+    for (int h = 0; h < 2; ++h) {
+        mbar_init(&bars.s_full[h], 1);
+        mbar_init(&bars.p_full[h], split_p ? 32 * 4 * kSoftmaxWGs / 2    // the half's two warpgroups
+                                           : 32 * 4 * kSoftmaxWGs);      // every softmax thread
+    }
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     fence_barrier_init();
@@ -137,7 +150,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const int T = group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, ST);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, ST, true);
     if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -203,7 +216,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
+            const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile / 2, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
             const uint64_t dV = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128B);
@@ -212,38 +225,52 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const uint64_t dQm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
             const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16384, 1024, kSwizzle128B);
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
-            auto issue_sp = [&](int t) {            // S^T = Khat Qhat^T, dP^T = V dO^T
-                const uint64_t so = (uint64_t)(t % ST) * kStep;
+            // S^T = Khat Qhat^T and dP^T = V dO^T for the queries [64h, 64h+64) of
+            // tile t (B rows 64h.. start 8 KB into each 64-column chunk)
+            auto issue_sp = [&](int t, int h) {
+                const uint64_t so = (uint64_t)(t % ST) * kStep + (uint64_t)h * (8192 >> 4);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem, dK + kmajor_off(kk), dQk0 + so + kmajor_off(kk), idesc_s, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128, dV + kmajor_off(kk), dDOk0 + so + kmajor_off(kk), idesc_s,
+                    mma_ss(tmem + 64 * h, dK + kmajor_off(kk), dQk0 + so + kmajor_off(kk), idesc_s,
                            kk > 0);
-                mma_commit(&bars.s_full);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off(kk), dDOk0 + so + kmajor_off(kk),
+                           idesc_s, kk > 0);
+                mma_commit(&bars.s_full[h]);
             };
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
                       mbar_wait(&bars.st_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_sp(0);
+                issue_sp(0, 0);
+                issue_sp(0, 1);
             }
+            // Per half h: once its P/dS are in TMEM, accumulate its 4 k-steps of
+            // dV += P^T dO and dKhat += dS^T Qhat, then start S/dP of the same half
+            // of the next tile (in-order execution keeps them behind those reads).
             for (int t = 0; ok && t < T; ++t) {
                 const int st = t % ST;
-                if (!(ok = mbar_wait(&bars.p_full, t & 1, abort_flag))) break;
-                tc_fence_after();
                 const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)   // dV += P^T dO
-                    mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(kk),
-                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < 2; ++h) {
+                    if (!(ok = mbar_wait(&bars.p_full[h], t & 1, abort_flag))) break;
+                    tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)   // dKhat += dS^T Qhat
-                    mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(kk),
-                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bars.st_empty[st]);
-                if (t + 1 < T) issue_sp(t + 1);       // operands checked by the softmax warps
+                    for (int k4 = 0; k4 < 4; ++k4) {   // dV += P^T dO
+                        const int kk = 4 * h + k4;
+                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(kk),
+                               idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {   // dKhat += dS^T Qhat
+                        const int kk = 4 * h + k4;
+                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(kk),
+                               idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (h == 1) mma_commit(&bars.st_empty[st]);
+                    if (t + 1 < T) issue_sp(t + 1, h);   // operands checked by the softmax warps
+                }
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -260,7 +287,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         bool ok = true;
         for (int t = 0; t < T; ++t) {
             const int st = t % ST;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, t & 1, abort_flag) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[wg >> 1], t & 1, abort_flag) &&
                                              mbar_wait(&bars.st_full[st], (t / ST) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -313,7 +340,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             }
             tmem_st16x2_sync(tS, pp, tP, dd);
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            mbar_arrive(&bars.p_full[wg >> 1]);
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
@@ -393,7 +420,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST, false);
     if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -436,7 +463,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, 1024, kSwizzle128B);
             const uint64_t dKm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
-            auto issue_sp = [&](int t) {            // S = Qhat Khat^T, dP = dO V^T (A in TMEM)
+            // S = Qhat Khat^T and dP = dO V^T (A in TMEM), full 128-key tiles: the
+            // TS form at N = 128 runs at the full MMA rate (N = 64 does not)
+            auto issue_sp = [&](int t) {
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
@@ -445,7 +474,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off(kk), idesc_s,
                            kk > 0);
-                mma_commit(&bars.s_full);
+                mma_commit(&bars.s_full[0]);
             };
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
                       mbar_wait(&bars.st_full[0], 0, abort_flag);
@@ -455,9 +484,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             }
             for (int t = 0; ok && t < T; ++t) {
                 const int st = t % ST;
-                if (!(ok = mbar_wait(&bars.p_full, t & 1, abort_flag))) break;
-                tc_fence_after();
                 const uint64_t so = (uint64_t)st * kStep;
+                if (!(ok = mbar_wait(&bars.p_full[0], t & 1, abort_flag))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
                     mma_ts(tmem + 256, tmem + packed_col(kk), dKm0 + so + mnmajor_off(kk),
@@ -500,7 +529,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         }
         bool ok = true;
         for (int t = 0; t < T; ++t) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full, t & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], t & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int c0 = wg * kWgCols;
@@ -539,7 +568,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             }
             tmem_st16_sync(tS, dd);
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            mbar_arrive(&bars.p_full[0]);
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
