@@ -59,16 +59,22 @@ constexpr int kSoftmaxWGs = 4;     // softmax warpgroups; WG w takes columns [32
 constexpr int kWgCols = kTile / kSoftmaxWGs;
 constexpr int kWarpTma = 4 * kSoftmaxWGs, kWarpMma = kWarpTma + 1;
 constexpr int kThreadsBwd = 32 * (kWarpMma + 1);
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 
 template <int D> struct BwdCfg {
     static constexpr int kChunks = D / 64;
     static constexpr int kTileBytes = kChunks * 16384;   // 128 rows x D bf16
+    static constexpr int kHalfBytes = kChunks * 8192;    // 64 rows x D bf16
+    // dQ kernel: a stage holds a K and a V tile
     static constexpr int kStages = (D == 128) ? 2 : 4;
-    // a stage: two 128-row tiles and (dK/dV kernel) 2 x 128 row statistics
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-    static constexpr int kSmemA = 2 * kTileBytes + kStages * kStageBytes + 1024;
     static constexpr int kSmemB = kStages * kStageBytes + 1024;
+    // dK/dV kernel: a ring of half tiles, each the Qhat and dO rows of one half
+    // of a streamed query tile plus their 2 x 64 row statistics, so that a half
+    // is reloaded as soon as its own MMAs are done
+    static constexpr int kHStages = (D == 128) ? 4 : 8;
+    static constexpr int kHStageBytes = 2 * kHalfBytes + 1024;
+    static constexpr int kSmemA = 2 * kTileBytes + kHStages * kHStageBytes + 1024;
 };
 
 struct BwdBarriers {
@@ -115,10 +121,11 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
 }
 
 // Operand descriptors (128B swizzle, 8-row groups 1024 B apart): a K-major
-// operand advances 16 elements by +32 B inside a 64-column chunk of 16 KB;
-// an MN-major B operand advances 16 rows by +2048 B, its 64-column N chunks
-// 16 KB apart.
+// operand advances 16 elements by +32 B inside a 64-column chunk (16 KB for
+// 128 rows, 8 KB for a 64-row half tile); an MN-major B operand advances 16
+// rows by +2048 B, its 64-column N chunks a chunk apart (in the descriptor).
 constexpr uint64_t kmajor_off(int kk) { return (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; }
+constexpr uint64_t kmajor_off_half(int kk) { return (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4; }
 constexpr uint64_t mnmajor_off(int kk) { return (uint64_t)(kk * 2048) >> 4; }
 
 // ---------------------------------------------------------------------------
@@ -132,7 +139,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
               float *__restrict__ dkhat, bf16 *__restrict__ dv, int S, int H, int G,
               int n_kvt, unsigned int *err) {
     using C = BwdCfg<D>;
-    constexpr int ST = C::kStages;
+    constexpr int HS = C::kHStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -150,7 +157,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const int T = group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, ST, true);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, HS, true);
     if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -172,12 +179,13 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g, j * kTile, b);
             }
         }
+        // half tile x = 2 t + hf: rows [64 hf, 64 hf + 64) of streamed tile t
         int issued = 0;
-        for (int t = 0; t < T; ++t) {
-            const int st = t % ST;
+        for (int x = 0; x < 2 * T; ++x) {
+            const int hs = x % HS, t = x >> 1, hf = x & 1;
             bool ok = true;
-            if (t >= ST && lane == 0)
-                ok = mbar_wait(&bars.st_empty[st], ((t / ST) - 1) & 1, abort_flag);
+            if (x >= HS && lane == 0)
+                ok = mbar_wait(&bars.st_empty[hs], ((x / HS) - 1) & 1, abort_flag);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) {
                 if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
@@ -185,33 +193,33 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             }
             const int r = t / nU, u = j + (t - r * nU);
             const int h = g * group + r;
-            uint8_t *base = sStage + st * C::kStageBytes;
+            const int q0 = u * kTile + 64 * hf;
+            uint8_t *base = sStage + hs * C::kHStageBytes;
             if (lane == 0) {
-                mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
+                mbar_expect_tx(&bars.st_full[hs], 2 * C::kHalfBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 16384, &map_q, &bars.st_full[st], c * 64, u * kTile,
-                                b * H + h);
-                    tma_load_4d(base + C::kTileBytes + c * 16384, &map_do, &bars.st_full[st],
-                                c * 64, h, u * kTile, b);
+                    tma_load_3d(base + c * 8192, &map_q, &bars.st_full[hs], c * 64, q0, b * H + h);
+                    tma_load_4d(base + C::kHalfBytes + c * 8192, &map_do, &bars.st_full[hs],
+                                c * 64, h, q0, b);
                 }
             }
-            float *sl = reinterpret_cast<float *>(base + 2 * C::kTileBytes);
+            float *sl = reinterpret_cast<float *>(base + 2 * C::kHalfBytes);
             const size_t row0 = ((size_t)b * H + h) * S;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int k = lane + 32 * e, q = u * kTile + k;
-                sl[k] = q < S ? lse[row0 + q] * kLog2e : 0.f;
-                sl[128 + k] = q < S ? dlt[row0 + q] : 0.f;
+            for (int e = 0; e < 2; ++e) {
+                const int kq = lane + 32 * e, q = q0 + kq;
+                sl[kq] = q < S ? lse[row0 + q] * kLog2e : 0.f;
+                sl[64 + kq] = q < S ? dlt[row0 + q] : 0.f;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars.st_full[st]);
-            issued = t + 1;
+            if (lane == 0) mbar_arrive(&bars.st_full[hs]);
+            issued = x + 1;
         }
         if (lane == 0) {
             // drain: every copy issued by this CTA lands before it exits
             mbar_wait(&bars.own_full, 0, nullptr);
-            for (int t = max(0, issued - ST); t < issued; ++t)
-                mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
+            for (int x = max(0, issued - HS); x < issued; ++x)
+                mbar_wait(&bars.st_full[x % HS], (x / HS) & 1, nullptr);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -221,26 +229,27 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
             const uint64_t dV = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128B);
             const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
-            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, 1024, kSwizzle128B);
-            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
-            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16384, 1024, kSwizzle128B);
-            constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
+            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 16, 1024, kSwizzle128B);
+            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
+            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 8192, 1024, kSwizzle128B);
+            constexpr uint64_t kStep = (uint64_t)C::kHStageBytes >> 4;
             // S^T = Khat Qhat^T and dP^T = V dO^T for the queries [64h, 64h+64) of
-            // tile t (B rows 64h.. start 8 KB into each 64-column chunk)
+            // tile t, from half stage (2t + h) % HS
             auto issue_sp = [&](int t, int h) {
-                const uint64_t so = (uint64_t)(t % ST) * kStep + (uint64_t)h * (8192 >> 4);
+                const uint64_t so = (uint64_t)((2 * t + h) % HS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 64 * h, dK + kmajor_off(kk), dQk0 + so + kmajor_off(kk), idesc_s,
-                           kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off(kk), dDOk0 + so + kmajor_off(kk),
+                    mma_ss(tmem + 64 * h, dK + kmajor_off(kk), dQk0 + so + kmajor_off_half(kk),
                            idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off(kk),
+                           dDOk0 + so + kmajor_off_half(kk), idesc_s, kk > 0);
                 mma_commit(&bars.s_full[h]);
             };
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
-                      mbar_wait(&bars.st_full[0], 0, abort_flag);
+                      mbar_wait(&bars.st_full[0], 0, abort_flag) &&
+                      mbar_wait(&bars.st_full[1], 0, abort_flag);   // both halves of tile 0
             if (ok) {
                 tc_fence_after();
                 issue_sp(0, 0);
@@ -250,25 +259,25 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             // dV += P^T dO and dKhat += dS^T Qhat, then start S/dP of the same half
             // of the next tile (in-order execution keeps them behind those reads).
             for (int t = 0; ok && t < T; ++t) {
-                const int st = t % ST;
-                const uint64_t so = (uint64_t)st * kStep;
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
+                    const int hs = (2 * t + h) % HS;
+                    const uint64_t so = (uint64_t)hs * kStep;
                     if (!(ok = mbar_wait(&bars.p_full[h], t & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dV += P^T dO
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(kk),
+                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dKhat += dS^T Qhat
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(kk),
+                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
-                    if (h == 1) mma_commit(&bars.st_empty[st]);
+                    mma_commit(&bars.st_empty[hs]);       // this half stage may be reloaded
                     if (t + 1 < T) issue_sp(t + 1, h);   // operands checked by the softmax warps
                 }
             }
@@ -285,17 +294,20 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         bool ok = true;
+        const int hf = wg >> 1;                         // this warpgroup's half of the tile
         for (int t = 0; t < T; ++t) {
-            const int st = t % ST;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[wg >> 1], t & 1, abort_flag) &&
-                                             mbar_wait(&bars.st_full[st], (t / ST) & 1, abort_flag));
+            const int x = 2 * t + hf, hs = x % HS;
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[hf], t & 1, abort_flag) &&
+                                             mbar_wait(&bars.st_full[hs], (x / HS) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int u = j + (t % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            const float *sl = reinterpret_cast<const float *>(sStage + st * C::kStageBytes +
-                                                              2 * C::kTileBytes);
+            // statistics of the half: lse at [0,64), Dlt at [64,128)
+            const float *sl = reinterpret_cast<const float *>(sStage + hs * C::kHStageBytes +
+                                                              2 * C::kHalfBytes) +
+                              32 * (wg & 1);
             const uint32_t tS = tmem + lane_off + c0;         // S^T columns
             const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
             // no masking when every query of these columns is at/after every owned key and < S
@@ -309,8 +321,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 auto body = [&](auto masked) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(sl + c0 + e);
-                        const float4 d4 = *reinterpret_cast<const float4 *>(sl + 128 + c0 + e);
+                        const float4 l4 = *reinterpret_cast<const float4 *>(sl + e);
+                        const float4 d4 = *reinterpret_cast<const float4 *>(sl + 64 + e);
                         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
                         const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
                         float pv[4], dsv[4];
@@ -333,9 +345,9 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 if (interior) body(std::false_type{});
                 else body(std::true_type{});
             }
-            if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dV/dK
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
-                                                       ((t + 1) / ST) & 1, abort_flag));
+            if (t + 1 < T) {   // operands of this half of tile t+1, issued right behind its dV/dK
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(x + 2) % HS],
+                                                       ((x + 2) / HS) & 1, abort_flag));
                 if (!ok) break;
             }
             tmem_st16x2_sync(tS, pp, tP, dd);
@@ -613,7 +625,8 @@ struct BwdMaps {
 };
 
 // Qhat [B*H, S, D] / Khat [B*G, S, D] as 3-D maps; V [B, S, G, D] and
-// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of 64 columns x 128 rows.
+// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of 64 columns x 128 rows
+// (K, V: whole tiles) or x 64 rows (Qhat, dO: the dK/dV kernel's half tiles).
 cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, const void *v,
                       const void *dout, BwdMaps &m) {
     const uint64_t esz = 2, D = (uint64_t)p.D;
@@ -621,7 +634,7 @@ cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, cons
     {
         const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, (uint32_t)kTile, 1};
+        const uint32_t box[3] = {64, (uint32_t)kTile / 2, 1};
         if ((e = encode_tmap_bf16(&m.q, qhat, 3, dims, strides, box)) != cudaSuccess) return e;
     }
     {
@@ -639,7 +652,7 @@ cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, cons
     {
         const uint64_t dims[4] = {D, (uint64_t)p.H, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.H * D * esz, (uint64_t)p.S * p.H * D * esz};
-        const uint32_t box[4] = {64, 1, (uint32_t)kTile, 1};
+        const uint32_t box[4] = {64, 1, (uint32_t)kTile / 2, 1};
         if ((e = encode_tmap_bf16(&m.dout, dout, 4, dims, strides, box)) != cudaSuccess) return e;
     }
     return cudaSuccess;
