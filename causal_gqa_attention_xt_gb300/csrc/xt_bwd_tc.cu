@@ -32,9 +32,15 @@
 // then S^T/dP^T of the same half of the next tile: the tensor core works on one
 // half while the other half's softmax runs. One thread's tcgen05.mma
 // operations execute in issue order, so the next tile's S/dP cannot overwrite
-// P/dS before they are read. (In the dQ kernel the S/dP MMAs are TS-form, which
-// at N = 64 runs well below the full rate: it keeps full 128-key tiles and one
-// "P ready" barrier for all four warpgroups.)
+// P/dS before they are read.
+//
+// dQ pipeline: the S/dP MMAs are TS-form (Qhat and dO of the owned rows are
+// TMEM-resident A operands), which at N = 64 runs well below the full rate, so
+// the tiles stay whole. Each warpgroup writes its packed dS over its own dP
+// columns; as soon as every softmax thread holds S(t) and dP(t) in registers,
+// the MMA thread issues S(t+1) (it runs during the softmax of t), and once
+// dS(t) is in TMEM, dQ(t) followed by dP(t+1), which in issue order cannot
+// overwrite dS(t) before dQ(t) has read it.
 //
 // An mbarrier poll right after tcgen05.commit stalls the issuing thread until
 // earlier MMAs drain, so the TMA-arrival check for the next tile is done by the
@@ -431,6 +437,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int b = bh / H, h = bh - b * H, g = h / (H / G);
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
+    // p_full[0]: packed dS of tile t in TMEM; p_full[1]: every softmax thread
+    // has S(t) and dP(t) in registers (the S columns may be overwritten)
+    uint64_t *ds_ready = &bars.p_full[0];
+    uint64_t *sdp_taken = &bars.p_full[1];
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST, false);
     if (warp == kWarpMma) {
@@ -477,34 +487,50 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
             // S = Qhat Khat^T and dP = dO V^T (A in TMEM), full 128-key tiles: the
             // TS form at N = 128 runs at the full MMA rate (N = 64 does not)
-            auto issue_sp = [&](int t) {
+            auto issue_s = [&](int t) {
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off(kk), idesc_s, kk > 0);
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off(kk), idesc_s,
                            kk > 0);
-                mma_commit(&bars.s_full[0]);
+                mma_commit(&bars.s_full[0]);         // S and dP of tile t are in TMEM
             };
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
                       mbar_wait(&bars.st_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_sp(0);
+                issue_s(0);
+                issue_dp(0);
             }
+            // Per tile t: once the softmax warps hold S(t) and dP(t) in registers,
+            // S(t+1) is issued (it runs during the softmax of t); once dS(t) is
+            // packed over the dP columns, dQ(t) and then dP(t+1), which in issue
+            // order cannot overwrite dS(t) before dQ(t) has read it.
             for (int t = 0; ok && t < T; ++t) {
                 const int st = t % ST;
                 const uint64_t so = (uint64_t)st * kStep;
-                if (!(ok = mbar_wait(&bars.p_full[0], t & 1, abort_flag))) break;
+                if (t + 1 < T) {
+                    if (!(ok = mbar_wait(sdp_taken, t & 1, abort_flag) &&
+                               mbar_wait(&bars.st_full[(t + 1) % ST], ((t + 1) / ST) & 1,
+                                         abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                }
+                if (!(ok = mbar_wait(ds_ready, t & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts(tmem + 256, tmem + packed_col(kk), dKm0 + so + mnmajor_off(kk),
+                    mma_ts(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars.st_empty[st]);
-                if (t + 1 < T) issue_sp(t + 1);       // operands checked by the softmax warps
+                if (t + 1 < T) issue_dp(t + 1);
             }
             if (ok) mma_commit(&bars.acc_done);
             else if (!*abort_flag) raise_error_b(err, abort_flag);
@@ -554,6 +580,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             {
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_sync(tS, sv, tP, dpv);
+                tc_fence_before();
+                mbar_arrive(sdp_taken);                 // S(t+1) may now be issued
                 // only tiles that reach past the owned rows' diagonal take the select
                 auto body = [&](auto masked) {
 #pragma unroll
@@ -573,14 +601,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 if (interior) body(std::false_type{});
                 else body(std::true_type{});
             }
-            if (t + 1 < T) {   // operands of tile t+1, issued right behind this tile's dQ
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(t + 1) % ST],
-                                                       ((t + 1) / ST) & 1, abort_flag));
-                if (!ok) break;
-            }
-            tmem_st16_sync(tS, dd);
+            tmem_st16_sync(tP, dd);                     // packed dS over this warpgroup's dP columns
             tc_fence_before();
-            mbar_arrive(&bars.p_full[0]);
+            mbar_arrive(ds_ready);
         }
         if (ok) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
