@@ -71,6 +71,11 @@ SMALL = [
     Workload("s17_f32", 1, 17, 4, 2, 32, 1e4, 1e-5, "f32"),
     Workload("ragged_d128_f32", 1, 130, 2, 1, 128, 1e6, 1e-6, "f32"),
     Workload("d8_group1_f32", 2, 37, 3, 3, 8, 1e4, 1e-5, "f32"),
+    # head counts whose per-position chunks in the streaming kernels are uneven
+    # (a q chunk and a k chunk of different sizes, a partial q chunk)
+    Workload("chunks_h20_g5_bf16", 1, 150, 20, 5, 64, 1e4, 1e-5, "bf16"),
+    Workload("chunks_h48_g16_d128_bf16", 1, 140, 48, 16, 128, 1e6, 1e-6, "bf16"),
+    Workload("chunks_h12_g4_f32", 1, 70, 12, 4, 64, 1e4, 1e-5, "f32"),
 ]
 
 
@@ -232,3 +237,39 @@ def test_mqa_long_full_size_rows_and_sum_rule():
     dv_total = as_f64(g["dv"])[0, :, 0].sum(0)
     do_total = x["dout"][0].sum((0, 1))
     assert max_rel_err(dv_total, do_total) <= tol
+
+
+def test_positions_past_two_to_the_21():
+    """RoPE angles of positions >= 2^21 are formed in double, below in fp32 with
+    a compensated product: rows on both sides of the switch against the oracle
+    (norm + RoPE of single rows, attention rows over the whole prefix)."""
+    S = (1 << 21) + 192
+    w = Workload("positions_2p21_bf16", 1, S, 1, 1, 64, 1e6, 1e-6, "bf16")
+    tol = TOL[w.dtype]
+    cpu = make_inputs(w)
+    f, g = run_gpu(w, cpu)
+    x = to_f64(cpu)
+    pos = np.array([0, 1, 5000, (1 << 21) - 1, 1 << 21, (1 << 21) + 1, S - 1])
+    for name, src, gam, got in [("q_hat", "q", "gamma_q", f["q_hat"]),
+                                ("k_hat", "k", "gamma_k", f["k_hat"])]:
+        y, _ = oracle.rmsnorm_rows(x[src][0, pos, 0], x[gam], w.eps)
+        ref = oracle.rope_rows(y, pos, w.theta)
+        assert_close(name, got[0, 0, torch.as_tensor(pos, device=got.device)], ref, tol)
+    rows = [(0, 0, int(t)) for t in (S - 1, (1 << 21) + 3, (1 << 21) - 2)]
+    o, lse = oracle.attn_fwd_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], w.eps,
+                                  w.theta, rows)
+    dq = oracle.attn_dq_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
+                             w.eps, w.theta, rows)
+    go = np.stack([as_f64(f["out"][0, t, 0]) for _, _, t in rows])
+    glse = np.array([float(f["lse"][0, 0, t]) for _, _, t in rows])
+    gdq = np.stack([as_f64(g["dq"][0, t, 0]) for _, _, t in rows])
+    assert max_rel_err(go, o) <= tol
+    assert max_rel_err(glse, lse) <= tol
+    assert max_rel_err(gdq, dq) <= tol
+    krows = [(0, 0, S - 1), (0, 0, (1 << 21) + 10)]
+    dk, dv = oracle.attn_dkdv_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
+                                   w.eps, w.theta, krows)
+    gdk = np.stack([as_f64(g["dk"][0, j, 0]) for _, _, j in krows])
+    gdv = np.stack([as_f64(g["dv"][0, j, 0]) for _, _, j in krows])
+    assert max_rel_err(gdk, dk) <= tol
+    assert max_rel_err(gdv, dv) <= tol
