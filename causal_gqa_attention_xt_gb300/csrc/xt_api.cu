@@ -43,7 +43,7 @@ const char *kKernelNames[KID_COUNT] = {
     "prologue_qknorm_rope", "fwd_simt_f32", "fwd_tcgen05_bf16", "bwd_pre_dlt",
     "bwd_dq_simt_f32",      "bwd_dkdv_simt_f32", "bwd_dq_tcgen05_bf16",
     "bwd_dkdv_tcgen05_bf16", "bwd_epilogue_rope_norm", "bwd_dgamma_reduce",
-    "rope_table"};
+    "rope_table", "decode_rows", "decode_attn", "decode_combine"};
 
 void drain_locked() {
     for (auto &p : g_timing.pending) {
@@ -270,6 +270,48 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     });
 }
 
+size_t xt_attn_decode_workspace_bytes(int B, int S_max, int n_heads, int n_kv_heads,
+                                      int head_dim, int dtype) {
+    if (validate_shape(B, S_max, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
+    return decode_plan(make_problem(B, S_max, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype)).total;
+}
+
+int xt_attn_decode(int B, int S_max, int n_heads, int n_kv_heads, int head_dim, double eps,
+                   double theta, const int *pos, const void *q, const void *k, const void *v,
+                   const float *gamma_q, const float *gamma_k, int dtype, void *k_cache,
+                   void *v_cache, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                   void *stream) {
+    int st = validate_shape(B, S_max, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    if (pos == nullptr || ((uintptr_t)pos & 3u) != 0) return XT_EINVAL;
+    const void *ptrs[] = {q, k, v, gamma_q, gamma_k, k_cache, v_cache, out, lse};
+    for (const void *ptr : ptrs)
+        if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
+    const Problem p = make_problem(B, S_max, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    const DecodePlan d = decode_plan(p);
+    if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < d.total)
+        return XT_EWORKSPACE;
+    char *ws = (char *)workspace;
+    float *qhat = (float *)(ws + d.off_qhat);
+    float *part_o = (float *)(ws + d.off_o);
+    float *part_ml = (float *)(ws + d.off_ml);
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned int *err = error_word_ptr();
+    if (!err) return cuda_fail(cudaGetLastError());
+    st = timed_launch(KID_DECODE_ROWS, s, [&] {
+        return launch_decode_rows(p, pos, q, k, v, gamma_q, gamma_k, qhat, k_cache, v_cache, err, s);
+    });
+    if (st != XT_OK) return st;
+    st = timed_launch(KID_DECODE_ATTN, s, [&] {
+        return launch_decode_attn(p, d, pos, qhat, k_cache, v_cache, part_o, part_ml, err, s);
+    });
+    if (st != XT_OK) return st;
+    return timed_launch(KID_DECODE_COMBINE, s, [&] {
+        return launch_decode_combine(p, d, part_o, part_ml, out, lse, s);
+    });
+}
+
 int xt_attn_check(void *stream) {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -280,7 +322,7 @@ int xt_attn_check(void *stream) {
         const unsigned int zero = 0;
         e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
         if (e != cudaSuccess) return cuda_fail(e);
-        return XT_ETIMEOUT;
+        return (word & ERR_TIMEOUT) ? XT_ETIMEOUT : XT_EINVAL;
     }
     return XT_OK;
 }

@@ -23,6 +23,9 @@ enum KernelId {
     KID_BWD_EPILOGUE,     // RoPE^-1 + RMSNorm backward, dgamma partials
     KID_DGAMMA_REDUCE,    // fixed-order sum of dgamma partials
     KID_ROPE_TABLE,       // cos/sin table of the RoPE angles
+    KID_DECODE_ROWS,      // decode: the new token's rows normed, rotated, cached
+    KID_DECODE_ATTN,      // decode: split attention over the cache
+    KID_DECODE_COMBINE,   // decode: fixed-order merge of the splits
     KID_COUNT
 };
 
@@ -34,8 +37,8 @@ struct Problem {
     int group() const { return H / G; }
 };
 
-// Error word bits raised by kernels whose bounded waits run out.
-enum : unsigned int { ERR_TIMEOUT = 1u };
+// Error word bits: a bounded wait ran out; a decode position was out of range.
+enum : unsigned int { ERR_TIMEOUT = 1u, ERR_BADPOS = 2u };
 
 // ---- norm / RoPE kernels (xt_normrope.cu) ----
 // Persistent grids: at most this many CTAs, which bounds the number of
@@ -62,6 +65,23 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
 cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
                                  int nparts_q, int nparts_k, float *dgq, float *dgk,
                                  cudaStream_t st);
+
+// ---- decode step against a key/value cache (xt_decode.cu) ----
+// Problem::S is the cache capacity S_max. The workspace holds the fp32 q rows
+// and the per-split partials.
+struct DecodePlan {
+    int nsplit, L, nhc;   // key splits, keys per split, query-head chunks per kv head
+    size_t off_qhat, off_o, off_ml, total;
+};
+DecodePlan decode_plan(const Problem &p);
+cudaError_t launch_decode_rows(const Problem &p, const int *pos, const void *q, const void *k,
+                               const void *v, const float *gq, const float *gk, float *qhat,
+                               void *kc, void *vc, unsigned int *err, cudaStream_t st);
+cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int *pos,
+                               const float *qhat, const void *kc, const void *vc, float *part_o,
+                               float *part_ml, unsigned int *err, cudaStream_t st);
+cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const float *part_o,
+                                  const float *part_ml, void *out, float *lse, cudaStream_t st);
 
 // ---- TMA tensor maps (xt_tmap.cu) ----
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,

@@ -31,14 +31,11 @@
 // elements of the first half of the row and the VEC matching elements of the
 // second half (the RoPE pair); a warp-iteration covers 32 / tpr heads.
 //
-// RoPE angles (rope_table): for positions below 2^21 the product pos * f is
-// formed in fp32 with f = theta^(-2i/D) split as hi + lo and the rounding
-// error of pos * hi recovered exactly by an fma, then reduced by 2*pi with
-// Cody and Waite's three-constant scheme; beyond 2^21 product and reduction
-// are done in double. The reduced angle (|r| <= pi + small, within a few fp32
-// ulps) goes to the fp32 sincosf.
+// RoPE angles: xt_rope.cuh (one table per call, read by the prologue and the
+// epilogue).
 #include "xt_common.cuh"
 #include "xt_internal.h"
+#include "xt_rope.cuh"
 #include "xt_tc.cuh"
 
 namespace xt {
@@ -56,15 +53,6 @@ using tc::mbar_wait_sleep;
 constexpr int kWarps = 8;                    // warps per CTA, each its own pipeline
 constexpr int kThreads = 32 * kWarps;
 constexpr int kCtasPerSm = 2;
-constexpr int kRopeFp32Limit = 1 << 21;      // positions with the fp32 angle path
-
-// 2*pi = kC1 + kC2 + kC3 (Cody-Waite): kC1 has 5 significant bits, so k * kC1
-// is exact for |k| < 2^19; kC2 and kC3 carry the rest.
-constexpr double kTwoPi = 6.283185307179586476925;
-constexpr float kC1 = 6.25f;
-constexpr float kC2 = (float)(kTwoPi - 6.25);
-constexpr float kC3 = (float)((kTwoPi - 6.25) - (double)kC2);
-constexpr float kInvTwoPi = (float)(1.0 / kTwoPi);
 
 __host__ __device__ inline int pow2_at_least(int x) {
     int p = 1;
@@ -95,19 +83,11 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
 }
 
 // ---------------------------------------------------------------- RoPE table
-// Inverse frequencies theta^(-2i/D), formed on the host in double; fhi + flo
-// is that double to ~48 bits.
-constexpr int kMaxHalf = 64;   // D / 2 for D <= 128
-struct RopeConsts {
-    float fhi[kMaxHalf], flo[kMaxHalf];
-    double fd[kMaxHalf];
-};
-
 // tab[s * half + i] = (cos, sin) of s * theta^(-2i/D), s < S, i < half.
 __global__ void __launch_bounds__(256)
 k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ RopeConsts rc) {
-    __shared__ float fhi[kMaxHalf], flo[kMaxHalf];
-    __shared__ double fd[kMaxHalf];
+    __shared__ float fhi[kRopeMaxHalf], flo[kRopeMaxHalf];
+    __shared__ double fd[kRopeMaxHalf];
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
         fhi[i] = rc.fhi[i];
         flo[i] = rc.flo[i];
@@ -118,23 +98,7 @@ k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ 
     for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long)gridDim.x * blockDim.x) {
         const int s = (int)(e / half), i = (int)(e - (long)s * half);
-        float red;
-        if (s < kRopeFp32Limit) {
-            const float fs = (float)s;   // exact
-            const float hi = fhi[i];
-            const float p = __fmul_rn(fs, hi);
-            const float tail = fmaf(fs, flo[i], fmaf(fs, hi, -p));   // s * f - p
-            const float k = rintf(p * kInvTwoPi);
-            float r = fmaf(-k, kC1, p);   // exact
-            r = fmaf(-k, kC2, r);
-            red = __fadd_rn(r, fmaf(-k, kC3, tail));
-        } else {
-            const double ang = (double)s * fd[i];
-            red = (float)fma(-rint(ang * (1.0 / kTwoPi)), kTwoPi, ang);
-        }
-        float sv, cv;
-        sincosf(red, &sv, &cv);
-        tab[e] = make_float2(cv, sv);
+        tab[e] = rope_cos_sin(s, fhi[i], flo[i], fd[i]);
     }
 }
 
@@ -573,16 +537,6 @@ k_dgamma_reduce(const float *__restrict__ part_q, const float *__restrict__ part
 }
 
 // ---------------------------------------------------------------- host side
-RopeConsts rope_consts(const Problem &p) {
-    RopeConsts f = {};
-    for (int i = 0; i < p.D / 2 && i < kMaxHalf; ++i) {
-        const double v = pow(p.theta, -2.0 * (double)i / (double)p.D);
-        f.fd[i] = v;
-        f.fhi[i] = (float)v;
-        f.flo[i] = (float)(v - (double)f.fhi[i]);
-    }
-    return f;
-}
 
 // Units over H q heads and G k heads (G = 0: q only), one position each. A
 // stage holds HC rows of x_row + y_row + r_row bytes (and a cos/sin row with
@@ -646,7 +600,7 @@ cudaError_t launch_rope_table(const Problem &p, void *tab, cudaStream_t st) {
     const long n = (long)p.S * (p.D / 2);
     long blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    k_rope_table<<<(unsigned)blocks, 256, 0, st>>>((float2 *)tab, p.S, p.D / 2, rope_consts(p));
+    k_rope_table<<<(unsigned)blocks, 256, 0, st>>>((float2 *)tab, p.S, p.D / 2, make_rope_consts(p.theta, p.D));
     return cudaGetLastError();
 }
 

@@ -55,6 +55,11 @@ def lib():
     L.xt_attn_bwd_noalloc.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
                                       vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.xt_attn_bwd_noalloc.restype = i
+    L.xt_attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
+    L.xt_attn_decode_workspace_bytes.restype = sz
+    L.xt_attn_decode.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
+                                 vp, sz, vp]
+    L.xt_attn_decode.restype = i
     L.xt_attn_check.argtypes = [vp]
     L.xt_attn_check.restype = i
     L.xt_status_str.argtypes = [i]
@@ -188,8 +193,42 @@ def xt_attn_bwd_noalloc(q, k, v, gamma_q, gamma_k, saved, dout, eps, theta, *, d
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
 
 
+def xt_attn_decode_workspace_bytes(B, S_max, n_heads, n_kv_heads, head_dim, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().xt_attn_decode_workspace_bytes(B, S_max, n_heads, n_kv_heads, head_dim, code))
+
+
+def xt_attn_decode(pos, q, k, v, gamma_q, gamma_k, k_cache, v_cache, eps, theta, *, out=None,
+                   lse=None, workspace=None, stream=None):
+    """One decode step: the new token of each batch element (q [B, H, D], k and v
+    [B, G, D]) at position pos[b] (int32 CUDA tensor [B]) is appended to the
+    caches (k_cache, v_cache [B, G, S_max, D], updated in place) and attends over
+    rows 0..pos[b]. Returns dict(out [B, H, D], lse [B, H] fp32)."""
+    B, H, D = q.shape
+    G = k.shape[1]
+    S_max = k_cache.shape[2]
+    if pos.dtype != torch.int32 or pos.numel() != B:
+        raise ValueError("pos must be an int32 tensor of B positions")
+    dev = q.device
+    code = _dtype_code(q.dtype)
+    out = out if out is not None else torch.empty_like(q)
+    lse = lse if lse is not None else torch.empty(B, H, device=dev, dtype=torch.float32)
+    need = xt_attn_decode_workspace_bytes(B, S_max, H, G, D, code)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    wbytes = workspace.numel() * workspace.element_size()
+    st = lib().xt_attn_decode(B, S_max, H, G, D, float(eps), float(theta), _ptr(pos), _ptr(q),
+                              _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), code,
+                              _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse),
+                              _ptr(workspace), wbytes, _stream(stream))
+    if st != XT_OK:
+        raise XtError(st, "xt_attn_decode")
+    return dict(out=out, lse=lse)
+
+
 def xt_attn_check(stream=None) -> int:
-    """Synchronizes the stream and returns the library's device status (XT_OK / XT_ETIMEOUT)."""
+    """Synchronizes the stream and returns the library's device status
+    (XT_OK, XT_ETIMEOUT, or XT_EINVAL for an out-of-range decode position)."""
     return int(lib().xt_attn_check(_stream(stream)))
 
 

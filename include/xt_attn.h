@@ -136,8 +136,44 @@ int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                         void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
                         void *stream);
 
+/* ---------------------------------------------------------------- decode
+ * One decode step against a key/value cache (Mint project report, 10.3 "KV
+ * cache": the new token computes its own q, k, v, appends k and v to the
+ * cache, and its query attends over every cached key, all of which are at or
+ * before it, so the mask is implicit; the page states this equals the
+ * full-sequence attention at that row).
+ *
+ * For each batch element b, with p = pos[b] (device memory, int32 [B]):
+ *  - k_cache[b, g, p, :] = rope(norm(k[b, g]) * gamma_k, p) and
+ *    v_cache[b, g, p, :] = v[b, g] for every kv head g (the rows the
+ *    training forward writes to k_hat, and v, at position p);
+ *  - out[b, h] = sum_{j <= p} softmax_j(q_hat . k_cache[b, h/group, j] /
+ *    sqrt(head_dim)) v_cache[b, h/group, j] with q_hat = rope(norm(q[b, h]) *
+ *    gamma_q, p), and lse[b, h] its natural-log log-sum-exp.
+ * Rows 0..p-1 of the caches must hold the earlier tokens (e.g. the k_hat of a
+ * training-style forward over the prompt, and v transposed to the cache
+ * layout); rows after p are not read.
+ *
+ * Layouts: q [B, H, D], k and v [B, G, D] (the new token; input dtype),
+ * k_cache and v_cache [B, G, S_max, D] (head-major, dtype), out [B, H, D]
+ * (dtype), lse [B, H] fp32, gamma_q / gamma_k [D] fp32. Same dtype and
+ * head_dim rules as xt_attn_fwd. The workspace must hold
+ * xt_attn_decode_workspace_bytes() bytes. A position outside [0, S_max) is
+ * detected on the device: that batch element is skipped and xt_attn_check()
+ * reports XT_EINVAL. Deterministic: the key splits are merged in a fixed
+ * order. */
+size_t xt_attn_decode_workspace_bytes(int B, int S_max, int n_heads, int n_kv_heads, int head_dim,
+                                      int dtype);
+int xt_attn_decode(int B, int S_max, int n_heads, int n_kv_heads, int head_dim,
+                   double eps, double theta, const int *pos,
+                   const void *q, const void *k, const void *v,
+                   const float *gamma_q, const float *gamma_k, int dtype,
+                   void *k_cache, void *v_cache, void *out, float *lse,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
 /* Synchronizes `stream`, then reads and clears the device error word of the
- * current device: XT_OK, XT_ETIMEOUT (a bounded wait ran out) or XT_ECUDA. */
+ * current device: XT_OK, XT_ETIMEOUT (a bounded wait ran out), XT_EINVAL (a
+ * decode position was out of range) or XT_ECUDA. */
 int xt_attn_check(void *stream);
 
 /* Human-readable name of an xt_status value (static storage). */

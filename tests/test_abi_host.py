@@ -99,3 +99,19 @@ def test_timing_hooks_without_launches(L):
 def test_head_count_limit(L):
     # n_heads + n_kv_heads above 8192 is refused before any launch
     assert _fwd(L, H=8192, G=1) == xt.XT_EUNSUPPORTED
+
+
+def test_decode_validation_and_workspace(L):
+    p = ctypes.c_void_p(16)
+    need = xt.xt_attn_decode_workspace_bytes(2, 64, 4, 2, 16, 0)
+    assert need > 0 and need % 256 == 0
+    assert xt.xt_attn_decode_workspace_bytes(2, 64, 3, 2, 16, 0) == 0
+    assert xt.xt_attn_decode_workspace_bytes(2, 64, 4, 2, 32, 1) == 0   # bf16 wants D 64 / 128
+    args = [2, 64, 4, 2, 16, 1e-5, 1e4]
+    tail = [p] * 5 + [0] + [p] * 4
+    assert L.xt_attn_decode(*args, p, *tail, p, need - 1, None) == xt.XT_EWORKSPACE
+    assert L.xt_attn_decode(*args, None, *tail, p, need, None) == xt.XT_EINVAL      # no positions
+    assert L.xt_attn_decode(*args, ctypes.c_void_p(18), *tail, p, need, None) == xt.XT_EINVAL
+    bad = list(args)
+    bad[2] = 3
+    assert L.xt_attn_decode(*bad, p, *tail, p, need, None) == xt.XT_EINVAL
