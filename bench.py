@@ -9,6 +9,12 @@ per-step CUDA events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle timed on host cores
+  python bench.py --mode decode ...      # one decode step against a full KV cache
+
+In decode mode a step is one xt_attn_decode call: every sequence's next token
+against a cache that holds its whole capacity (the largest cache read), and
+the metric is the cache bytes read per second (K-hat and V rows, the algorithmic
+bytes of the step); the cache is larger than L2, so no flush is needed.
 
 Under torchrun (N > 1) every rank runs its own shard of independent batch
 units on its own GPU (weak scaling, no collective on the data path); rank 0
@@ -31,6 +37,9 @@ sys.path.insert(0, ROOT)
 METRIC = "causal GQA attention fwd+bwd TFLOP/s at 1 GB300 and % of dense BF16 peak"
 UNIT = "TFLOP/s"
 DEFAULT_WORKLOAD = "qwen3_like_bf16"
+DECODE_METRIC = ("GQA decode step (each sequence's next token against its full KV cache): "
+                 "cache bytes read per second at 1 GB300")
+DECODE_WORKLOAD = "qwen3_like_decode_bf16"
 
 
 def load_peaks():
@@ -415,6 +424,230 @@ def bench_ours(args, w):
     return 0
 
 
+def decode_bytes(w):
+    """Algorithmic bytes of one decode step with every cache full: the K-hat and V
+    rows of every (sequence, kv head) read once."""
+    esz = 2 if w.dtype == "bf16" else 4
+    return 2 * w.B * w.G * w.S * w.D * esz
+
+
+def decode_oracle_sample(w):
+    """The oracle on one sequence of the decode workload: every query head of the
+    last position over the whole prefix (raw q, k, v; norm and RoPE inside)."""
+    from causal_gqa_attention_xt_gb300.inputs import make_inputs, to_f64
+    sub = w.with_(B=1)
+    x = to_f64(make_inputs(sub))
+    rows = [(0, h, w.S - 1) for h in range(w.H)]
+    return sub, x, rows
+
+
+def run_decode_oracle(sub, x, rows, threads, reps):
+    """reps decode steps of one sequence each (the same synthetic sequence)."""
+    import oracle
+    for _ in range(reps):
+        oracle.attn_fwd_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], sub.eps,
+                             sub.theta, rows, nthreads=threads)
+
+
+def decode_sample_desc(w, reps):
+    return (f"{reps} sequence-steps of {w.S} cached positions each (the {w.H} query heads of "
+            f"the last position, G={w.G}, D={w.D}): oracle single-row attention in fp64, "
+            f"bytes counted as the GPU step's per sequence")
+
+
+def decode_cpu_baseline(w, seconds_target=10.0):
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    sub, x, rows = decode_oracle_sample(w)
+    t0 = time.perf_counter()
+    run_decode_oracle(sub, x, rows, cores, 1)
+    one = max(time.perf_counter() - t0, 1e-4)
+    reps = max(1, int(seconds_target / one))
+    t0 = time.perf_counter()
+    run_decode_oracle(sub, x, rows, cores, reps)
+    dt_s = time.perf_counter() - t0
+    return {"value": reps * decode_bytes(w) / w.B / dt_s / 1e9, "unit": "GB/s",
+            "cores": min(cores, len(rows)), "kind": "oracle", "sample": decode_sample_desc(w, reps),
+            "seconds": dt_s}
+
+
+def bench_decode(args, w):
+    import torch
+    import torch.distributed as dist
+
+    from causal_gqa_attention_xt_gb300 import build as xbuild
+    from causal_gqa_attention_xt_gb300 import xt
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    xbuild.build()
+    xt.lib()
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    seed = shard_seed(w.seed, rank)
+    gen_dev = torch.Generator(device=dev).manual_seed(seed)
+    gen = torch.Generator().manual_seed(seed)
+    # a full cache of synthetic rows (N(0,1); the step's cost does not depend on the values)
+    kc = torch.randn(w.B, w.G, w.S, w.D, generator=gen_dev, device=dev).to(dt)
+    vc = torch.randn(w.B, w.G, w.S, w.D, generator=gen_dev, device=dev).to(dt)
+    host = {"q": torch.randn(w.B, w.H, w.D, generator=gen).to(dt),
+            "k": torch.randn(w.B, w.G, w.D, generator=gen).to(dt),
+            "v": torch.randn(w.B, w.G, w.D, generator=gen).to(dt)}
+    gq = (1 + 0.1 * torch.randn(w.D, generator=gen)).to(dev)
+    gk = (1 + 0.1 * torch.randn(w.D, generator=gen)).to(dev)
+    d = {k_: v_.to(dev) for k_, v_ in host.items()}
+    pos = torch.full((w.B,), w.S - 1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty(w.B, w.H, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, xt.xt_attn_decode_workspace_bytes(w.B, w.S, w.H, w.G, w.D,
+                                                                1 if w.dtype == "bf16" else 0)),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        xt.xt_attn_decode(pos, d["q"], d["k"], d["v"], gq, gk, kc, vc, w.eps, w.theta, out=out,
+                          lse=lse, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if xt.xt_attn_check() != xt.XT_OK:
+        raise RuntimeError("device error flag raised during warm-up")
+    clocks = ClockSampler(gpu_pci_id(torch))
+    clocks.start()
+    time.sleep(0.4)
+    xt.xt_timing_reset()
+    xt.xt_timing_enable(True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    xt.xt_timing_enable(False)
+    per_kernel = xt.xt_timing_query()
+    clk = clocks.stop()
+    if xt.xt_attn_check() != xt.XT_OK:
+        raise RuntimeError("device error flag raised during the timed steps")
+    step_ms = reduce_max([sum(a.elapsed_time(b) for a, b in ev) / args.steps], dev)[0]
+
+    # end to end: the new rows in from pinned host memory, out and lse back
+    pin = {k_: v_.pin_memory() for k_, v_ in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(v_.numel() * v_.element_size() for v_ in pin.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        for k_, v_ in pin.items():
+            d[k_].copy_(v_, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+    for i in range(args.steps):
+        e2e_ev[i][0].record(stream)
+        e2e_step()
+        e2e_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max([sum(a.elapsed_time(b) for a, b in e2e_ev) / args.steps], dev)[0]
+
+    nbytes = decode_bytes(w)
+    value = world * nbytes / (step_ms * 1e-3) / 1e9
+    peaks = load_peaks()
+    roofline = None
+    if "decode_attn" in per_kernel:
+        tot_ms, n = per_kernel["decode_attn"]
+        ach = nbytes / (tot_ms / n * 1e-3) / 1e9
+        roofline = {"kernel": "decode_attn", "bound": "hbm", "achieved": ach,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": ach / peaks["hbm_gbs"],
+                    "peak_source": f"{peaks['source']} copy", "traffic": None,
+                    "avg_launch_ms": tot_ms / n}
+        traffic_file = os.path.join(ROOT, "profiles", "traffic.json")
+        try:
+            with open(traffic_file) as f:
+                ent = json.load(f).get("decode_attn", {})
+            if ent.get("workload") == w.name and ent.get("source_hash") == source_hash():
+                roofline["traffic"] = ent.get("bytes_per_launch")
+        except (OSError, ValueError):
+            pass
+    line = {
+        "metric": DECODE_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "sequences": w.B, "cache_rows": w.S, "position": w.S - 1,
+                   "n_heads": w.H, "n_kv_heads": w.G, "head_dim": w.D, "theta": w.theta,
+                   "eps": w.eps, "cache_bytes_read_per_step": nbytes,
+                   "l2": "not flushed: the caches are larger than L2",
+                   "inputs": "N(0,1) cache rows and new rows, gammas 1+0.1*N(0,1), seed 0+rank"},
+        "tokens_per_s": world * w.B / (step_ms * 1e-3),
+        "roofline": roofline,
+        "kernels": {k_: {"total_ms": v_[0], "launches": v_[1]} for k_, v_ in per_kernel.items()},
+        "e2e": {"value": world * nbytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(n for _, n in per_kernel.values()),
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(w)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def bench_decode_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    cores = host_cores()
+    sub, x, rows = decode_oracle_sample(w)
+    reps = 8   # sequence-steps per timed step, about half a second of oracle work
+    for _ in range(args.warmup):
+        run_decode_oracle(sub, x, rows, cores, reps)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run_decode_oracle(sub, x, rows, cores, reps)
+        times.append(time.perf_counter() - t0)
+    value = reps * decode_bytes(w) / w.B * len(times) / sum(times) / 1e9
+    desc = decode_sample_desc(w, reps)
+    line = {
+        "impl": "reference", "metric": DECODE_METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * sum(times) / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "sequences": w.B, "cache_rows": w.S, "n_heads": w.H,
+                   "n_kv_heads": w.G, "head_dim": w.D, "sample_per_step": desc},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": min(cores, len(rows)),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def profile_run(w):
     """One warm-up and one measured-shape fwd+bwd step (launch order: prologue,
     fwd, bwd_pre, dkdv, dq, epilogue, dgamma_reduce, twice), for ncu."""
@@ -452,7 +685,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--mode", choices=["train", "decode"], default="train",
+                    help="train: fwd+bwd step (the headline); decode: one KV-cache decode step")
+    ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=1024,
                     help="sequence length of the oracle's per-step sample (reference arm)")
@@ -461,13 +696,15 @@ def main(argv=None):
                     help="one warm-up and one fwd+bwd step, no timing (for ncu captures)")
     args = ap.parse_args(argv)
     from causal_gqa_attention_xt_gb300.inputs import WORKLOADS
-    w = WORKLOADS[args.workload]
+    w = WORKLOADS[args.workload or (DECODE_WORKLOAD if args.mode == "decode" else DEFAULT_WORKLOAD)]
     if args.batch is not None:
         w = w.with_(B=args.batch, name=f"{w.name}_B{args.batch}")
     if args.profile_run:
         return profile_run(w)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.mode == "decode":
+        return bench_decode_reference(args, w) if args.impl == "reference" else bench_decode(args, w)
     if args.impl == "reference":
         return bench_reference(args, w)
     return bench_ours(args, w)

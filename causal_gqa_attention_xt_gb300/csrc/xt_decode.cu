@@ -20,12 +20,19 @@
 //    rows copied into the v cache. A position outside [0, S_max) raises an
 //    error bit (reported as XT_EINVAL by xt_attn_check) and the batch element
 //    is skipped.
-//  * k_decode_attn: grid (kv head x chunk of <= 16 of its query heads, key
-//    split). A CTA streams its split's cached rows, 64 keys per tile, through
-//    a 2-stage shared-memory ring filled by bulk asynchronous copies; one
-//    thread per (head, key) forms the score over D, one warp per head keeps
-//    the running max and sum, one thread per (head, column) accumulates P V.
-//    It writes the split's partial (max, sum, unnormalised output).
+//  * k_decode_attn: work unit = (b, kv head, chunk of <= 4 of its query
+//    heads, key split); a CTA's warps run units independently, each on its own
+//    ring of 3 shared-memory stages (a stage = 16 cached K-hat rows and the same
+//    V rows, two bulk asynchronous copies) that its lane 0 refills as soon as
+//    the warp is done with a stage, running ahead across unit boundaries.
+//    Lanes: lane / 8 picks one key of each group of four, lane % 8 the 16-byte
+//    chunks lane % 8, lane % 8 + 8, ... of the row, so a quarter warp reads one
+//    row's 128 contiguous bytes (no bank conflicts). The four heads' partial
+//    dot products are summed over the 8 lanes of a key by a transposing
+//    butterfly (each step halves the values a lane carries), the online softmax
+//    runs on the result (one (key, head pair) per lane), and P V accumulates
+//    in registers (4 heads x the lane's columns), fp32 pairs through the packed
+//    fp32 FMA. It writes the unit's partial (max, sum, unnormalised output).
 //  * k_decode_combine: per (b, h), the splits merged in split order, so the
 //    result does not depend on scheduling: m = max m_s, l = sum l_s 2^(m_s-m),
 //    o = sum o_s 2^(m_s-m) / l; lse = (m + log2 l) ln 2 (natural log).
@@ -42,12 +49,15 @@ using tc::bulk_load;
 using tc::mbar_expect_tx;
 using tc::mbar_init;
 using tc::mbar_wait;
+using tc::mbar_wait_sleep;
 
-constexpr int kDecThreads = 256;
-constexpr int kDecKeys = 64;        // keys per staged tile
-constexpr int kDecHeads = 16;       // query heads per CTA (a chunk of the group)
-constexpr int kDecStages = 2;
-constexpr int kDecAcc = kDecHeads * 128 / kDecThreads;   // outputs per thread (D <= 128)
+constexpr int kDecKT = 16;   // keys per stage: four passes of four keys
+constexpr int kDecHP = 4;    // query heads per work unit
+constexpr int kDecNS = 3;    // stages per warp
+
+// Warps per CTA: one CTA per SM with 3 stages per warp, 192 KB of stages at
+// D = 128 (8 KB stages in bf16, 16 KB in fp32).
+template <typename T> __host__ __device__ constexpr int dec_warps() { return sizeof(T) == 2 ? 8 : 4; }
 
 // ---------------------------------------------------------------- new rows
 template <typename T>
@@ -115,150 +125,317 @@ k_decode_rows(const int *__restrict__ pos, const T *__restrict__ q, const T *__r
 }
 
 // ---------------------------------------------------------------- attention
+template <typename T, int DP>
+struct DecLane {
+    static constexpr int VEC = 16 / (int)sizeof(T);   // elements per 16-byte chunk
+    static constexpr int CPL = DP / VEC / 8;          // chunks per lane
+    static constexpr int P2 = CPL * VEC / 2;          // fp32 pairs per lane
+};
+
+// a += b * c on two fp32 lanes at once (the packed fp32 FMA of sm_100 on)
+__device__ __forceinline__ void fma2(float2 &a, const float2 b, const float2 c) {
+    asm("{\n .reg .b64 ra, rb, rc;\n"
+        " mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n mov.b64 rc, {%4, %5};\n"
+        " fma.rn.f32x2 ra, rb, rc, ra;\n mov.b64 {%0, %1}, ra;\n}\n"
+        : "+f"(a.x), "+f"(a.y)
+        : "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+}
+
+// 16 bytes of shared memory as fp32 pairs (bf16 widened exactly)
 template <typename T>
-__global__ void __launch_bounds__(kDecThreads, 2)
+__device__ __forceinline__ void lds_pairs(const T *p, float2 *dst) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(p);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    if constexpr (sizeof(T) == 4) {
+        dst[0] = make_float2(__uint_as_float(w[0]), __uint_as_float(w[1]));
+        dst[1] = make_float2(__uint_as_float(w[2]), __uint_as_float(w[3]));
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            dst[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+    }
+}
+
+struct DecUnit {
+    int b, g, hc, split, k0, k1, nt;   // keys [k0, k1) in nt stages
+};
+
+__device__ __forceinline__ DecUnit dec_unit(int u, const int *pos, int S_max, int G, int L,
+                                            int nsplit, int nhc) {
+    DecUnit U;
+    U.hc = u % nhc;
+    const int t = u / nhc;
+    U.split = t % nsplit;
+    const int bg = t / nsplit;
+    U.g = bg % G;
+    U.b = bg / G;
+    const int p = pos[U.b];
+    U.k0 = U.split * L;
+    U.k1 = (p >= 0 && p < S_max) ? min(U.k0 + L, p + 1) : U.k0;
+    U.nt = U.k1 > U.k0 ? (U.k1 - U.k0 + kDecKT - 1) / kDecKT : 0;
+    return U;
+}
+
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return make_float2(a.x + b.x, a.y + b.y); }
+__device__ __forceinline__ float2 shfl_xor2(float2 v, int m) {
+    return make_float2(__shfl_xor_sync(0xffffffffu, v.x, m), __shfl_xor_sync(0xffffffffu, v.y, m));
+}
+
+// FULL: D == DP (every lane chunk lies inside the row)
+template <typename T, int DP, bool FULL>
+__global__ void __launch_bounds__(dec_warps<T>() * 32, 1)
 k_decode_attn(const int *__restrict__ pos, const float *__restrict__ qhat,
               const T *__restrict__ kc, const T *__restrict__ vc, float *__restrict__ part_o,
-              float *__restrict__ part_ml, int B, int S_max, int H, int G, int D, int L, int nhc,
-              unsigned int *err) {
-    constexpr int VEC = 16 / sizeof(T);
+              float *__restrict__ part_ml, int B, int S_max, int H, int G, int D, int L,
+              int nsplit, int nhc, int units, unsigned int *err) {
+    using LG = DecLane<T, DP>;
+    constexpr int VEC = LG::VEC, CPL = LG::CPL, P2 = LG::P2;
+    constexpr int HP = kDecHP, KT = kDecKT, NS = kDecNS, WARPS = dec_warps<T>();
+    constexpr unsigned FULLMASK = 0xffffffffu;
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ uint64_t full[kDecStages];
-    __shared__ float m_run[kDecHeads], l_run[kDecHeads], alpha[kDecHeads];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hc = blockIdx.x % nhc;
-    const int bg = blockIdx.x / nhc;
-    const int g = bg % G, b = bg / G;
-    const int split = blockIdx.y;
+    __shared__ uint64_t full[WARPS][NS];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int gw = warp * (int)gridDim.x + (int)blockIdx.x;   // units spread over CTAs first
+    const int TW = (int)gridDim.x * WARPS;
+    if (gw >= units) return;
+    const int kq = lane >> 3, j = lane & 7;
     const int group = H / G;
-    const int h0 = g * group + hc * kDecHeads;
-    const int nh = min(kDecHeads, group - hc * kDecHeads);
-    const int rowb = D * (int)sizeof(T);
-    const int tile_bytes = kDecKeys * rowb;
-    unsigned char *ring = smem;                                         // [stage][K | V]
-    float *qs = reinterpret_cast<float *>(smem + kDecStages * 2 * tile_bytes);   // [head][D]
-    float *sp = qs + kDecHeads * D;                                     // [head][key]
-
-    const int p = pos[b];
-    const bool valid = p >= 0 && p < S_max;
-    const int k0 = split * L;
-    const int k1 = valid ? min(k0 + L, p + 1) : k0;                     // keys [k0, k1)
-    const int ntiles = k1 > k0 ? (k1 - k0 + kDecKeys - 1) / kDecKeys : 0;
-    const size_t crow0 = ((size_t)b * G + g) * S_max;
-
-    if (tid == 0) {
-        for (int st = 0; st < kDecStages; ++st) mbar_init(&full[st], 1);
+    const int rowe = D;                                        // elements per cached row
+    const uint32_t rowb = (uint32_t)(D * (int)sizeof(T));
+    const uint32_t stage_bytes = 2u * KT * rowb;
+    unsigned char *ring = smem + (size_t)warp * NS * stage_bytes;
+    uint64_t *bar = full[warp];
+    if (lane == 0) {
+        for (int st = 0; st < NS; ++st) mbar_init(&bar[st], 1);
         tc::fence_barrier_init();
     }
-    for (int e = tid; e < nh * D; e += kDecThreads) qs[e] = qhat[((size_t)b * H + h0) * D + e];
-    if (tid < kDecHeads) {
-        m_run[tid] = -INFINITY;
-        l_run[tid] = 0.f;
-    }
-    __syncthreads();
-    auto issue = [&](int i) {   // thread 0
-        const int st = i % kDecStages;
-        const int ks = k0 + i * kDecKeys, n = min(kDecKeys, k1 - ks);
-        unsigned char *base = ring + st * 2 * tile_bytes;
-        mbar_expect_tx(&full[st], (uint32_t)(2 * n * rowb));
-        bulk_load(base, kc + (crow0 + ks) * D, (uint32_t)(n * rowb), &full[st]);
-        bulk_load(base + tile_bytes, vc + (crow0 + ks) * D, (uint32_t)(n * rowb), &full[st]);
-    };
-    if (tid == 0)
-        for (int i = 0; i < ntiles && i < kDecStages; ++i) issue(i);
+    __syncwarp();
 
-    float acc[kDecAcc];
-#pragma unroll
-    for (int r = 0; r < kDecAcc; ++r) acc[r] = 0.f;
-    const float sl2 = kLog2e * rsqrtf((float)D);
-    const int nch = D / VEC;
-    bool ok = true;
-    for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kDecStages;
-        const int n = min(kDecKeys, k1 - (k0 + i * kDecKeys));
-        ok = mbar_wait(&full[st], (uint32_t)((i / kDecStages) & 1), nullptr);
-        if (__syncthreads_or(!ok)) {
-            if (tid == 0) {
-                atomicOr(err, ERR_TIMEOUT);
-                for (int j = i; j < ntiles && j < i + kDecStages; ++j)
-                    mbar_wait(&full[j % kDecStages], (uint32_t)((j / kDecStages) & 1), nullptr);
-            }
-            return;
+    // Producer: every lane steps through the warp's (unit, stage) sequence;
+    // lane 0 issues the copies.
+    int pu = gw, pt = 0, issued = 0;
+    DecUnit PU = dec_unit(pu, pos, S_max, G, L, nsplit, nhc);
+    auto produce = [&]() {
+        while (pu < units && pt >= PU.nt) {
+            pu += TW;
+            pt = 0;
+            if (pu < units) PU = dec_unit(pu, pos, S_max, G, L, nsplit, nhc);
         }
-        const unsigned char *base = ring + st * 2 * tile_bytes;
-        const T *Kt = reinterpret_cast<const T *>(base);
-        const T *Vt = reinterpret_cast<const T *>(base + tile_bytes);
-        // scores in the log2 domain, one thread per (head, key); the 16-byte
-        // chunks are visited in a lane-rotated order so that the 8 lanes of a
-        // quarter warp read 8 different bank groups of their 8 rows
-        for (int e = tid; e < nh * kDecKeys; e += kDecThreads) {
-            const int hh = e / kDecKeys, key = e - hh * kDecKeys;
-            float s = -INFINITY;
-            if (key < n) {
-                const T *kr = Kt + (size_t)key * D;
-                const float *qr = qs + hh * D;
-                float a0 = 0.f, a1 = 0.f;
-                for (int c0 = 0; c0 < nch; ++c0) {
-                    const int c = (c0 + lane) % nch;
-                    float kv[VEC];
-                    load16<T>(kr + c * VEC, kv);
+        if (pu >= units) return;
+        if (lane == 0) {
+            const int st = issued % NS;
+            const int ks = PU.k0 + pt * KT;
+            const uint32_t bytes = (uint32_t)min(KT, PU.k1 - ks) * rowb;
+            unsigned char *dst = ring + (size_t)st * stage_bytes;
+            const size_t row = ((size_t)PU.b * G + PU.g) * S_max + ks;
+            mbar_expect_tx(&bar[st], 2u * bytes);
+            bulk_load(dst, kc + row * rowe, bytes, &bar[st]);
+            bulk_load(dst + (size_t)KT * rowb, vc + row * rowe, bytes, &bar[st]);
+        }
+        ++pt;
+        ++issued;
+    };
+#pragma unroll 1
+    for (int i = 0; i < NS; ++i) produce();
+
+    const float sl2 = kLog2e * rsqrtf((float)D);
+    bool dv[CPL];
 #pragma unroll
-                    for (int x = 0; x < VEC; x += 2) {
-                        a0 = fmaf(qr[c * VEC + x], kv[x], a0);
-                        a1 = fmaf(qr[c * VEC + x + 1], kv[x + 1], a1);
+    for (int c = 0; c < CPL; ++c) dv[c] = FULL || (j + 8 * c) * VEC < D;
+    const bool b2 = (j & 4) != 0, b1 = (j & 2) != 0, b0 = (j & 1) != 0;
+    const bool c0 = (lane & 8) != 0, c1 = (lane & 16) != 0;
+    int x = 0;   // stages consumed
+
+#pragma unroll 1
+    for (int u = gw; u < units; u += TW) {
+        const DecUnit U = dec_unit(u, pos, S_max, G, L, nsplit, nhc);
+        const int h0 = U.g * group + U.hc * HP;
+        const int nh = min(HP, group - U.hc * HP);
+        // this lane's columns of the unit's (pre-scaled) query rows
+        float2 q2[HP][P2];
+#pragma unroll
+        for (int h = 0; h < HP; ++h)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+#pragma unroll
+                for (int e = 0; e < VEC / 2; ++e) {
+                    float2 v = make_float2(0.f, 0.f);
+                    if (h < nh && dv[c]) {
+                        const float2 r = *reinterpret_cast<const float2 *>(
+                            qhat + ((size_t)U.b * H + h0 + h) * D + (j + 8 * c) * VEC + 2 * e);
+                        v = make_float2(r.x * sl2, r.y * sl2);
+                    }
+                    q2[h][c * (VEC / 2) + e] = v;
+                }
+        float2 o2[HP][P2];
+#pragma unroll
+        for (int h = 0; h < HP; ++h)
+#pragma unroll
+            for (int e = 0; e < P2; ++e) o2[h][e] = make_float2(0.f, 0.f);
+        // running max and (lane-partial) sum of this lane's two heads 2*b0, 2*b0+1
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+
+#pragma unroll 1
+        for (int t = 0; t < U.nt; ++t, ++x) {
+            const int st = x % NS;
+            const bool ok = __all_sync(FULLMASK, mbar_wait_sleep(&bar[st], (uint32_t)((x / NS) & 1)));
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(err, ERR_TIMEOUT);
+                    for (int y = x; y < issued; ++y)   // let the copies in flight land
+                        mbar_wait_sleep(&bar[y % NS], (uint32_t)((y / NS) & 1));
+                }
+                __syncwarp();
+                return;
+            }
+            const T *Kt = reinterpret_cast<const T *>(ring + (size_t)st * stage_bytes);
+            const T *Vt = Kt + (size_t)KT * rowe;
+            const int n = min(KT, U.k1 - (U.k0 + t * KT));
+
+            // partial scores: key 4*pass + kq, heads 0..3, over this lane's chunks
+            float sc[4 * HP];
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int key = 4 * pass + kq;
+                float2 a[HP];
+#pragma unroll
+                for (int h = 0; h < HP; ++h) a[h] = make_float2(0.f, 0.f);
+                if (key < n) {
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) {
+                        if (!dv[c]) continue;
+                        float2 kv[VEC / 2];
+                        lds_pairs<T>(Kt + (size_t)key * rowe + (j + 8 * c) * VEC, kv);
+#pragma unroll
+                        for (int e = 0; e < VEC / 2; ++e)
+#pragma unroll
+                            for (int h = 0; h < HP; ++h) fma2(a[h], q2[h][c * (VEC / 2) + e], kv[e]);
                     }
                 }
-                s = (a0 + a1) * sl2;
-            }
-            sp[hh * kDecKeys + key] = s;
-        }
-        __syncthreads();
-        // online softmax, one warp per head
-        for (int hh = warp; hh < nh; hh += kDecThreads / 32) {
-            const float s0 = sp[hh * kDecKeys + lane], s1 = sp[hh * kDecKeys + 32 + lane];
-            const float mo = m_run[hh];
-            const float mn = fmaxf(mo, warp_max(fmaxf(s0, s1)));   // finite: every tile has a key
-            const float p0 = exp2f(s0 - mn), p1 = exp2f(s1 - mn);
-            const float lt = warp_sum(p0 + p1);
-            sp[hh * kDecKeys + lane] = p0;
-            sp[hh * kDecKeys + 32 + lane] = p1;
-            __syncwarp();
-            if (lane == 0) {
-                const float a = exp2f(mo - mn);   // 0 on the first tile
-                alpha[hh] = a;
-                m_run[hh] = mn;
-                l_run[hh] = l_run[hh] * a + lt;
-            }
-        }
-        __syncthreads();
-        // O = alpha O + P V, one thread per (head, column)
 #pragma unroll
-        for (int r = 0; r < kDecAcc; ++r) {
-            const int o = tid + kDecThreads * r;
-            if (o < nh * D) {
-                const int hh = o / D, d = o - hh * D;
-                const float *pr = sp + hh * kDecKeys;
-                float a = acc[r] * alpha[hh];
-                for (int key = 0; key < n; ++key) a = fmaf(pr[key], to_f32(Vt[(size_t)key * D + d]), a);
-                acc[r] = a;
+                for (int h = 0; h < HP; ++h) sc[pass * HP + h] = a[h].x + a[h].y;
+            }
+            // sum over the key's 8 lanes, halving the carried values per step:
+            // afterwards this lane holds key 4*(j>>1) + kq, heads 2*b0 + {0,1}
+            float r8[8], r4[4], r2[2];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float snd = b2 ? sc[i] : sc[i + 8], kp = b2 ? sc[i + 8] : sc[i];
+                r8[i] = kp + __shfl_xor_sync(FULLMASK, snd, 4);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float snd = b1 ? r8[i] : r8[i + 4], kp = b1 ? r8[i + 4] : r8[i];
+                r4[i] = kp + __shfl_xor_sync(FULLMASK, snd, 2);
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const float snd = b0 ? r4[i] : r4[i + 2], kp = b0 ? r4[i + 2] : r4[i];
+                r2[i] = kp + __shfl_xor_sync(FULLMASK, snd, 1);
+            }
+            // online softmax (log2 domain) over the stage's keys
+            const bool kvalid = 4 * (j >> 1) + kq < n;
+            float s0 = kvalid ? r2[0] : -INFINITY, s1 = kvalid ? r2[1] : -INFINITY;
+            float t0 = s0, t1 = s1;
+#pragma unroll
+            for (int o = 2; o <= 16; o <<= 1) {
+                t0 = fmaxf(t0, __shfl_xor_sync(FULLMASK, t0, o));
+                t1 = fmaxf(t1, __shfl_xor_sync(FULLMASK, t1, o));
+            }
+            const float mn0 = fmaxf(m_run[0], t0), mn1 = fmaxf(m_run[1], t1);
+            const float al0 = exp2f(m_run[0] - mn0), al1 = exp2f(m_run[1] - mn1);
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+            const float p0 = exp2f(s0 - mn0), p1 = exp2f(s1 - mn1);
+            l_run[0] = fmaf(l_run[0], al0, p0);
+            l_run[1] = fmaf(l_run[1], al1, p1);
+            const float ax0 = __shfl_xor_sync(FULLMASK, al0, 1);
+            const float ax1 = __shfl_xor_sync(FULLMASK, al1, 1);
+            const float alpha[HP] = {b0 ? ax0 : al0, b0 ? ax1 : al1, b0 ? al0 : ax0,
+                                     b0 ? al1 : ax1};
+            if (!(alpha[0] == 1.f && alpha[1] == 1.f && alpha[2] == 1.f && alpha[3] == 1.f)) {
+#pragma unroll
+                for (int h = 0; h < HP; ++h)
+#pragma unroll
+                    for (int e = 0; e < P2; ++e) {
+                        o2[h][e].x *= alpha[h];
+                        o2[h][e].y *= alpha[h];
+                    }
+            }
+            // O += P V: key 4*pass + kq, its probabilities from the lanes holding them
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+                const int key = 4 * pass + kq;
+                const int src = (kq << 3) | (2 * pass);
+                const float ph[HP] = {__shfl_sync(FULLMASK, p0, src), __shfl_sync(FULLMASK, p1, src),
+                                      __shfl_sync(FULLMASK, p0, src + 1),
+                                      __shfl_sync(FULLMASK, p1, src + 1)};
+                if (key < n) {
+#pragma unroll
+                    for (int c = 0; c < CPL; ++c) {
+                        if (!dv[c]) continue;
+                        float2 vv[VEC / 2];
+                        lds_pairs<T>(Vt + (size_t)key * rowe + (j + 8 * c) * VEC, vv);
+#pragma unroll
+                        for (int e = 0; e < VEC / 2; ++e)
+#pragma unroll
+                            for (int h = 0; h < HP; ++h)
+                                fma2(o2[h][c * (VEC / 2) + e], make_float2(ph[h], ph[h]), vv[e]);
+                    }
+                }
+            }
+            __syncwarp();   // the stage is free: refill it
+            if (lane == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            produce();
+        }
+
+        // the unit's partial: sum the four key slots (lane bits 3, 4), halving
+        // the carried heads per step; this lane ends with head 2*c0 + c1
+        float2 h2[2][P2], h1[P2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+            for (int e = 0; e < P2; ++e) {
+                const float2 snd = c0 ? o2[hh][e] : o2[hh + 2][e];
+                const float2 kp = c0 ? o2[hh + 2][e] : o2[hh][e];
+                h2[hh][e] = f2add(kp, shfl_xor2(snd, 8));
+            }
+#pragma unroll
+        for (int e = 0; e < P2; ++e) {
+            const float2 snd = c1 ? h2[0][e] : h2[1][e];
+            const float2 kp = c1 ? h2[1][e] : h2[0][e];
+            h1[e] = f2add(kp, shfl_xor2(snd, 16));
+        }
+        float lt0 = l_run[0], lt1 = l_run[1];
+#pragma unroll
+        for (int o = 2; o <= 16; o <<= 1) {
+            lt0 += __shfl_xor_sync(FULLMASK, lt0, o);
+            lt1 += __shfl_xor_sync(FULLMASK, lt1, o);
+        }
+        const size_t pbase = ((size_t)U.split * B + U.b) * H + h0;
+        const int hw = 2 * (int)c0 + (int)c1;
+        if (hw < nh) {
+            float *dst = part_o + (pbase + hw) * D;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                if (!dv[c]) continue;
+#pragma unroll
+                for (int e = 0; e < VEC / 2; e += 2)
+                    *reinterpret_cast<float4 *>(dst + (j + 8 * c) * VEC + 2 * e) =
+                        make_float4(h1[c * (VEC / 2) + e].x, h1[c * (VEC / 2) + e].y,
+                                    h1[c * (VEC / 2) + e + 1].x, h1[c * (VEC / 2) + e + 1].y);
             }
         }
-        __syncthreads();   // the stage is free
-        if (tid == 0 && i + kDecStages < ntiles) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            issue(i + kDecStages);
-        }
-    }
-    // partials of this split (m in the log2 domain; o unnormalised)
-    const size_t pbase = (size_t)split * B + b;
+        if (lane < 2) {
 #pragma unroll
-    for (int r = 0; r < kDecAcc; ++r) {
-        const int o = tid + kDecThreads * r;
-        if (o < nh * D) part_o[(pbase * H + h0) * D + o] = acc[r];
-    }
-    if (tid < nh) {
-        part_ml[((pbase * H) + h0 + tid) * 2] = m_run[tid];
-        part_ml[((pbase * H) + h0 + tid) * 2 + 1] = l_run[tid];
+            for (int k = 0; k < 2; ++k) {
+                const int h = 2 * lane + k;
+                if (h < nh) {
+                    part_ml[(pbase + h) * 2] = m_run[k];
+                    part_ml[(pbase + h) * 2 + 1] = k ? lt1 : lt0;
+                }
+            }
+        }
     }
 }
 
@@ -301,19 +478,38 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 DecodePlan decode_plan(const Problem &p) {
     DecodePlan d = {};
     const int group = p.H / p.G;
-    d.nhc = (group + kDecHeads - 1) / kDecHeads;
+    d.nhc = (group + kDecHP - 1) / kDecHP;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
         sms = 148;
-    const long units = (long)p.B * p.G * d.nhc;
-    const long tiles = (p.S + kDecKeys - 1) / kDecKeys;
-    long ns = (2L * sms + units - 1) / units;   // about two CTAs per SM
-    if (ns > tiles) ns = tiles;
-    if (ns < 1) ns = 1;
-    const long per = (tiles + ns - 1) / ns;
-    d.L = (int)(per * kDecKeys);
-    d.nsplit = (int)((p.S + d.L - 1) / d.L);
+    // Key splits: each SM runs its units side by side, one per warp, and is
+    // bound by the bytes it streams once about four warps stream at once, so
+    // the step takes about max(ceil(units / SMs), 4) * (stages per unit + a
+    // fixed cost of two stages); take the split count that minimises that
+    // (ties: more, shorter units).
+    const long base = (long)p.B * p.G * d.nhc;
+    const long tiles = (p.S + kDecKT - 1) / kDecKT;
+    long best_cost = -1, best_per = tiles, best_ns = 1;
+    for (long ns = 1; ns <= tiles && ns <= 1024; ++ns) {
+        const long per = (tiles + ns - 1) / ns;
+        const long nse = (tiles + per - 1) / per;
+        if (nse != ns) continue;
+        const long units = base * nse;
+        if (units > (1L << 30)) break;
+        const long cost = std::max<long>((units + sms - 1) / sms, 4) * (per + 2);
+        if (best_cost < 0 || cost <= best_cost) {
+            best_cost = cost;
+            best_per = per;
+            best_ns = nse;
+        }
+    }
+    d.L = (int)(best_per * kDecKT);
+    d.nsplit = (int)best_ns;
+    d.units = (int)(base * best_ns);
+    // units go to the CTAs first (warp w of CTA c runs units w * grid + c, ...),
+    // so every SM gets a share even when the units fill only part of the warps
+    d.grid = std::min(sms, d.units);
     const size_t align = 256;
     auto up = [&](size_t x) { return (x + align - 1) & ~(align - 1); };
     d.off_qhat = 0;
@@ -339,27 +535,34 @@ cudaError_t launch_decode_rows(const Problem &p, const int *pos, const void *q, 
     return cudaGetLastError();
 }
 
+template <typename T, int DP, bool FULL>
+cudaError_t run_decode_attn(const Problem &p, const DecodePlan &d, const int *pos,
+                            const float *qhat, const void *kc, const void *vc, float *part_o,
+                            float *part_ml, unsigned int *err, cudaStream_t st) {
+    constexpr int warps = dec_warps<T>();
+    const size_t smem = (size_t)warps * kDecNS * 2 * kDecKT * p.D * sizeof(T);
+    auto kern = k_decode_attn<T, DP, FULL>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<d.grid, warps * 32, smem, st>>>(pos, qhat, (const T *)kc, (const T *)vc, part_o, part_ml,
+                                           p.B, p.S, p.H, p.G, p.D, d.L, d.nsplit, d.nhc, d.units,
+                                           err);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int *pos,
                                const float *qhat, const void *kc, const void *vc, float *part_o,
                                float *part_ml, unsigned int *err, cudaStream_t st) {
-    const size_t es = p.dtype == 1 ? 2 : 4;
-    const size_t smem = (size_t)kDecStages * 2 * kDecKeys * p.D * es +
-                        sizeof(float) * kDecHeads * (p.D + kDecKeys);
-    dim3 grid((unsigned)((long)p.B * p.G * d.nhc), (unsigned)d.nsplit);
-    cudaError_t e;
-    if (p.dtype == 1) {
-        if ((e = set_smem(k_decode_attn<bf16>, smem)) != cudaSuccess) return e;
-        k_decode_attn<bf16><<<grid, kDecThreads, smem, st>>>(pos, qhat, (const bf16 *)kc,
-                                                             (const bf16 *)vc, part_o, part_ml, p.B,
-                                                             p.S, p.H, p.G, p.D, d.L, d.nhc, err);
-    } else {
-        if ((e = set_smem(k_decode_attn<float>, smem)) != cudaSuccess) return e;
-        k_decode_attn<float><<<grid, kDecThreads, smem, st>>>(pos, qhat, (const float *)kc,
-                                                              (const float *)vc, part_o, part_ml,
-                                                              p.B, p.S, p.H, p.G, p.D, d.L, d.nhc,
-                                                              err);
-    }
-    return cudaGetLastError();
+    if (p.dtype == 1)
+        return p.D == 128 ? run_decode_attn<bf16, 128, true>(p, d, pos, qhat, kc, vc, part_o,
+                                                             part_ml, err, st)
+                          : run_decode_attn<bf16, 64, true>(p, d, pos, qhat, kc, vc, part_o,
+                                                            part_ml, err, st);
+    if (p.D > 64)
+        return run_decode_attn<float, 128, false>(p, d, pos, qhat, kc, vc, part_o, part_ml, err, st);
+    if (p.D > 32)
+        return run_decode_attn<float, 64, false>(p, d, pos, qhat, kc, vc, part_o, part_ml, err, st);
+    return run_decode_attn<float, 32, false>(p, d, pos, qhat, kc, vc, part_o, part_ml, err, st);
 }
 
 cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const float *part_o,

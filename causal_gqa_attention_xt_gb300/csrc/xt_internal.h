@@ -71,6 +71,7 @@ cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const fl
 // and the per-split partials.
 struct DecodePlan {
     int nsplit, L, nhc;   // key splits, keys per split, query-head chunks per kv head
+    int units, grid;      // work units (b, kv head, head chunk, split); CTAs of the attention kernel
     size_t off_qhat, off_o, off_ml, total;
 };
 DecodePlan decode_plan(const Problem &p);
