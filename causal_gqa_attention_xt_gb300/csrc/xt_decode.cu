@@ -13,7 +13,9 @@
 // forward's k_hat), so a kv head's cached rows are one contiguous run.
 //
 // Three kernels (the work is a matrix-vector product per kv head, bound by
-// reading the cache from HBM, so it runs on the CUDA cores):
+// reading the cache from HBM, so it runs on the CUDA cores), the second and
+// third launched as programmatic dependents of the one before, so each is
+// launched while its predecessor still runs and waits for it on the device:
 //  * k_decode_rows: one warp per new row: q heads normed + rotated into an
 //    fp32 scratch (rounded through the storage type, as the training forward
 //    rounds q_hat), k heads normed + rotated into the k cache at row pos[b], v
@@ -66,6 +68,8 @@ k_decode_rows(const int *__restrict__ pos, const T *__restrict__ q, const T *__r
               const T *__restrict__ v, const float *__restrict__ gq, const float *__restrict__ gk,
               float *__restrict__ qhat, T *__restrict__ kc, T *__restrict__ vc, int S_max, int H,
               int G, int D, float eps, const __grid_constant__ RopeConsts rc, unsigned int *err) {
+    // the attention kernel may launch now; it waits for this grid before reading
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int b = blockIdx.y;
     const int row = blockIdx.x * 8 + (threadIdx.x >> 5);   // H q rows, G k rows, G v rows
     const int lane = threadIdx.x & 31;
@@ -197,6 +201,10 @@ k_decode_attn(const int *__restrict__ pos, const float *__restrict__ qhat,
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gw = warp * (int)gridDim.x + (int)blockIdx.x;   // units spread over CTAs first
     const int TW = (int)gridDim.x * WARPS;
+    // the merge kernel may launch now (it waits for this grid); this grid waits
+    // for the new-rows grid before it reads q-hat or the caches
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (gw >= units) return;
     const int kq = lane >> 3, j = lane & 7;
     const int group = H / G;
@@ -444,6 +452,7 @@ template <typename T>
 __global__ void __launch_bounds__(128)
 k_decode_combine(const float *__restrict__ part_o, const float *__restrict__ part_ml,
                  T *__restrict__ out, float *__restrict__ lse, int B, int H, int D, int nsplit) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the attention grid's partials
     const int bh = blockIdx.x;   // b * H + h
     float m = -INFINITY;
     for (int s = 0; s < nsplit; ++s)
@@ -471,6 +480,25 @@ k_decode_combine(const float *__restrict__ part_o, const float *__restrict__ par
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// Launches `kernel` as a programmatic dependent of the previous launch on the
+// stream: it may start before that grid ends and waits for it (griddepcontrol)
+// before touching its results.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace
@@ -544,10 +572,9 @@ cudaError_t run_decode_attn(const Problem &p, const DecodePlan &d, const int *po
     auto kern = k_decode_attn<T, DP, FULL>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<d.grid, warps * 32, smem, st>>>(pos, qhat, (const T *)kc, (const T *)vc, part_o, part_ml,
-                                           p.B, p.S, p.H, p.G, p.D, d.L, d.nsplit, d.nhc, d.units,
-                                           err);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3(d.grid), dim3(warps * 32), smem, st, pos, qhat,
+                            (const T *)kc, (const T *)vc, part_o, part_ml, p.B, p.S, p.H, p.G, p.D,
+                            d.L, d.nsplit, d.nhc, d.units, err);
 }
 
 cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int *pos,
@@ -567,14 +594,12 @@ cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int 
 
 cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const float *part_o,
                                   const float *part_ml, void *out, float *lse, cudaStream_t st) {
-    const unsigned grid = (unsigned)((long)p.B * p.H);
+    const dim3 grid((unsigned)((long)p.B * p.H));
     if (p.dtype == 1)
-        k_decode_combine<bf16><<<grid, 128, 0, st>>>(part_o, part_ml, (bf16 *)out, lse, p.B, p.H,
-                                                     p.D, d.nsplit);
-    else
-        k_decode_combine<float><<<grid, 128, 0, st>>>(part_o, part_ml, (float *)out, lse, p.B,
-                                                      p.H, p.D, d.nsplit);
-    return cudaGetLastError();
+        return launch_dependent(k_decode_combine<bf16>, grid, dim3(128), 0, st, part_o, part_ml,
+                                (bf16 *)out, lse, p.B, p.H, p.D, d.nsplit);
+    return launch_dependent(k_decode_combine<float>, grid, dim3(128), 0, st, part_o, part_ml,
+                            (float *)out, lse, p.B, p.H, p.D, d.nsplit);
 }
 
 }  // namespace xt
