@@ -21,6 +21,9 @@ follows a passage of the pages:
   qh/group) and Decision 2 (repeat_kv copy; backward = in-order group sum).
 * softmax backward -- the pages give none; the oracle uses the exact Jacobian
   dS = P o (dP - rowsum(dP o P)).
+* packed batches -- Mint report 8.2 (a chat batch flattened to [total] rows,
+  RoPE positions numbered inside each sample, block-causal mask: other
+  samples' rows hidden, causal inside a sample).
 
 Parity status: every function here is pinned by tests in
 ``tests/test_oracle_pins.py`` (library routines, closed forms, invariants,
@@ -79,6 +82,12 @@ def _load():
             lib.orc_attn_bwd.argtypes = [I, I, I, I, I, Dd, Dd, dp, dp, dp, dp, dp, dp,
                                          dp, dp, dp, dp, dp, I]
             lib.orc_attn_bwd.restype = I
+            lib.orc_attn_fwd_packed.argtypes = [I, lp, I, I, I, Dd, Dd, dp, dp, dp, dp, dp,
+                                                dp, dp, dp, dp, dp, dp, I]
+            lib.orc_attn_fwd_packed.restype = I
+            lib.orc_attn_bwd_packed.argtypes = [I, lp, I, I, I, Dd, Dd, dp, dp, dp, dp, dp, dp,
+                                                dp, dp, dp, dp, dp, I]
+            lib.orc_attn_bwd_packed.restype = I
             lib.orc_attn_fwd_rows.argtypes = [I, I, I, I, I, Dd, Dd, dp, dp, dp, dp, dp,
                                               L, lp, dp, dp, I]
             lib.orc_attn_fwd_rows.restype = I
@@ -231,6 +240,58 @@ def attn_bwd(q, k, v, gamma_q, gamma_k, dout, eps, theta, nthreads=None):
                               int(nthreads or default_threads()))
     if rc:
         raise ValueError("oracle: invalid shape")
+    return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgq, dgamma_k=dgk)
+
+
+def _cu(cu_seqlens) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64).reshape(-1))
+
+
+def attn_fwd_packed(q, k, v, gamma_q, gamma_k, cu_seqlens, eps, theta, nthreads=None):
+    """Forward over a packed batch: sample s on rows cu[s]..cu[s+1]-1.
+
+    q [T,H,D], k/v [T,G,D]. Returns a dict with out [T,H,D], lse [H,T],
+    qhat [H,T,D], khat [G,T,D], rstd_q [T,H], rstd_k [T,G].
+    """
+    q, k, v, gq, gk = map(_f64, (q, k, v, gamma_q, gamma_k))
+    cu = _cu(cu_seqlens)
+    T, H, D = q.shape
+    G = k.shape[1]
+    out = np.empty((T, H, D))
+    lse = np.empty((H, T))
+    qhat = np.empty((H, T, D))
+    khat = np.empty((G, T, D))
+    rq = np.empty((T, H))
+    rk = np.empty((T, G))
+    if cu[-1] != T:
+        raise ValueError("oracle: cu_seqlens[-1] must equal the row count")
+    rc = _load().orc_attn_fwd_packed(len(cu) - 1, _lp(cu), H, G, D, float(eps), float(theta),
+                                     _p(q), _p(k), _p(v), _p(gq), _p(gk), _p(out), _p(lse),
+                                     _p(qhat), _p(khat), _p(rq), _p(rk),
+                                     int(nthreads or default_threads()))
+    if rc:
+        raise ValueError("oracle: invalid shape or offsets")
+    return dict(out=out, lse=lse, qhat=qhat, khat=khat, rstd_q=rq, rstd_k=rk)
+
+
+def attn_bwd_packed(q, k, v, gamma_q, gamma_k, cu_seqlens, dout, eps, theta, nthreads=None):
+    """Backward over a packed batch for upstream gradient dout [T,H,D]."""
+    q, k, v, gq, gk, do = map(_f64, (q, k, v, gamma_q, gamma_k, dout))
+    cu = _cu(cu_seqlens)
+    T, H, D = q.shape
+    G = k.shape[1]
+    if cu[-1] != T:
+        raise ValueError("oracle: cu_seqlens[-1] must equal the row count")
+    dq = np.empty_like(q)
+    dk = np.empty_like(k)
+    dv = np.empty_like(v)
+    dgq = np.empty(D)
+    dgk = np.empty(D)
+    rc = _load().orc_attn_bwd_packed(len(cu) - 1, _lp(cu), H, G, D, float(eps), float(theta),
+                                     _p(q), _p(k), _p(v), _p(gq), _p(gk), _p(do), _p(dq), _p(dk),
+                                     _p(dv), _p(dgq), _p(dgk), int(nthreads or default_threads()))
+    if rc:
+        raise ValueError("oracle: invalid shape or offsets")
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgq, dgamma_k=dgk)
 
 

@@ -24,6 +24,10 @@
  *   [T15]  xtrain "Phase T15: Grouped-Query Attention" (docs/14-gqa.md):
  *          "What is GQA" (q head qh reads kv head qh/group) and Decision 2
  *          (repeat_kv forward copy; backward = in-order group-row sum).
+ *   [MINT 8.2] Mint project report, 8.2 (forward pass of a flattened chat
+ *          batch): samples are packed into [total] rows, RoPE numbers the
+ *          positions inside each sample, and a block-causal mask hides other
+ *          samples' rows entirely and, inside a sample, the later rows.
  *
  * Arithmetic is double throughout. Matrix products are written as the plain
  * triple loop; every output element is accumulated over its summation index
@@ -34,6 +38,7 @@
  *   q [B,S,H,D]; k, v [B,S,G,D]; out, dout, dq [B,S,H,D]; dk, dv [B,S,G,D];
  *   lse [B,H,S]; qhat [B,H,S,D]; khat [B,G,S,D]; rstd_q [B,S,H];
  *   rstd_k [B,S,G]; gamma_q, gamma_k, dgamma_q, dgamma_k [D].
+ * Packed batches use the same layouts with B = 1 and S = total rows.
  */
 #include <math.h>
 #include <pthread.h>
@@ -145,8 +150,11 @@ void orc_repeat_kv_bwd(int B, int H, int G, long SD, const double *dout, double 
 /*   o      = p v ;  lse_t = max_t + ln sum_j exp(scores_tj - max_t)           */
 /* p is the caller's [S, S] buffer and holds the probabilities on return.     */
 /* ------------------------------------------------------------------------ */
-void orc_sdpa_head_fwd(int S, int D, const double *q, const double *k, const double *v,
-                       double *p, double *o, double *lse)
+/* blk (may be NULL): sample id of every row, for the block-causal mask of
+ * [MINT 8.2]: key j is visible to row t iff j <= t and blk[j] == blk[t];
+ * every other key gets the additive -1e9. NULL is the plain causal mask.   */
+void orc_sdpa_head_fwd_blk(int S, int D, const int *blk, const double *q, const double *k,
+                           const double *v, double *p, double *o, double *lse)
 {
     double scale = 1.0 / sqrt((double)D);
     double *kt = (double *)malloc(sizeof(double) * (size_t)D * S);
@@ -161,7 +169,10 @@ void orc_sdpa_head_fwd(int S, int D, const double *q, const double *k, const dou
             const double *ktd = kt + (long)d * S;
             for (int j = 0; j < S; ++j) pr[j] += qd * ktd[j];
         }
-        for (int j = 0; j < S; ++j) pr[j] = pr[j] * scale + (j <= t ? 0.0 : ORC_MASK_VALUE);
+        for (int j = 0; j < S; ++j) {
+            int visible = j <= t && (blk == NULL || blk[j] == blk[t]);
+            pr[j] = pr[j] * scale + (visible ? 0.0 : ORC_MASK_VALUE);
+        }
         double m = pr[0];
         for (int j = 1; j < S; ++j) if (pr[j] > m) m = pr[j];
         double sum = 0.0;
@@ -177,6 +188,12 @@ void orc_sdpa_head_fwd(int S, int D, const double *q, const double *k, const dou
         }
     }
     free(kt);
+}
+
+void orc_sdpa_head_fwd(int S, int D, const double *q, const double *k, const double *v,
+                       double *p, double *o, double *lse)
+{
+    orc_sdpa_head_fwd_blk(S, D, NULL, q, k, v, p, o, lse);
 }
 
 /* Backward of one head, by hand from the forward above (the softmax Jacobian):
@@ -290,16 +307,20 @@ static void orc_parallel(long count, int nthreads, void (*fn)(void *, long), voi
 /*   per-head 2D causal SDPA -> merge back to [B, S, H, D].                   */
 /* ------------------------------------------------------------------------ */
 
-/* Norm + RoPE of x [B,S,NH,D] into xhat [B,NH,S,D]; rstd [B,S,NH]. */
+/* Norm + RoPE of x [B,S,NH,D] into xhat [B,NH,S,D]; rstd [B,S,NH]. tokpos
+ * (may be NULL) gives the RoPE position of every token row b*S+s (packed
+ * batches, [MINT 8.2]); NULL means position s. */
 static void orc_qk_prologue(int B, int S, int NH, int D, double eps, double theta,
-                            const double *x, const double *gamma, double *xhat, double *rstd)
+                            const long *tokpos, const double *x, const double *gamma,
+                            double *xhat, double *rstd)
 {
     long rows = (long)B * S * NH;
     double *y = (double *)malloc(sizeof(double) * rows * D);
     double *yr = (double *)malloc(sizeof(double) * rows * D);
     long *pos = (long *)malloc(sizeof(long) * rows);
     orc_rmsnorm_rows(rows, D, x, gamma, eps, y, rstd);
-    for (long r = 0; r < rows; ++r) pos[r] = (r / NH) % S;   /* row (b, s, h) sits at s */
+    for (long r = 0; r < rows; ++r)   /* row (b, s, h) sits at s (or at its packed position) */
+        pos[r] = tokpos ? tokpos[r / NH] : (r / NH) % S;
     orc_rope_rows(rows, D, theta, pos, y, yr, 0);
     for (int b = 0; b < B; ++b)
         for (int s = 0; s < S; ++s)
@@ -330,6 +351,7 @@ static void orc_to_token_major(int B, int S, int NH, int D, const double *x, dou
 
 typedef struct {
     int S, D;
+    const int *blk;                        /* [S] sample ids (packed) or NULL */
     const double *qh, *krep, *vrep, *dor;  /* [B*H, S, D] */
     double *o, *lse;                       /* [B*H, S, D], [B*H, S] */
     double *dq, *dk, *dv;                  /* [B*H, S, D] (backward only) */
@@ -340,8 +362,8 @@ static void orc_head_fwd_unit(void *vctx, long u)
     orc_heads_ctx *c = (orc_heads_ctx *)vctx;
     long SD = (long)c->S * c->D;
     double *p = (double *)malloc(sizeof(double) * (size_t)c->S * c->S);
-    orc_sdpa_head_fwd(c->S, c->D, c->qh + u * SD, c->krep + u * SD, c->vrep + u * SD,
-                      p, c->o + u * SD, c->lse + u * c->S);
+    orc_sdpa_head_fwd_blk(c->S, c->D, c->blk, c->qh + u * SD, c->krep + u * SD,
+                          c->vrep + u * SD, p, c->o + u * SD, c->lse + u * c->S);
     free(p);
 }
 
@@ -352,7 +374,8 @@ static void orc_head_bwd_unit(void *vctx, long u)
     double *p = (double *)malloc(sizeof(double) * (size_t)c->S * c->S);
     double *o = (double *)malloc(sizeof(double) * SD);
     double *lse = (double *)malloc(sizeof(double) * c->S);
-    orc_sdpa_head_fwd(c->S, c->D, c->qh + u * SD, c->krep + u * SD, c->vrep + u * SD, p, o, lse);
+    orc_sdpa_head_fwd_blk(c->S, c->D, c->blk, c->qh + u * SD, c->krep + u * SD,
+                          c->vrep + u * SD, p, o, lse);
     orc_sdpa_head_bwd(c->S, c->D, c->qh + u * SD, c->krep + u * SD, c->vrep + u * SD, p,
                       c->dor + u * SD, c->dq + u * SD, c->dk + u * SD, c->dv + u * SD);
     free(p); free(o); free(lse);
@@ -365,12 +388,15 @@ static int orc_check_shape(int B, int S, int H, int G, int D)
     return 0;
 }
 
-/* Forward. out [B,S,H,D], lse [B,H,S]; qhat/khat/rstd_q/rstd_k may be NULL. */
-int orc_attn_fwd(int B, int S, int H, int G, int D, double eps, double theta,
-                 const double *q, const double *k, const double *v,
-                 const double *gamma_q, const double *gamma_k,
-                 double *out, double *lse, double *qhat_out, double *khat_out,
-                 double *rstd_q_out, double *rstd_k_out, int nthreads)
+/* Forward. out [B,S,H,D], lse [B,H,S]; qhat/khat/rstd_q/rstd_k may be NULL.
+ * blk / tokpos: sample ids and positions of the rows of a packed batch (B = 1),
+ * or NULL. */
+static int orc_attn_fwd_impl(int B, int S, int H, int G, int D, double eps, double theta,
+                             const int *blk, const long *tokpos,
+                             const double *q, const double *k, const double *v,
+                             const double *gamma_q, const double *gamma_k,
+                             double *out, double *lse, double *qhat_out, double *khat_out,
+                             double *rstd_q_out, double *rstd_k_out, int nthreads)
 {
     if (orc_check_shape(B, S, H, G, D)) return 1;
     long SD = (long)S * D;
@@ -383,13 +409,13 @@ int orc_attn_fwd(int B, int S, int H, int G, int D, double eps, double theta,
     double *rq = (double *)malloc(sizeof(double) * B * S * H);
     double *rk = (double *)malloc(sizeof(double) * B * S * G);
 
-    orc_qk_prologue(B, S, H, D, eps, theta, q, gamma_q, qh, rq);
-    orc_qk_prologue(B, S, G, D, eps, theta, k, gamma_k, kh, rk);
+    orc_qk_prologue(B, S, H, D, eps, theta, tokpos, q, gamma_q, qh, rq);
+    orc_qk_prologue(B, S, G, D, eps, theta, tokpos, k, gamma_k, kh, rk);
     orc_to_head_major(B, S, G, D, v, vh);
     orc_repeat_kv(B, H, G, SD, kh, krep);
     orc_repeat_kv(B, H, G, SD, vh, vrep);
 
-    orc_heads_ctx c = {S, D, qh, krep, vrep, NULL, oh, lse, NULL, NULL, NULL};
+    orc_heads_ctx c = {S, D, blk, qh, krep, vrep, NULL, oh, lse, NULL, NULL, NULL};
     orc_parallel((long)B * H, nthreads, orc_head_fwd_unit, &c);
     orc_to_token_major(B, S, H, D, oh, out);
 
@@ -401,15 +427,26 @@ int orc_attn_fwd(int B, int S, int H, int G, int D, double eps, double theta,
     return 0;
 }
 
+int orc_attn_fwd(int B, int S, int H, int G, int D, double eps, double theta,
+                 const double *q, const double *k, const double *v,
+                 const double *gamma_q, const double *gamma_k,
+                 double *out, double *lse, double *qhat_out, double *khat_out,
+                 double *rstd_q_out, double *rstd_k_out, int nthreads)
+{
+    return orc_attn_fwd_impl(B, S, H, G, D, eps, theta, NULL, NULL, q, k, v, gamma_q, gamma_k,
+                             out, lse, qhat_out, khat_out, rstd_q_out, rstd_k_out, nthreads);
+}
+
 /* Backward by the chain rule, in reverse op order: per-head SDPA backward ->
  * repeat_kv backward (group-row sum) -> RoPE backward (negative angle) ->
  * RMSNorm backward. dgamma_q / dgamma_k are overwritten with the sum over all
  * (b, s, head) rows in that row order. */
-int orc_attn_bwd(int B, int S, int H, int G, int D, double eps, double theta,
-                 const double *q, const double *k, const double *v,
-                 const double *gamma_q, const double *gamma_k, const double *dout,
-                 double *dq, double *dk, double *dv, double *dgamma_q, double *dgamma_k,
-                 int nthreads)
+static int orc_attn_bwd_impl(int B, int S, int H, int G, int D, double eps, double theta,
+                             const int *blk, const long *tokpos,
+                             const double *q, const double *k, const double *v,
+                             const double *gamma_q, const double *gamma_k, const double *dout,
+                             double *dq, double *dk, double *dv, double *dgamma_q,
+                             double *dgamma_k, int nthreads)
 {
     if (orc_check_shape(B, S, H, G, D)) return 1;
     long SD = (long)S * D;
@@ -428,14 +465,14 @@ int orc_attn_bwd(int B, int S, int H, int G, int D, double eps, double theta,
     double *rq = (double *)malloc(sizeof(double) * B * S * H);
     double *rk = (double *)malloc(sizeof(double) * B * S * G);
 
-    orc_qk_prologue(B, S, H, D, eps, theta, q, gamma_q, qh, rq);
-    orc_qk_prologue(B, S, G, D, eps, theta, k, gamma_k, kh, rk);
+    orc_qk_prologue(B, S, H, D, eps, theta, tokpos, q, gamma_q, qh, rq);
+    orc_qk_prologue(B, S, G, D, eps, theta, tokpos, k, gamma_k, kh, rk);
     orc_to_head_major(B, S, G, D, v, vh);
     orc_repeat_kv(B, H, G, SD, kh, krep);
     orc_repeat_kv(B, H, G, SD, vh, vrep);
     orc_to_head_major(B, S, H, D, dout, doh);
 
-    orc_heads_ctx c = {S, D, qh, krep, vrep, doh, NULL, lse, dqh, dkrep, dvrep};
+    orc_heads_ctx c = {S, D, blk, qh, krep, vrep, doh, NULL, lse, dqh, dkrep, dvrep};
     orc_parallel((long)B * H, nthreads, orc_head_bwd_unit, &c);
 
     orc_repeat_kv_bwd(B, H, G, SD, dkrep, dkh);
@@ -452,8 +489,8 @@ int orc_attn_bwd(int B, int S, int H, int G, int D, double eps, double theta,
     long *posk = (long *)malloc(sizeof(long) * rk_rows);
     orc_to_token_major(B, S, H, D, dqh, tmpq);
     orc_to_token_major(B, S, G, D, dkh, tmpk);
-    for (long r = 0; r < rq_rows; ++r) posq[r] = (r / H) % S;
-    for (long r = 0; r < rk_rows; ++r) posk[r] = (r / G) % S;
+    for (long r = 0; r < rq_rows; ++r) posq[r] = tokpos ? tokpos[r / H] : (r / H) % S;
+    for (long r = 0; r < rk_rows; ++r) posk[r] = tokpos ? tokpos[r / G] : (r / G) % S;
     orc_rope_rows(rq_rows, D, theta, posq, tmpq, dyq, 1);
     orc_rope_rows(rk_rows, D, theta, posk, tmpk, dyk, 1);
     memset(dgamma_q, 0, sizeof(double) * D);
@@ -465,6 +502,71 @@ int orc_attn_bwd(int B, int S, int H, int G, int D, double eps, double theta,
     free(dkrep); free(dvrep); free(dkh); free(dvh); free(lse); free(rq); free(rk);
     free(dyq); free(dyk); free(tmpq); free(tmpk); free(posq); free(posk);
     return 0;
+}
+
+int orc_attn_bwd(int B, int S, int H, int G, int D, double eps, double theta,
+                 const double *q, const double *k, const double *v,
+                 const double *gamma_q, const double *gamma_k, const double *dout,
+                 double *dq, double *dk, double *dv, double *dgamma_q, double *dgamma_k,
+                 int nthreads)
+{
+    return orc_attn_bwd_impl(B, S, H, G, D, eps, theta, NULL, NULL, q, k, v, gamma_q, gamma_k,
+                             dout, dq, dk, dv, dgamma_q, dgamma_k, nthreads);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Packed batches ([MINT 8.2]): nseq samples, sample s on rows cu[s] ..      */
+/* cu[s+1]-1 of [T = cu[nseq]] rows; positions restart at 0 in every sample; */
+/* the block-causal mask keeps samples apart. Layouts as above with B = 1,   */
+/* S = T: q [T,H,D], k/v [T,G,D], out [T,H,D], lse [H,T], qhat [H,T,D],      */
+/* khat [G,T,D], rstd_q [T,H], rstd_k [T,G]. Empty samples are allowed.      */
+/* ------------------------------------------------------------------------ */
+static int orc_packed_rows(int nseq, const long *cu, int **blk, long **tokpos)
+{
+    if (nseq <= 0 || cu[0] != 0) return 1;
+    for (int s = 0; s < nseq; ++s)
+        if (cu[s + 1] < cu[s]) return 1;
+    long T = cu[nseq];
+    if (T <= 0 || T > 2147483647L) return 1;
+    *blk = (int *)malloc(sizeof(int) * T);
+    *tokpos = (long *)malloc(sizeof(long) * T);
+    for (int s = 0; s < nseq; ++s)
+        for (long t = cu[s]; t < cu[s + 1]; ++t) {
+            (*blk)[t] = s;
+            (*tokpos)[t] = t - cu[s];
+        }
+    return 0;
+}
+
+int orc_attn_fwd_packed(int nseq, const long *cu, int H, int G, int D, double eps, double theta,
+                        const double *q, const double *k, const double *v,
+                        const double *gamma_q, const double *gamma_k,
+                        double *out, double *lse, double *qhat_out, double *khat_out,
+                        double *rstd_q_out, double *rstd_k_out, int nthreads)
+{
+    int *blk = NULL;
+    long *tokpos = NULL;
+    if (orc_packed_rows(nseq, cu, &blk, &tokpos)) return 1;
+    int rc = orc_attn_fwd_impl(1, (int)cu[nseq], H, G, D, eps, theta, blk, tokpos, q, k, v,
+                               gamma_q, gamma_k, out, lse, qhat_out, khat_out, rstd_q_out,
+                               rstd_k_out, nthreads);
+    free(blk); free(tokpos);
+    return rc;
+}
+
+int orc_attn_bwd_packed(int nseq, const long *cu, int H, int G, int D, double eps, double theta,
+                        const double *q, const double *k, const double *v,
+                        const double *gamma_q, const double *gamma_k, const double *dout,
+                        double *dq, double *dk, double *dv, double *dgamma_q, double *dgamma_k,
+                        int nthreads)
+{
+    int *blk = NULL;
+    long *tokpos = NULL;
+    if (orc_packed_rows(nseq, cu, &blk, &tokpos)) return 1;
+    int rc = orc_attn_bwd_impl(1, (int)cu[nseq], H, G, D, eps, theta, blk, tokpos, q, k, v,
+                               gamma_q, gamma_k, dout, dq, dk, dv, dgamma_q, dgamma_k, nthreads);
+    free(blk); free(tokpos);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */
