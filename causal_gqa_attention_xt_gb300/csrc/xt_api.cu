@@ -101,6 +101,7 @@ int validate_shape(int B, int S, int H, int G, int D, int dtype) {
     if (dtype == XT_BF16 && D != 64 && D != 128) return XT_EUNSUPPORTED;
     if (dtype == XT_F32 && (D % 8 != 0 || D > 128)) return XT_EUNSUPPORTED;
     if (H + G > kMaxHeads) return XT_EUNSUPPORTED;
+    if (dtype == XT_F32 && (long)B * H > 65535) return XT_EUNSUPPORTED;   // grid.y of the fp32 path
     return XT_OK;
 }
 
@@ -153,49 +154,46 @@ Problem make_problem(int B, int S, int H, int G, int D, double eps, double theta
     Problem p;
     p.B = B; p.S = S; p.H = H; p.G = G; p.D = D;
     p.eps = (float)eps; p.theta = theta; p.dtype = dtype;
+    p.cu = nullptr; p.units = B; p.max_len = S;
     return p;
 }
 
-}  // namespace
-}  // namespace xt
-
-using namespace xt;
-
-extern "C" {
-
-size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
-                               int dtype, int backward) {
-    if (validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
-    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype);
-    return backward ? bwd_layout(p).total : fwd_workspace(p);
+// A packed batch: one plane of `total` rows holding nseq samples.
+Problem make_packed_problem(int total, int nseq, int max_seqlen, const int *cu, int H, int G,
+                            int D, double eps, double theta, int dtype) {
+    Problem p = make_problem(1, total, H, G, D, eps, theta, dtype);
+    p.cu = cu; p.units = nseq; p.max_len = max_seqlen;
+    return p;
 }
 
-int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
-                double theta, const void *q, const void *k, const void *v,
-                const float *gamma_q, const float *gamma_k, int dtype, void *out, float *lse,
-                void *q_hat, void *k_hat, float *rstd_q, float *rstd_k, void *workspace,
-                size_t workspace_bytes, void *stream) {
-    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
-    if (st != XT_OK) return st;
-    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+int validate_packed(int total, int nseq, int max_seqlen, const int *cu, int H, int dtype) {
+    if (nseq <= 0 || max_seqlen <= 0 || max_seqlen > total) return XT_EINVAL;
+    if (cu == nullptr || ((uintptr_t)cu & 3u) != 0) return XT_EINVAL;
+    if (dtype == XT_F32 && (long)nseq * H > 65535) return XT_EUNSUPPORTED;
+    return XT_OK;
+}
+
+// The forward pipeline: RoPE table, prologue, attention.
+int run_fwd(const Problem &p, const void *q, const void *k, const void *v, const float *gamma_q,
+            const float *gamma_k, void *out, float *lse, void *q_hat, void *k_hat, float *rstd_q,
+            float *rstd_k, void *workspace, size_t workspace_bytes, void *stream) {
     const void *ptrs[] = {q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k};
     for (const void *ptr : ptrs)
         if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
-    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
     if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < fwd_workspace(p))
         return XT_EWORKSPACE;
     void *tab = workspace;
     cudaStream_t s = (cudaStream_t)stream;
     unsigned int *err = error_word_ptr();
     if (!err) return cuda_fail(cudaGetLastError());
-    st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, s); });
+    int st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, err, s); });
     if (st != XT_OK) return st;
     st = timed_launch(KID_PROLOGUE, s, [&] {
         return launch_prologue(p, q, k, gamma_q, gamma_k, tab, q_hat, k_hat, rstd_q, rstd_k, err,
                                s);
     });
     if (st != XT_OK) return st;
-    if (dtype == XT_BF16) {
+    if (p.dtype == XT_BF16) {
         return timed_launch(KID_FWD_TC, s, [&] {
             return launch_fwd_tc(p, q_hat, k_hat, v, out, lse, err, s);
         });
@@ -205,21 +203,16 @@ int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     });
 }
 
-int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
-                double theta, const void *q, const void *k, const void *v,
-                const float *gamma_q, const float *gamma_k, int dtype, const void *out,
-                const float *lse, const void *q_hat, const void *k_hat, const float *rstd_q,
-                const float *rstd_k, const void *dout, void *dq, void *dk, void *dv,
-                float *dgamma_q, float *dgamma_k, void *workspace, size_t workspace_bytes,
-                void *stream) {
-    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
-    if (st != XT_OK) return st;
-    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+// The backward pipeline: RoPE table, Dlt, dK/dV, dQ, epilogue, dgamma reduce.
+int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const float *gamma_q,
+            const float *gamma_k, const void *out, const float *lse, const void *q_hat,
+            const void *k_hat, const float *rstd_q, const float *rstd_k, const void *dout,
+            void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k, void *workspace,
+            size_t workspace_bytes, void *stream) {
     const void *ptrs[] = {q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k,
                           dout, dq, dk, dv, dgamma_q, dgamma_k};
     for (const void *ptr : ptrs)
         if (ptr == nullptr || !aligned16(ptr)) return XT_EINVAL;
-    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
     const BwdWorkspace w = bwd_layout(p);
     if (workspace == nullptr || !aligned16(workspace) || workspace_bytes < w.total)
         return XT_EWORKSPACE;
@@ -234,13 +227,13 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     unsigned int *err = error_word_ptr();
     if (!err) return cuda_fail(cudaGetLastError());
 
-    st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, s); });
+    int st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, err, s); });
     if (st != XT_OK) return st;
     st = timed_launch(KID_BWD_PRE, s, [&] {
         return launch_bwd_pre(p, out, dout, dlt, err, s);
     });
     if (st != XT_OK) return st;
-    if (dtype == XT_BF16) {
+    if (p.dtype == XT_BF16) {
         st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
             return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, err, s);
         });
@@ -268,6 +261,92 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
     return timed_launch(KID_DGAMMA_REDUCE, s, [&] {
         return launch_dgamma_reduce(p, part_q, part_k, nparts, nparts, dgamma_q, dgamma_k, s);
     });
+}
+
+}  // namespace
+}  // namespace xt
+
+using namespace xt;
+
+extern "C" {
+
+size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
+                               int dtype, int backward) {
+    if (validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype);
+    return backward ? bwd_layout(p).total : fwd_workspace(p);
+}
+
+int xt_attn_fwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
+                double theta, const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype, void *out, float *lse,
+                void *q_hat, void *k_hat, float *rstd_q, float *rstd_k, void *workspace,
+                size_t workspace_bytes, void *stream) {
+    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    return run_fwd(p, q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k,
+                   workspace, workspace_bytes, stream);
+}
+
+int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double eps,
+                double theta, const void *q, const void *k, const void *v,
+                const float *gamma_q, const float *gamma_k, int dtype, const void *out,
+                const float *lse, const void *q_hat, const void *k_hat, const float *rstd_q,
+                const float *rstd_k, const void *dout, void *dq, void *dk, void *dv,
+                float *dgamma_q, float *dgamma_k, void *workspace, size_t workspace_bytes,
+                void *stream) {
+    int st = validate_shape(B, S, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    const Problem p = make_problem(B, S, n_heads, n_kv_heads, head_dim, eps, theta, dtype);
+    return run_bwd(p, q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k, dout,
+                   dq, dk, dv, dgamma_q, dgamma_k, workspace, workspace_bytes, stream);
+}
+
+size_t xt_attn_varlen_workspace_bytes(int total, int max_seqlen, int n_heads, int n_kv_heads,
+                                      int head_dim, int dtype, int backward) {
+    if (validate_shape(1, total, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
+    if (max_seqlen <= 0 || max_seqlen > total) return 0;
+    const Problem p = make_problem(1, total, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype);
+    return backward ? bwd_layout(p).total : fwd_workspace(p);
+}
+
+int xt_attn_fwd_varlen(int total, int nseq, int max_seqlen, int n_heads, int n_kv_heads,
+                       int head_dim, double eps, double theta, const int *cu_seqlens,
+                       const void *q, const void *k, const void *v, const float *gamma_q,
+                       const float *gamma_k, int dtype, void *out, float *lse, void *q_hat,
+                       void *k_hat, float *rstd_q, float *rstd_k, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    int st = validate_shape(1, total, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    if ((st = validate_packed(total, nseq, max_seqlen, cu_seqlens, n_heads, dtype)) != XT_OK)
+        return st;
+    const Problem p = make_packed_problem(total, nseq, max_seqlen, cu_seqlens, n_heads,
+                                          n_kv_heads, head_dim, eps, theta, dtype);
+    return run_fwd(p, q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k,
+                   workspace, workspace_bytes, stream);
+}
+
+int xt_attn_bwd_varlen(int total, int nseq, int max_seqlen, int n_heads, int n_kv_heads,
+                       int head_dim, double eps, double theta, const int *cu_seqlens,
+                       const void *q, const void *k, const void *v, const float *gamma_q,
+                       const float *gamma_k, int dtype, const void *out, const float *lse,
+                       const void *q_hat, const void *k_hat, const float *rstd_q,
+                       const float *rstd_k, const void *dout, void *dq, void *dk, void *dv,
+                       float *dgamma_q, float *dgamma_k, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    int st = validate_shape(1, total, n_heads, n_kv_heads, head_dim, dtype);
+    if (st != XT_OK) return st;
+    if ((st = validate_scalars(eps, theta)) != XT_OK) return st;
+    if ((st = validate_packed(total, nseq, max_seqlen, cu_seqlens, n_heads, dtype)) != XT_OK)
+        return st;
+    const Problem p = make_packed_problem(total, nseq, max_seqlen, cu_seqlens, n_heads,
+                                          n_kv_heads, head_dim, eps, theta, dtype);
+    return run_bwd(p, q, k, v, gamma_q, gamma_k, out, lse, q_hat, k_hat, rstd_q, rstd_k, dout,
+                   dq, dk, dv, dgamma_q, dgamma_k, workspace, workspace_bytes, stream);
 }
 
 size_t xt_attn_decode_workspace_bytes(int B, int S_max, int n_heads, int n_kv_heads,

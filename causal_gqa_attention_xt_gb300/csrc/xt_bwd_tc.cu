@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
               const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
               const float *__restrict__ lse, const float *__restrict__ dlt,
-              float *__restrict__ dkhat, bf16 *__restrict__ dv, int S, int H, int G,
+              float *__restrict__ dkhat, bf16 *__restrict__ dv, const SeqRows sr, int H, int G,
               int n_kvt, unsigned int *err) {
     using C = BwdCfg<D>;
     constexpr int HS = C::kHStages;
@@ -157,8 +157,11 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const int BG = gridDim.x / n_kvt;
     const int j = (int)(blockIdx.x / BG);          // key tile, longest first
     const int bg = blockIdx.x % BG;
-    const int b = bg / G, g = bg - b * G, group = H / G;
+    const int unit = bg / G, g = bg - unit * G, group = H / G;
+    const SeqSpan sp = seq_span(sr, unit);
+    const int S = sp.len;                           // rows of this unit
     const int n_q = (S + kTile - 1) / kTile;
+    if (j >= n_q) return;                           // a packed sample shorter than this tile
     const int nU = n_q - j;                         // query tiles at/after the keys, per head
     const int T = group * nU;
     volatile int *abort_flag = &bars.abort_flag;
@@ -181,8 +184,10 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             tma_prefetch_desc(&map_do);
             mbar_expect_tx(&bars.own_full, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(sK + c * 16384, &map_k, &bars.own_full, c * 64, j * kTile, bg);
-                tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g, j * kTile, b);
+                tma_load_3d(sK + c * 16384, &map_k, &bars.own_full, c * 64,
+                            sp.start + j * kTile, sp.plane * G + g);
+                tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g,
+                            sp.start + j * kTile, sp.plane);
             }
         }
         // half tile x = 2 t + hf: rows [64 hf, 64 hf + 64) of streamed tile t
@@ -204,13 +209,14 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             if (lane == 0) {
                 mbar_expect_tx(&bars.st_full[hs], 2 * C::kHalfBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 8192, &map_q, &bars.st_full[hs], c * 64, q0, b * H + h);
+                    tma_load_3d(base + c * 8192, &map_q, &bars.st_full[hs], c * 64,
+                                sp.start + q0, sp.plane * H + h);
                     tma_load_4d(base + C::kHalfBytes + c * 8192, &map_do, &bars.st_full[hs],
-                                c * 64, h, q0, b);
+                                c * 64, h, sp.start + q0, sp.plane);
                 }
             }
             float *sl = reinterpret_cast<float *>(base + 2 * C::kHalfBytes);
-            const size_t row0 = ((size_t)b * H + h) * S;
+            const size_t row0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int kq = lane + 32 * e, q = q0 + kq;
@@ -367,8 +373,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 // 32-column chunks: dV (bf16) chunks 0..D/32-1, then dKhat (fp32, scaled);
                 // warpgroup w writes chunks w, w + kSoftmaxWGs, ...
                 const float scale = rsqrtf((float)D);
-                bf16 *dvrow = dv + (((size_t)b * S + kp) * G + g) * D;
-                float *dkrow = dkhat + ((size_t)bg * S + kp) * D;
+                bf16 *dvrow = dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D;
+                float *dkrow = dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D;
 #pragma unroll
                 for (int cc = wg; cc < 2 * (D / 32); cc += kSoftmaxWGs) {
                     const bool isv = cc < D / 32;
@@ -419,7 +425,8 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
             const bf16 *__restrict__ qhat, const bf16 *__restrict__ dout,
             const float *__restrict__ lse, const float *__restrict__ dlt,
-            float *__restrict__ dqhat, int S, int H, int G, int n_qt, unsigned int *err) {
+            float *__restrict__ dqhat, const SeqRows sr, int H, int G, int n_qt,
+            unsigned int *err) {
     using C = BwdCfg<D>;
     constexpr int ST = C::kStages;
     // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), and the
@@ -434,7 +441,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int BH = gridDim.x / n_qt;
     const int i = n_qt - 1 - (int)(blockIdx.x / BH);   // query tile, longest first
     const int bh = blockIdx.x % BH;
-    const int b = bh / H, h = bh - b * H, g = h / (H / G);
+    const int unit = bh / H, h = bh - unit * H, g = h / (H / G);
+    const SeqSpan sp = seq_span(sr, unit);
+    const int S = sp.len;                              // rows of this unit
+    if (i * kTile >= S) return;                        // a packed sample shorter than this tile
+    const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;   // [.., H, S, ..] rows
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
     // p_full[0]: packed dS of tile t in TMEM; p_full[1]: every softmax thread
@@ -466,10 +477,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 uint8_t *base = sStage + st * C::kStageBytes;
                 mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 16384, &map_k, &bars.st_full[st], c * 64, t * kTile,
-                                b * G + g);
+                    tma_load_3d(base + c * 16384, &map_k, &bars.st_full[st], c * 64,
+                                sp.start + t * kTile, sp.plane * G + g);
                     tma_load_4d(base + C::kTileBytes + c * 16384, &map_v, &bars.st_full[st],
-                                c * 64, g, t * kTile, b);
+                                c * 64, g, sp.start + t * kTile, sp.plane);
                 }
                 issued = t + 1;
             }
@@ -544,16 +555,17 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         const int tq = i * kTile + r;                  // query position
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
-        const float lse2 = tq < S ? lse[(size_t)bh * S + tq] * kLog2e : 0.f;
-        const float dl = tq < S ? dlt[(size_t)bh * S + tq] : 0.f;
+        const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
+        const float dl = tq < S ? dlt[qrow0 + tq] : 0.f;
         if (wg < 2) {
             // the owned Qhat (warpgroup 0) and dO (warpgroup 1) rows become TMEM-resident
             // A operands (lane = row; a 32-bit column holds two consecutive bf16, the lower
             // index in the low half)
             uint32_t xa[D / 2];
             const uint4 *src = wg == 0
-                ? reinterpret_cast<const uint4 *>(qhat + ((size_t)bh * S + tq) * D)
-                : reinterpret_cast<const uint4 *>(dout + (((size_t)b * S + tq) * H + h) * D);
+                ? reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D)
+                : reinterpret_cast<const uint4 *>(
+                      dout + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D);
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
@@ -610,7 +622,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             if (ok) {
                 tc_fence_after();
                 const float scale = rsqrtf((float)D);
-                float *dst = dqhat + ((size_t)bh * S + tq) * D;
+                float *dst = dqhat + (qrow0 + tq) * D;
                 // warpgroup w writes the 32-column chunks w, w + kSoftmaxWGs, ... of the row
 #pragma unroll
                 for (int c = wg; c < D / 32; c += kSoftmaxWGs) {
@@ -685,13 +697,14 @@ template <int D>
 cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, const float *dlt,
                           float *dkhat, void *dv, unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
-    const int n_kvt = (p.S + kTile - 1) / kTile;
-    const long blocks = (long)p.B * p.G * n_kvt;
+    const int n_kvt = (p.max_len + kTile - 1) / kTile;
+    const long blocks = (long)p.units * p.G * n_kvt;
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemA);
     if (e != cudaSuccess) return e;
     k_bwd_dkdv_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
-        m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, p.S, p.H, p.G, n_kvt, err);
+        m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, SeqRows{p.cu, p.S, p.max_len}, p.H,
+        p.G, n_kvt, err);
     return cudaGetLastError();
 }
 
@@ -700,13 +713,14 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
                         const float *lse, const float *dlt, float *dqhat, unsigned int *err,
                         cudaStream_t st) {
     using C = BwdCfg<D>;
-    const int n_qt = (p.S + kTile - 1) / kTile;
-    const long blocks = (long)p.B * p.H * n_qt;
+    const int n_qt = (p.max_len + kTile - 1) / kTile;
+    const long blocks = (long)p.units * p.H * n_qt;
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, dqhat, p.S, p.H, p.G, n_qt, err);
+        m.k, m.v, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, dqhat,
+        SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
     return cudaGetLastError();
 }
 

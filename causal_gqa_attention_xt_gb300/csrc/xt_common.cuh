@@ -77,4 +77,29 @@ __device__ __forceinline__ float group_sum(float v, int width) {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Rows of the attention kernels. A unit is either a batch element b (plane b
+// of the [B, ..., S, ...] tensors, rows 0..S-1) or, for a packed batch (cu set;
+// Mint report 8.2: samples flattened into one [total] row dimension), a sample
+// u on rows cu[u]..cu[u+1]-1 of plane 0 of tensors whose row count S is the
+// total. Causal masking inside the unit is then the block-causal mask: a
+// unit's tiles never start before its first row, and rows past its end are
+// only visible to query rows past its end, which are not stored.
+struct SeqRows {
+    const int *cu;   // [units + 1] row offsets (device), or nullptr
+    int S;           // rows per plane
+    int max_len;     // longest unit: S, or the packed batch's longest sample
+};
+struct SeqSpan {
+    int plane, start, len;
+};
+// Offsets out of order or out of range are clamped into [0, S] (with a
+// length of at most max_len), so every access stays inside the tensors; the
+// library's offset check reports them.
+__device__ __forceinline__ SeqSpan seq_span(const SeqRows &sr, int u) {
+    if (sr.cu == nullptr) return SeqSpan{u, 0, sr.S};
+    const int s0 = min(max(sr.cu[u], 0), sr.S);
+    const int s1 = min(max(sr.cu[u + 1], s0), min(sr.S, s0 + sr.max_len));
+    return SeqSpan{0, s0, s1 - s0};
+}
+
 }  // namespace xt

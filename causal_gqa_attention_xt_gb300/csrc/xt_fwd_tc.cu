@@ -65,7 +65,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
 k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
          const __grid_constant__ CUtensorMap map_v, bf16 *__restrict__ out,
-         float *__restrict__ lse, int S, int H, int G, int n_pairs, unsigned int *err) {
+         float *__restrict__ lse, const SeqRows sr, int H, int G, int n_pairs,
+         unsigned int *err) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBarriers bars;
@@ -77,14 +78,17 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     const int BH = gridDim.x / n_pairs;
     const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);   // longest first
     const int bh = blockIdx.x % BH;
-    const int b = bh / H, h = bh - b * H, g = h / (H / G);
-    const int n_qtiles = (S + kBM - 1) / kBM;
+    const int unit = bh / H, h = bh - unit * H, g = h / (H / G);
+    const SeqSpan sp = seq_span(sr, unit);
+    const int n_qtiles = (sp.len + kBM - 1) / kBM;
     int n_kv[2];
     for (int i = 0; i < 2; ++i) {
         const int qt = 2 * pair + i;
         n_kv[i] = qt < n_qtiles ? qt + 1 : 0;
     }
+    if (n_kv[0] == 0) return;   // a packed sample shorter than this pair's rows
     const int n_iter = max(n_kv[0], n_kv[1]);
+    const int qplane = sp.plane * H + h, kplane = sp.plane * G + g;
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) {
@@ -122,7 +126,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             for (int i = 0; i < nq; ++i)
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_3d(sQ + i * C::kTileBytes + c * 16384, &map_q, &bars.q_full, c * 64,
-                                (2 * pair + i) * kBM, bh);
+                                sp.start + (2 * pair + i) * kBM, qplane);
             int issued = 0;
             for (int j = 0; j < n_iter; ++j) {
                 const int st = j % C::kStages;
@@ -135,11 +139,12 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                 uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
                 mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + c * 16384, &map_k, &bars.k_full[st], c * 64, j * kBN,
-                                b * G + g);
+                    tma_load_3d(sK + c * 16384, &map_k, &bars.k_full[st], c * 64,
+                                sp.start + j * kBN, kplane);
                 mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sV + c * 16384, &map_v, &bars.v_full[st], c * 64, g, j * kBN, b);
+                    tma_load_4d(sV + c * 16384, &map_v, &bars.v_full[st], c * 64, g,
+                                sp.start + j * kBN, sp.plane);
                 issued = j + 1;
             }
             // Drain: every copy this CTA issued must land before it exits.
@@ -224,7 +229,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         const int i = warp >> 2;                 // query tile of this warpgroup
         const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter+32)
         const int r = quarter * 32 + lane;       // row within the tile
-        const int t = (2 * pair + i) * kBM + r;  // query position
+        const int t = (2 * pair + i) * kBM + r;  // query position inside the unit
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off;
         const uint32_t tO = tmem + 256 + i * 128 + lane_off;
@@ -296,12 +301,13 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             if (__all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (n - 1) & 1, abort_flag))) {
                 tc_fence_after();
                 const float inv_l = 1.0f / l;
-                bf16 *dst = out + (((size_t)b * S + t) * H + h) * D;
+                const size_t row = (size_t)sp.plane * sr.S + sp.start + t;
+                bf16 *dst = out + (row * H + h) * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
                     tmem_ld32_sync(tO + c * 32, o);
-                    if (t < S) {
+                    if (t < sp.len) {
 #pragma unroll
                         for (int q8 = 0; q8 < 4; ++q8) {
                             uint4 v;
@@ -313,7 +319,8 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                         }
                     }
                 }
-                if (t < S) lse[(size_t)bh * S + t] = (m_used + __log2f(l)) * kLn2;
+                if (t < sp.len)
+                    lse[(size_t)qplane * sr.S + sp.start + t] = (m_used + __log2f(l)) * kLn2;
             } else {
                 ok = false;
             }
@@ -355,14 +362,14 @@ cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat
         cudaError_t e = encode_tmap_bf16(&mv, v, 4, dims, strides, box);
         if (e != cudaSuccess) return e;
     }
-    const int n_qtiles = (p.S + kBM - 1) / kBM;
+    const int n_qtiles = (p.max_len + kBM - 1) / kBM;
     const int n_pairs = (n_qtiles + 1) / 2;
-    const long blocks = (long)p.B * p.H * n_pairs;
+    const long blocks = (long)p.units * p.H * n_pairs;
     cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     k_fwd_tc<D><<<(unsigned)blocks, kThreadsFwd, C::kSmemBytes, st>>>(
-        mq, mk, mv, (bf16 *)out, lse, p.S, p.H, p.G, n_pairs, err);
+        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_pairs, err);
     return cudaGetLastError();
 }
 

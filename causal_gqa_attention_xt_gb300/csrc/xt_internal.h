@@ -29,16 +29,23 @@ enum KernelId {
     KID_COUNT
 };
 
+// B planes of S rows. A packed batch is B = 1, S = total rows, with the
+// samples' row offsets cu [units + 1] (device) and the longest sample max_len;
+// a plain batch has cu = nullptr, units = B, max_len = S.
 struct Problem {
     int B, S, H, G, D;
     float eps;
     double theta;
     int dtype;  // 0 = fp32, 1 = bf16
+    const int *cu;
+    int units, max_len;
     int group() const { return H / G; }
 };
 
-// Error word bits: a bounded wait ran out; a decode position was out of range.
-enum : unsigned int { ERR_TIMEOUT = 1u, ERR_BADPOS = 2u };
+// Error word bits: a bounded wait ran out; a decode position was out of
+// range; packed-batch offsets were not 0 = cu[0] <= ... <= cu[n] = total
+// with every sample at most max_len rows.
+enum : unsigned int { ERR_TIMEOUT = 1u, ERR_BADPOS = 2u, ERR_BADSEQ = 4u };
 
 // ---- norm / RoPE kernels (xt_normrope.cu) ----
 // Persistent grids: at most this many CTAs, which bounds the number of
@@ -49,8 +56,10 @@ constexpr int kMaxNormParts = 1024;
 constexpr int kMaxHeads = 8 * kMaxNormParts;
 // cos/sin table [S][D/2] of (cos, sin) float pairs, filled by launch_rope_table
 // and read by the prologue and the epilogue.
+// A packed batch gets one table row per packed row (its position inside its
+// sample); that launch also checks the offsets (ERR_BADSEQ).
 size_t rope_table_bytes(const Problem &p);
-cudaError_t launch_rope_table(const Problem &p, void *tab, cudaStream_t st);
+cudaError_t launch_rope_table(const Problem &p, void *tab, unsigned int *err, cudaStream_t st);
 cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, const float *gq,
                             const float *gk, const void *tab, void *qhat, void *khat,
                             float *rstd_q, float *rstd_k, unsigned int *err, cudaStream_t st);

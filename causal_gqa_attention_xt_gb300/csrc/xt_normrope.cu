@@ -83,9 +83,13 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
 }
 
 // ---------------------------------------------------------------- RoPE table
-// tab[s * half + i] = (cos, sin) of s * theta^(-2i/D), s < S, i < half.
+// tab[s * half + i] = (cos, sin) of pos(s) * theta^(-2i/D), s < S, i < half,
+// where pos(s) = s, or for a packed batch (cu set) the row's position inside
+// its sample (Mint report 8.2: positions restart in every sample), s - cu[u]
+// for the last sample u with cu[u] <= s. Block 0 also checks the offsets.
 __global__ void __launch_bounds__(256)
-k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ RopeConsts rc) {
+k_rope_table(float2 *__restrict__ tab, int S, int half, const int *__restrict__ cu, int units,
+             int max_len, unsigned int *err, const __grid_constant__ RopeConsts rc) {
     __shared__ float fhi[kRopeMaxHalf], flo[kRopeMaxHalf];
     __shared__ double fd[kRopeMaxHalf];
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
@@ -93,12 +97,29 @@ k_rope_table(float2 *__restrict__ tab, int S, int half, const __grid_constant__ 
         flo[i] = rc.flo[i];
         fd[i] = rc.fd[i];
     }
+    if (cu != nullptr && blockIdx.x == 0) {
+        for (int u = threadIdx.x; u < units; u += blockDim.x) {
+            const int a = cu[u], b = cu[u + 1];
+            if ((u == 0 && a != 0) || b < a || b - a > max_len || (u == units - 1 && b != S))
+                atomicOr(err, ERR_BADSEQ);
+        }
+    }
     __syncthreads();
     const long n = (long)S * half;
     for (long e = (long)blockIdx.x * blockDim.x + threadIdx.x; e < n;
          e += (long)gridDim.x * blockDim.x) {
         const int s = (int)(e / half), i = (int)(e - (long)s * half);
-        tab[e] = rope_cos_sin(s, fhi[i], flo[i], fd[i]);
+        int pos = s;
+        if (cu != nullptr) {
+            int lo = 0, hi = units;   // cu[lo] <= s < cu[hi] for well-formed offsets
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cu[mid] <= s) lo = mid;
+                else hi = mid;
+            }
+            pos = max(0, s - cu[lo]);
+        }
+        tab[e] = rope_cos_sin(pos, fhi[i], flo[i], fd[i]);
     }
 }
 
@@ -596,11 +617,13 @@ int rows_per_iter(int D, int dtype, bool halves) {
 
 size_t rope_table_bytes(const Problem &p) { return (size_t)p.S * (p.D / 2) * sizeof(float2); }
 
-cudaError_t launch_rope_table(const Problem &p, void *tab, cudaStream_t st) {
+cudaError_t launch_rope_table(const Problem &p, void *tab, unsigned int *err, cudaStream_t st) {
     const long n = (long)p.S * (p.D / 2);
     long blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    k_rope_table<<<(unsigned)blocks, 256, 0, st>>>((float2 *)tab, p.S, p.D / 2, make_rope_consts(p.theta, p.D));
+    k_rope_table<<<(unsigned)blocks, 256, 0, st>>>((float2 *)tab, p.S, p.D / 2, p.cu, p.units,
+                                                   p.max_len, err,
+                                                   make_rope_consts(p.theta, p.D));
     return cudaGetLastError();
 }
 

@@ -43,20 +43,25 @@ __device__ __forceinline__ void stage_tile(float *dst, int ld, const T *src, siz
 template <typename T>
 __global__ void __launch_bounds__(256)
 k_fwd_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__restrict__ v,
-           T *__restrict__ out, float *__restrict__ lse, int S, int H, int G, int D) {
+           T *__restrict__ out, float *__restrict__ lse, const SeqRows sr, int H, int G, int D) {
     extern __shared__ float sm[];
     const int ldk = D + 1;
     float *Qs = sm;                    // [32][D]
     float *Ks = Qs + kBR * D;          // [32][D+1]
     float *Vs = Ks + kBC * ldk;        // [32][D]
-    const int bh = blockIdx.y, b = bh / H, h = bh - b * H, g = h / (H / G);
+    const int bh = blockIdx.y, unit = bh / H, h = bh - unit * H, g = h / (H / G);
+    const SeqSpan sp = seq_span(sr, unit);
+    const int S = sp.len;
     const int q0 = blockIdx.x * kBR;
+    if (q0 >= S) return;   // a packed sample shorter than this block's rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float sl2 = kLog2e * rsqrtf((float)D);
+    const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;   // [.., H, S, ..] rows
+    const size_t trow0 = (size_t)sp.plane * sr.S + sp.start;              // [.., S, heads, ..] rows
 
-    const T *qsrc = qhat + ((size_t)bh * S) * D;
-    const T *ksrc = khat + ((size_t)(b * G + g) * S) * D;
-    const T *vsrc = v + ((size_t)b * S * G + g) * D;   // row stride G*D
+    const T *qsrc = qhat + qrow0 * D;
+    const T *ksrc = khat + (((size_t)sp.plane * G + g) * sr.S + sp.start) * D;
+    const T *vsrc = v + (trow0 * G + g) * D;   // row stride G*D
     stage_tile<T>(Qs, D, qsrc, D, q0, min(kBR, S - q0), D);
 
     float m[kRowsPerWarp], l[kRowsPerWarp], o[kRowsPerWarp][4];
@@ -108,9 +113,9 @@ k_fwd_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__re
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int d = lane + 32 * c;
-            if (d < D) out[(((size_t)b * S + t) * H + h) * D + d] = from_f32<T>(o[r][c] * inv);
+            if (d < D) out[((trow0 + t) * H + h) * D + d] = from_f32<T>(o[r][c] * inv);
         }
-        if (lane == 0) lse[(size_t)bh * S + t] = (m[r] + log2f(l[r])) * kLn2;
+        if (lane == 0) lse[qrow0 + t] = (m[r] + log2f(l[r])) * kLn2;
     }
 }
 
@@ -119,30 +124,35 @@ template <typename T>
 __global__ void __launch_bounds__(256)
 k_dq_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__restrict__ v,
           const T *__restrict__ dout, const float *__restrict__ lse, const float *__restrict__ dlt,
-          float *__restrict__ dqhat, int S, int H, int G, int D) {
+          float *__restrict__ dqhat, const SeqRows sr, int H, int G, int D) {
     extern __shared__ float sm[];
     const int ld = D + 1;
     float *Qs = sm;                 // [32][D]
     float *dOs = Qs + kBR * D;      // [32][D]
     float *Ks = dOs + kBR * D;      // [32][D+1]
     float *Vs = Ks + kBC * ld;      // [32][D+1]
-    const int bh = blockIdx.y, b = bh / H, h = bh - b * H, g = h / (H / G);
+    const int bh = blockIdx.y, unit = bh / H, h = bh - unit * H, g = h / (H / G);
+    const SeqSpan sp = seq_span(sr, unit);
+    const int S = sp.len;
     const int q0 = blockIdx.x * kBR;
+    if (q0 >= S) return;   // a packed sample shorter than this block's rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float scale = rsqrtf((float)D);
     const float sl2 = kLog2e * scale;
+    const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
+    const size_t trow0 = (size_t)sp.plane * sr.S + sp.start;
 
-    stage_tile<T>(Qs, D, qhat + ((size_t)bh * S) * D, D, q0, min(kBR, S - q0), D);
-    stage_tile<T>(dOs, D, dout + ((size_t)b * S * H + h) * D, (size_t)H * D, q0, min(kBR, S - q0), D);
-    const T *ksrc = khat + ((size_t)(b * G + g) * S) * D;
-    const T *vsrc = v + ((size_t)b * S * G + g) * D;
+    stage_tile<T>(Qs, D, qhat + qrow0 * D, D, q0, min(kBR, S - q0), D);
+    stage_tile<T>(dOs, D, dout + (trow0 * H + h) * D, (size_t)H * D, q0, min(kBR, S - q0), D);
+    const T *ksrc = khat + (((size_t)sp.plane * G + g) * sr.S + sp.start) * D;
+    const T *vsrc = v + (trow0 * G + g) * D;
 
     float lse2[kRowsPerWarp], dl[kRowsPerWarp], acc[kRowsPerWarp][4];
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) {
         const int t = q0 + warp * kRowsPerWarp + r;
-        lse2[r] = t < S ? lse[(size_t)bh * S + t] * kLog2e : 0.f;
-        dl[r] = t < S ? dlt[(size_t)bh * S + t] : 0.f;
+        lse2[r] = t < S ? lse[qrow0 + t] * kLog2e : 0.f;
+        dl[r] = t < S ? dlt[qrow0 + t] : 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[r][c] = 0.f;
     }
@@ -184,7 +194,7 @@ k_dq_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__res
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             const int d = lane + 32 * c;
-            if (d < D) dqhat[((size_t)bh * S + t) * D + d] = acc[r][c] * scale;
+            if (d < D) dqhat[(qrow0 + t) * D + d] = acc[r][c] * scale;
         }
     }
 }
@@ -199,7 +209,7 @@ __global__ void __launch_bounds__(256)
 k_dkdv_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__restrict__ v,
             const T *__restrict__ dout, const float *__restrict__ lse,
             const float *__restrict__ dlt, float *__restrict__ dkhat, T *__restrict__ dv,
-            int S, int H, int G, int D) {
+            const SeqRows sr, int H, int G, int D) {
     extern __shared__ float sm[];
     const int ld = D + 1;
     float *Ks = sm;                 // [32][D+1] own key rows
@@ -208,14 +218,19 @@ k_dkdv_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__r
     float *dOs = Qs + kBC * ld;     // [32][D+1]
     float *lse2s = dOs + kBC * ld;  // [32]
     float *dls = lse2s + kBC;       // [32]
-    const int bg = blockIdx.y, b = bg / G, g = bg - b * G, group = H / G;
+    const int bg = blockIdx.y, unit = bg / G, g = bg - unit * G, group = H / G;
+    const SeqSpan sp = seq_span(sr, unit);
+    const int S = sp.len;
     const int j0 = blockIdx.x * kBR;
+    if (j0 >= S) return;   // a packed sample shorter than this block's rows
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const float scale = rsqrtf((float)D);
     const float sl2 = kLog2e * scale;
+    const size_t krow0 = ((size_t)sp.plane * G + g) * sr.S + sp.start;
+    const size_t trow0 = (size_t)sp.plane * sr.S + sp.start;
 
-    stage_tile<T>(Ks, ld, khat + ((size_t)bg * S) * D, D, j0, min(kBR, S - j0), D);
-    stage_tile<T>(Vs, ld, v + ((size_t)b * S * G + g) * D, (size_t)G * D, j0, min(kBR, S - j0), D);
+    stage_tile<T>(Ks, ld, khat + krow0 * D, D, j0, min(kBR, S - j0), D);
+    stage_tile<T>(Vs, ld, v + (trow0 * G + g) * D, (size_t)G * D, j0, min(kBR, S - j0), D);
 
     float dk[kRowsPerWarp][4], dvv[kRowsPerWarp][4];
 #pragma unroll
@@ -224,9 +239,10 @@ k_dkdv_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__r
         for (int c = 0; c < 4; ++c) { dk[r][c] = 0.f; dvv[r][c] = 0.f; }
 
     for (int rr = 0; rr < group; ++rr) {
-        const int h = g * group + rr, bh = b * H + h;
-        const T *qsrc = qhat + ((size_t)bh * S) * D;
-        const T *dsrc = dout + ((size_t)b * S * H + h) * D;
+        const int h = g * group + rr;
+        const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
+        const T *qsrc = qhat + qrow0 * D;
+        const T *dsrc = dout + (trow0 * H + h) * D;
         for (int t0 = j0; t0 < S; t0 += kBC) {
             __syncthreads();
             const int nv = min(kBC, S - t0);
@@ -234,8 +250,8 @@ k_dkdv_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__r
             stage_tile<T>(dOs, ld, dsrc, (size_t)H * D, t0, nv, D);
             if (threadIdx.x < kBC) {
                 const int t = t0 + threadIdx.x;
-                lse2s[threadIdx.x] = t < S ? lse[(size_t)bh * S + t] * kLog2e : 0.f;
-                dls[threadIdx.x] = t < S ? dlt[(size_t)bh * S + t] : 0.f;
+                lse2s[threadIdx.x] = t < S ? lse[qrow0 + t] * kLog2e : 0.f;
+                dls[threadIdx.x] = t < S ? dlt[qrow0 + t] : 0.f;
             }
             __syncthreads();
 #pragma unroll
@@ -276,8 +292,8 @@ k_dkdv_simt(const T *__restrict__ qhat, const T *__restrict__ khat, const T *__r
         for (int c = 0; c < 4; ++c) {
             const int d = lane + 32 * c;
             if (d < D) {
-                dkhat[((size_t)bg * S + j) * D + d] = dk[r][c] * scale;
-                dv[(((size_t)b * S + j) * G + g) * D + d] = from_f32<T>(dvv[r][c]);
+                dkhat[(krow0 + j) * D + d] = dk[r][c] * scale;
+                dv[((trow0 + j) * G + g) * D + d] = from_f32<T>(dvv[r][c]);
             }
         }
     }
@@ -293,19 +309,19 @@ cudaError_t allow_smem(K kernel, size_t bytes) {
 
 cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,
                             void *out, float *lse, cudaStream_t st) {
-    dim3 grid((p.S + kBR - 1) / kBR, p.B * p.H);
+    dim3 grid((p.max_len + kBR - 1) / kBR, p.units * p.H);
     size_t smem = sizeof(float) * (kBR * p.D + kBC * (p.D + 1) + kBC * p.D);
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = allow_smem(k_fwd_simt<bf16>, smem)) != cudaSuccess) return e;
         k_fwd_simt<bf16><<<grid, 256, smem, st>>>((const bf16 *)qhat, (const bf16 *)khat,
-                                                  (const bf16 *)v, (bf16 *)out, lse, p.S, p.H,
-                                                  p.G, p.D);
+                                                  (const bf16 *)v, (bf16 *)out, lse,
+                                                  SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, p.D);
     } else {
         if ((e = allow_smem(k_fwd_simt<float>, smem)) != cudaSuccess) return e;
         k_fwd_simt<float><<<grid, 256, smem, st>>>((const float *)qhat, (const float *)khat,
-                                                   (const float *)v, (float *)out, lse, p.S,
-                                                   p.H, p.G, p.D);
+                                                   (const float *)v, (float *)out, lse,
+                                                   SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, p.D);
     }
     return cudaGetLastError();
 }
@@ -313,19 +329,21 @@ cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat
 cudaError_t launch_bwd_dq_simt(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
                                const float *dlt, float *dqhat, cudaStream_t st) {
-    dim3 grid((p.S + kBR - 1) / kBR, p.B * p.H);
+    dim3 grid((p.max_len + kBR - 1) / kBR, p.units * p.H);
     size_t smem = sizeof(float) * (2 * kBR * p.D + 2 * kBC * (p.D + 1));
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = allow_smem(k_dq_simt<bf16>, smem)) != cudaSuccess) return e;
         k_dq_simt<bf16><<<grid, 256, smem, st>>>((const bf16 *)qhat, (const bf16 *)khat,
                                                  (const bf16 *)v, (const bf16 *)dout, lse, dlt,
-                                                 dqhat, p.S, p.H, p.G, p.D);
+                                                 dqhat, SeqRows{p.cu, p.S, p.max_len}, p.H,
+                                                 p.G, p.D);
     } else {
         if ((e = allow_smem(k_dq_simt<float>, smem)) != cudaSuccess) return e;
         k_dq_simt<float><<<grid, 256, smem, st>>>((const float *)qhat, (const float *)khat,
                                                   (const float *)v, (const float *)dout, lse,
-                                                  dlt, dqhat, p.S, p.H, p.G, p.D);
+                                                  dlt, dqhat, SeqRows{p.cu, p.S, p.max_len},
+                                                  p.H, p.G, p.D);
     }
     return cudaGetLastError();
 }
@@ -333,20 +351,21 @@ cudaError_t launch_bwd_dq_simt(const Problem &p, const void *qhat, const void *k
 cudaError_t launch_bwd_dkdv_simt(const Problem &p, const void *qhat, const void *khat,
                                  const void *v, const void *dout, const float *lse,
                                  const float *dlt, float *dkhat, void *dv, cudaStream_t st) {
-    dim3 grid((p.S + kBR - 1) / kBR, p.B * p.G);
+    dim3 grid((p.max_len + kBR - 1) / kBR, p.units * p.G);
     size_t smem = sizeof(float) * (4 * kBR * (p.D + 1) + 2 * kBC);
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = allow_smem(k_dkdv_simt<bf16>, smem)) != cudaSuccess) return e;
         k_dkdv_simt<bf16><<<grid, 256, smem, st>>>((const bf16 *)qhat, (const bf16 *)khat,
                                                    (const bf16 *)v, (const bf16 *)dout, lse, dlt,
-                                                   dkhat, (bf16 *)dv, p.S, p.H, p.G, p.D);
+                                                   dkhat, (bf16 *)dv,
+                                                   SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, p.D);
     } else {
         if ((e = allow_smem(k_dkdv_simt<float>, smem)) != cudaSuccess) return e;
         k_dkdv_simt<float><<<grid, 256, smem, st>>>((const float *)qhat, (const float *)khat,
                                                     (const float *)v, (const float *)dout, lse,
-                                                    dlt, dkhat, (float *)dv, p.S, p.H, p.G,
-                                                    p.D);
+                                                    dlt, dkhat, (float *)dv,
+                                                    SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, p.D);
     }
     return cudaGetLastError();
 }

@@ -9,6 +9,12 @@ q [B,S,H,D], k [B,S,G,D], v [B,S,G,D] and dout [B,S,H,D] ~ N(0, 1) in fp32,
 drawn in that order, then gamma_q and gamma_k = 1 + 0.1 * N(0, 1) [D], fp32.
 For bf16 workloads q, k, v and dout are rounded to bf16 (round to nearest
 even, ``Tensor.to``); the gammas stay fp32.
+
+Packed batches (samples of different lengths flattened into one row
+dimension) draw q [T,H,D], k, v [T,G,D], dout [T,H,D] and the gammas the same
+way, T the sum of the lengths. The benchmark's length mix draws each sample's
+length uniformly from [lo, hi] with its own generator (seed + 1) until the
+total is reached; the last sample takes the remainder.
 """
 from __future__ import annotations
 
@@ -94,3 +100,80 @@ def make_inputs(w: Workload, gamma_scale: float = 0.1, gamma_offset: float = 1.0
 def to_f64(inputs: dict) -> dict:
     """The same tensors widened exactly to float64 numpy arrays."""
     return {k: v.to(torch.float64).numpy() for k, v in inputs.items()}
+
+
+@dataclass(frozen=True)
+class PackedWorkload:
+    """Samples of the given lengths packed into one [T] row dimension."""
+    name: str
+    lens: tuple
+    H: int
+    G: int
+    D: int
+    theta: float
+    eps: float
+    dtype: str
+    seed: int = 0
+
+    @property
+    def T(self) -> int:
+        return int(sum(self.lens))
+
+    @property
+    def max_len(self) -> int:
+        return int(max(self.lens))
+
+    @property
+    def cu(self) -> list:
+        out = [0]
+        for n in self.lens:
+            out.append(out[-1] + int(n))
+        return out
+
+    @property
+    def fwd_flops(self) -> float:
+        """Causal forward FLOPs, counted per sample as 2 * H * len^2 * D."""
+        return float(sum(2.0 * self.H * n * n * self.D for n in self.lens))
+
+    @property
+    def bwd_flops(self) -> float:
+        return 2.5 * self.fwd_flops
+
+
+def length_mix(total: int, lo: int, hi: int, seed: int) -> tuple:
+    """Sample lengths drawn uniformly from [lo, hi] until they sum to total."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed + 1)
+    lens = []
+    left = total
+    while left > 0:
+        n = int(torch.randint(lo, hi + 1, (1,), generator=g).item())
+        n = min(n, left)
+        lens.append(n)
+        left -= n
+    return tuple(lens)
+
+
+PACKED_WORKLOADS = {
+    # 16384 rows (the Qwen3-like batch's rows) as samples of 256..4096 rows
+    "qwen3_like_varlen_bf16": PackedWorkload("qwen3_like_varlen_bf16",
+                                             length_mix(16384, 256, 4096, 0), 32, 8, 128,
+                                             1e6, 1e-6, "bf16"),
+}
+
+
+def make_packed_inputs(w: PackedWorkload, gamma_scale: float = 0.1, gamma_offset: float = 1.0):
+    """CPU tensors of a packed batch: q, k, v, dout (workload dtype), gammas
+    (fp32) and cu_seqlens (int32 [nseq + 1])."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    T = w.T
+    q = torch.randn((T, w.H, w.D), generator=g, dtype=torch.float32)
+    k = torch.randn((T, w.G, w.D), generator=g, dtype=torch.float32)
+    v = torch.randn((T, w.G, w.D), generator=g, dtype=torch.float32)
+    dout = torch.randn((T, w.H, w.D), generator=g, dtype=torch.float32)
+    gamma_q = gamma_offset + gamma_scale * torch.randn((w.D,), generator=g, dtype=torch.float32)
+    gamma_k = gamma_offset + gamma_scale * torch.randn((w.D,), generator=g, dtype=torch.float32)
+    dt = torch_dtype(w.dtype)
+    return dict(q=q.to(dt), k=k.to(dt), v=v.to(dt), dout=dout.to(dt), gamma_q=gamma_q,
+                gamma_k=gamma_k, cu_seqlens=torch.tensor(w.cu, dtype=torch.int32))

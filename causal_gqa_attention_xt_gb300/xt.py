@@ -55,6 +55,14 @@ def lib():
     L.xt_attn_bwd_noalloc.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
                                       vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.xt_attn_bwd_noalloc.restype = i
+    L.xt_attn_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.xt_attn_varlen_workspace_bytes.restype = sz
+    L.xt_attn_fwd_varlen.argtypes = [i, i, i, i, i, i, d, d, vp, vp, vp, vp, vp, vp, i, vp, vp,
+                                     vp, vp, vp, vp, vp, sz, vp]
+    L.xt_attn_fwd_varlen.restype = i
+    L.xt_attn_bwd_varlen.argtypes = [i, i, i, i, i, i, d, d, vp, vp, vp, vp, vp, vp, i, vp, vp,
+                                     vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.xt_attn_bwd_varlen.restype = i
     L.xt_attn_decode_workspace_bytes.argtypes = [i, i, i, i, i, i]
     L.xt_attn_decode_workspace_bytes.restype = sz
     L.xt_attn_decode.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
@@ -190,6 +198,84 @@ def xt_attn_bwd_noalloc(q, k, v, gamma_q, gamma_k, saved, dout, eps, theta, *, d
                                    _ptr(dgamma_q), _ptr(dgamma_k), _stream(stream))
     if st != XT_OK:
         raise XtError(st, "xt_attn_bwd_noalloc")
+    return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
+
+
+def xt_attn_varlen_workspace_bytes(total, max_seqlen, n_heads, n_kv_heads, head_dim, dtype,
+                                   backward) -> int:
+    code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
+    return int(lib().xt_attn_varlen_workspace_bytes(total, max_seqlen, n_heads, n_kv_heads,
+                                                    head_dim, code, int(bool(backward))))
+
+
+def _check_cu(cu_seqlens):
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D int32 CUDA tensor of nseq + 1 offsets")
+    return cu_seqlens.numel() - 1
+
+
+def xt_attn_fwd_varlen(q, k, v, gamma_q, gamma_k, cu_seqlens, max_seqlen, eps, theta, *,
+                       out=None, lse=None, q_hat=None, k_hat=None, rstd_q=None, rstd_k=None,
+                       workspace=None, stream=None):
+    """Forward over a packed batch: sample s on rows cu_seqlens[s]..cu_seqlens[s+1]-1.
+
+    q [T,H,D], k/v [T,G,D], cu_seqlens int32 [nseq+1] on the device, max_seqlen
+    the longest sample (host int). Returns a dict: out [T,H,D], lse [H,T],
+    q_hat [H,T,D], k_hat [G,T,D], rstd_q [T,H], rstd_k [T,G].
+    """
+    T, H, D = q.shape
+    G = k.shape[1]
+    nseq = _check_cu(cu_seqlens)
+    dev, dt = q.device, q.dtype
+    f32 = dict(device=dev, dtype=torch.float32)
+    out = out if out is not None else torch.empty((T, H, D), device=dev, dtype=dt)
+    lse = lse if lse is not None else torch.empty((H, T), **f32)
+    q_hat = q_hat if q_hat is not None else torch.empty((H, T, D), device=dev, dtype=dt)
+    k_hat = k_hat if k_hat is not None else torch.empty((G, T, D), device=dev, dtype=dt)
+    rstd_q = rstd_q if rstd_q is not None else torch.empty((T, H), **f32)
+    rstd_k = rstd_k if rstd_k is not None else torch.empty((T, G), **f32)
+    code = _dtype_code(dt)
+    need = xt_attn_varlen_workspace_bytes(T, max_seqlen, H, G, D, code, False)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    wbytes = workspace.numel() * workspace.element_size()
+    st = lib().xt_attn_fwd_varlen(T, nseq, int(max_seqlen), H, G, D, float(eps), float(theta),
+                                  _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q),
+                                  _ptr(gamma_k), code, _ptr(out), _ptr(lse), _ptr(q_hat),
+                                  _ptr(k_hat), _ptr(rstd_q), _ptr(rstd_k), _ptr(workspace),
+                                  wbytes, _stream(stream))
+    if st != XT_OK:
+        raise XtError(st, "xt_attn_fwd_varlen")
+    return dict(out=out, lse=lse, q_hat=q_hat, k_hat=k_hat, rstd_q=rstd_q, rstd_k=rstd_k)
+
+
+def xt_attn_bwd_varlen(q, k, v, gamma_q, gamma_k, cu_seqlens, max_seqlen, saved, dout, eps,
+                       theta, *, dq=None, dk=None, dv=None, dgamma_q=None, dgamma_k=None,
+                       workspace=None, stream=None):
+    """Backward over a packed batch; ``saved`` is the dict xt_attn_fwd_varlen returned."""
+    T, H, D = q.shape
+    G = k.shape[1]
+    nseq = _check_cu(cu_seqlens)
+    dev, dt = q.device, q.dtype
+    dq = dq if dq is not None else torch.empty_like(q)
+    dk = dk if dk is not None else torch.empty_like(k)
+    dv = dv if dv is not None else torch.empty_like(v)
+    dgamma_q = dgamma_q if dgamma_q is not None else torch.empty(D, device=dev, dtype=torch.float32)
+    dgamma_k = dgamma_k if dgamma_k is not None else torch.empty(D, device=dev, dtype=torch.float32)
+    code = _dtype_code(dt)
+    need = xt_attn_varlen_workspace_bytes(T, max_seqlen, H, G, D, code, True)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
+    wbytes = workspace.numel() * workspace.element_size()
+    st = lib().xt_attn_bwd_varlen(T, nseq, int(max_seqlen), H, G, D, float(eps), float(theta),
+                                  _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q),
+                                  _ptr(gamma_k), code, _ptr(saved["out"]), _ptr(saved["lse"]),
+                                  _ptr(saved["q_hat"]), _ptr(saved["k_hat"]),
+                                  _ptr(saved["rstd_q"]), _ptr(saved["rstd_k"]), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dgamma_q), _ptr(dgamma_k),
+                                  _ptr(workspace), wbytes, _stream(stream))
+    if st != XT_OK:
+        raise XtError(st, "xt_attn_bwd_varlen")
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
 
 

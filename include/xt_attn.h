@@ -44,8 +44,8 @@
  *
  * Supported shapes: B, S, H, G >= 1, H % G == 0, H + G <= 8192; dtype
  * XT_BF16 with head_dim 64 or 128 (tensor-core path), dtype XT_F32 with
- * head_dim a multiple of 8 up to 128 (fp32 CUDA-core path). Every tensor must
- * hold fewer than 2^31 elements.
+ * head_dim a multiple of 8 up to 128 and B * H <= 65535 (fp32 CUDA-core
+ * path). Every tensor must hold fewer than 2^31 elements.
  *
  * Errors: calls validate their arguments on the host before any launch and
  * return an xt_status; no call aborts the process. XT_ECUDA reports a launch
@@ -135,6 +135,51 @@ int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                         const float *rstd_q, const float *rstd_k, const void *dout,
                         void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
                         void *stream);
+
+/* ------------------------------------------------------- packed batches
+ * Variable-length samples packed into one row dimension (Mint project
+ * report, 8.2, forward pass of a chat batch: the batch is flattened to
+ * [total] rows, RoPE numbers the positions inside each sample, and a
+ * block-causal mask hides every other sample's rows entirely and, inside a
+ * sample, the later rows). Sample s holds rows cu_seqlens[s] ..
+ * cu_seqlens[s+1]-1; its rows sit at positions 0, 1, ... for RoPE and attend
+ * causally to the rows of the same sample only. The operation per sample is
+ * exactly xt_attn_fwd / xt_attn_bwd with B = 1, S = its length.
+ *
+ * Layouts: the batched ones with B = 1 and S = total:
+ *    q, out, dout, dq  [total, H, D];  k, v, dk, dv  [total, G, D]
+ *    q_hat [H, total, D];  k_hat [G, total, D];  lse [H, total]
+ *    rstd_q [total, H];  rstd_k [total, G]
+ * cu_seqlens: int32 [nseq + 1] in device memory (4-byte aligned), with
+ * 0 = cu[0] <= cu[1] <= ... <= cu[nseq] = total (empty samples allowed) and
+ * every cu[s+1] - cu[s] <= max_seqlen; 0 < max_seqlen <= total, nseq >= 1.
+ * Offsets are read on the device: the host checks nseq, max_seqlen and the
+ * pointer (XT_EINVAL), and a device-side check of the offsets raises the
+ * error word, which xt_attn_check() reports as XT_EINVAL (accesses stay in
+ * bounds either way; results are then unspecified).
+ * Workspace: xt_attn_varlen_workspace_bytes() (the forward's RoPE table has
+ * one row per packed row). Grids are sized by max_seqlen: a short sample's
+ * blocks past its end exit at once. dtype XT_F32 needs nseq * n_heads <= 65535.
+ * Deterministic, like the batched calls. */
+size_t xt_attn_varlen_workspace_bytes(int total, int max_seqlen, int n_heads, int n_kv_heads,
+                                      int head_dim, int dtype, int backward);
+
+int xt_attn_fwd_varlen(int total, int nseq, int max_seqlen, int n_heads, int n_kv_heads,
+                       int head_dim, double eps, double theta, const int *cu_seqlens,
+                       const void *q, const void *k, const void *v,
+                       const float *gamma_q, const float *gamma_k, int dtype,
+                       void *out, float *lse, void *q_hat, void *k_hat,
+                       float *rstd_q, float *rstd_k,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
+int xt_attn_bwd_varlen(int total, int nseq, int max_seqlen, int n_heads, int n_kv_heads,
+                       int head_dim, double eps, double theta, const int *cu_seqlens,
+                       const void *q, const void *k, const void *v,
+                       const float *gamma_q, const float *gamma_k, int dtype,
+                       const void *out, const float *lse, const void *q_hat, const void *k_hat,
+                       const float *rstd_q, const float *rstd_k, const void *dout,
+                       void *dq, void *dk, void *dv, float *dgamma_q, float *dgamma_k,
+                       void *workspace, size_t workspace_bytes, void *stream);
 
 /* ---------------------------------------------------------------- decode
  * One decode step against a key/value cache (Mint project report, 10.3 "KV

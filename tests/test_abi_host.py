@@ -115,3 +115,42 @@ def test_decode_validation_and_workspace(L):
     bad = list(args)
     bad[2] = 3
     assert L.xt_attn_decode(*bad, p, *tail, p, need, None) == xt.XT_EINVAL
+
+
+def test_fp32_grid_limit(L):
+    # the fp32 path runs one grid row per (batch element, head): at most 65535
+    assert _fwd(L, B=65536 // 2, S=1, H=2, G=2, D=16) == xt.XT_EUNSUPPORTED
+    assert _fwd(L, B=65536 // 2, S=1, H=2, G=2, D=64, dtype=1, ptr=0) == xt.XT_EINVAL   # bf16: not limited
+
+
+def _fwd_varlen(L, total=64, nseq=3, max_seqlen=32, H=4, G=2, D=64, dtype=1, cu=16, ptr=16,
+                ws=None, wbytes=0):
+    p = ctypes.c_void_p(ptr)
+    return L.xt_attn_fwd_varlen(total, nseq, max_seqlen, H, G, D, 1e-5, 1e4, ctypes.c_void_p(cu),
+                                p, p, p, p, p, dtype, p, p, p, p, p, p, ws, wbytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(nseq=0), xt.XT_EINVAL), (dict(max_seqlen=0), xt.XT_EINVAL),
+    (dict(max_seqlen=65), xt.XT_EINVAL), (dict(cu=0), xt.XT_EINVAL), (dict(cu=18), xt.XT_EINVAL),
+    (dict(total=0), xt.XT_EINVAL), (dict(H=3), xt.XT_EINVAL), (dict(ptr=8), xt.XT_EINVAL),
+    (dict(D=32), xt.XT_EUNSUPPORTED),
+    (dict(nseq=20000, D=16, dtype=0), xt.XT_EUNSUPPORTED),   # fp32 grid limit: nseq * H
+])
+def test_varlen_validation_rejects_before_launch(L, kw, code):
+    assert _fwd_varlen(L, **kw) == code
+
+
+def test_varlen_workspace(L):
+    fneed = xt.xt_attn_varlen_workspace_bytes(1000, 300, 4, 2, 64, 1, False)
+    bneed = xt.xt_attn_varlen_workspace_bytes(1000, 300, 4, 2, 64, 1, True)
+    assert fneed >= 1000 * 32 * 8 and bneed > fneed   # one (cos, sin) row per packed row
+    assert xt.xt_attn_varlen_workspace_bytes(1000, 1001, 4, 2, 64, 1, False) == 0
+    assert _fwd_varlen(L, ws=ctypes.c_void_p(16), wbytes=100) == xt.XT_EWORKSPACE
+    p = ctypes.c_void_p(16)
+    need = xt.xt_attn_varlen_workspace_bytes(64, 32, 4, 2, 64, 1, True)
+    args = [64, 3, 32, 4, 2, 64, 1e-5, 1e4, p] + [p] * 5 + [1] + [p] * 7 + [p] * 5
+    assert L.xt_attn_bwd_varlen(*args, p, need - 1, None) == xt.XT_EWORKSPACE
+    bad = list(args)
+    bad[2] = 0
+    assert L.xt_attn_bwd_varlen(*bad, p, need, None) == xt.XT_EINVAL
