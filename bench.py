@@ -10,11 +10,16 @@ per-step CUDA events.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the CPU oracle timed on host cores
   python bench.py --mode decode ...      # one decode step against a full KV cache
+  python bench.py --mode varlen ...      # fwd+bwd over a packed batch of unequal samples
 
 In decode mode a step is one xt_attn_decode call: every sequence's next token
 against a cache that holds its whole capacity (the largest cache read), and
 the metric is the cache bytes read per second (K-hat and V rows, the algorithmic
 bytes of the step); the cache is larger than L2, so no flush is needed.
+
+In varlen mode a step is xt_attn_fwd_varlen + xt_attn_bwd_varlen over 16384
+packed rows (samples of 256..4096 rows, seeded), FLOPs counted per sample as
+2*H*len^2*D forward and 2.5x that backward; otherwise as the default mode.
 
 Under torchrun (N > 1) every rank runs its own shard of independent batch
 units on its own GPU (weak scaling, no collective on the data path); rank 0
@@ -23,6 +28,7 @@ prints one JSON line with the max-over-ranks time.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -40,6 +46,9 @@ DEFAULT_WORKLOAD = "qwen3_like_bf16"
 DECODE_METRIC = ("GQA decode step (each sequence's next token against its full KV cache): "
                  "cache bytes read per second at 1 GB300")
 DECODE_WORKLOAD = "qwen3_like_decode_bf16"
+VARLEN_METRIC = ("packed variable-length causal GQA attention fwd+bwd TFLOP/s (block-causal, "
+                 "FLOPs counted per sample) at 1 GB300")
+VARLEN_WORKLOAD = "qwen3_like_varlen_bf16"
 
 
 def load_peaks():
@@ -189,7 +198,15 @@ def cpu_baseline(w, seconds_target=20.0):
             "sample": desc, "seconds": dt}
 
 
-def bench_reference(args, w):
+def longest_sample(w):
+    """The longest sample of a packed batch as a one-element batched workload
+    (what the oracle times for the packed mode's CPU numbers)."""
+    from causal_gqa_attention_xt_gb300.inputs import Workload
+    return Workload(w.name + "_longest", 1, w.max_len, w.H, w.G, w.D, w.theta, w.eps, w.dtype,
+                    w.seed)
+
+
+def bench_reference(args, w, metric=None, workload_name=None):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
@@ -209,12 +226,14 @@ def bench_reference(args, w):
     flops = sub.fwd_flops + sub.bwd_flops
     value = flops * len(times) / sum(times) / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric or METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G,
-                   "head_dim": w.D, "theta": w.theta, "eps": w.eps, "sample_per_step": desc},
+        "config": {"workload": workload_name or w.name, "B": w.B, "S": w.S, "n_heads": w.H,
+                   "n_kv_heads": w.G, "head_dim": w.D, "theta": w.theta, "eps": w.eps,
+                   "sample_per_step": desc},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -230,7 +249,7 @@ def bench_ours(args, w):
 
     from causal_gqa_attention_xt_gb300 import build as xbuild
     from causal_gqa_attention_xt_gb300 import xt
-    from causal_gqa_attention_xt_gb300.inputs import make_inputs
+    from causal_gqa_attention_xt_gb300.inputs import PackedWorkload, make_inputs, make_packed_inputs
 
     rank, world, local = dist_env()
     if world > 1:
@@ -239,38 +258,56 @@ def bench_ours(args, w):
     dev = torch.device("cuda", torch.cuda.current_device())
     xbuild.build()
     xt.lib()
+    packed = isinstance(w, PackedWorkload)
+    code = 1 if w.dtype == "bf16" else 0
 
     # each rank owns its own shard of batch units (weak scaling)
-    wr = w.with_(seed=shard_seed(w.seed, rank))
-    cpu = make_inputs(wr)
-    d = {k: v.to(dev) for k, v in cpu.items()}
-    saved = xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta)
-    grads = xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
-                           w.eps, w.theta)
-    ws = torch.empty(xt.xt_attn_workspace_bytes(w.B, w.S, w.H, w.G, w.D, w.dtype == "bf16" and 1 or 0, True),
-                     device=dev, dtype=torch.uint8)
+    if packed:
+        wr = dataclasses.replace(w, seed=shard_seed(w.seed, rank))
+        cpu = make_packed_inputs(wr)
+        d = {k: v.to(dev) for k, v in cpu.items()}
+
+        def fwd(**kw):
+            return xt.xt_attn_fwd_varlen(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"],
+                                         d["cu_seqlens"], w.max_len, w.eps, w.theta, **kw)
+
+        def bwd(saved_, **kw):
+            return xt.xt_attn_bwd_varlen(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"],
+                                         d["cu_seqlens"], w.max_len, saved_, d["dout"], w.eps,
+                                         w.theta, **kw)
+
+        ws_bytes = xt.xt_attn_varlen_workspace_bytes(w.T, w.max_len, w.H, w.G, w.D, code, True)
+    else:
+        wr = w.with_(seed=shard_seed(w.seed, rank))
+        cpu = make_inputs(wr)
+        d = {k: v.to(dev) for k, v in cpu.items()}
+
+        def fwd(**kw):
+            return xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps,
+                                  w.theta, **kw)
+
+        def bwd(saved_, **kw):
+            return xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved_,
+                                  d["dout"], w.eps, w.theta, **kw)
+
+        ws_bytes = xt.xt_attn_workspace_bytes(w.B, w.S, w.H, w.G, w.D, code, True)
+    saved = fwd()
+    grads = bwd(saved)
+    ws = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     flush = torch.empty(512 * 1024 * 1024, device=dev, dtype=torch.uint8)
     stream = torch.cuda.current_stream()
 
-    def step():
-        xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
-                       out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
-                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"],
-                       workspace=ws)
-        xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
-                       w.eps, w.theta, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
-                       dgamma_q=grads["dgamma_q"], dgamma_k=grads["dgamma_k"], workspace=ws)
-
     def fwd_only():
-        xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
-                       out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"],
-                       k_hat=saved["k_hat"], rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"],
-                       workspace=ws)
+        fwd(out=saved["out"], lse=saved["lse"], q_hat=saved["q_hat"], k_hat=saved["k_hat"],
+            rstd_q=saved["rstd_q"], rstd_k=saved["rstd_k"], workspace=ws)
 
     def bwd_only():
-        xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], saved, d["dout"],
-                       w.eps, w.theta, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"],
-                       dgamma_q=grads["dgamma_q"], dgamma_k=grads["dgamma_k"], workspace=ws)
+        bwd(saved, dq=grads["dq"], dk=grads["dk"], dv=grads["dv"], dgamma_q=grads["dgamma_q"],
+            dgamma_k=grads["dgamma_k"], workspace=ws)
+
+    def step():
+        fwd_only()
+        bwd_only()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -375,7 +412,8 @@ def bench_ours(args, w):
                         "frac_of_sustained": ach / peaks["tflops_sustained"],
                         "traffic": None, "avg_launch_ms": tot_ms / n}
         else:
-            rows_q, rows_k = w.B * w.S * w.H, w.B * w.S * w.G
+            rows = w.T if packed else w.B * w.S
+            rows_q, rows_k = rows * w.H, rows * w.G
             algo_bytes = {
                 "prologue_qknorm_rope": 2 * esz * D * (rows_q + rows_k) + 4 * (rows_q + rows_k),
                 "bwd_epilogue_rope_norm": (4 + 2 * esz) * D * (rows_q + rows_k) + 4 * (rows_q + rows_k),
@@ -399,14 +437,22 @@ def bench_ours(args, w):
             pass
 
     launches = sum(n for _, n in per_kernel.values())
+    if packed:
+        config = {"workload": w.name, "total_rows": w.T, "samples": len(w.lens),
+                  "lengths": list(w.lens), "max_seqlen": w.max_len, "n_heads": w.H,
+                  "n_kv_heads": w.G, "head_dim": w.D, "theta": w.theta, "eps": w.eps,
+                  "length_mix": "uniform 256..4096 rows per sample (seeded), last takes the rest"}
+    else:
+        config = {"workload": w.name, "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G,
+                  "head_dim": w.D, "theta": w.theta, "eps": w.eps, "per_rank_batch": w.B}
+    config["l2"] = "flushed between timed steps (512 MB write, outside the step events)"
+    config["inputs"] = "N(0,1) q/k/v/dout rounded to bf16, gammas 1+0.1*N(0,1) fp32, seed 0+rank"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": VARLEN_METRIC if packed else METRIC, "value": value, "unit": UNIT,
+        "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G,
-                   "head_dim": w.D, "theta": w.theta, "eps": w.eps, "per_rank_batch": w.B,
-                   "l2": "flushed between timed steps (512 MB write, outside the step events)",
-                   "inputs": "N(0,1) q/k/v/dout rounded to bf16, gammas 1+0.1*N(0,1) fp32, seed 0+rank"},
+        "config": config,
         "fwd": {"ms": fwd_ms_m, "tflops": w.fwd_flops / (fwd_ms_m * 1e-3) / 1e12,
                 "frac_of_peak": w.fwd_flops / (fwd_ms_m * 1e-3) / 1e12 / peaks["tflops"]},
         "bwd": {"ms": bwd_ms_m, "tflops": w.bwd_flops / (bwd_ms_m * 1e-3) / 1e12,
@@ -422,7 +468,7 @@ def bench_ours(args, w):
         "wall_s_timed_region": wall,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(longest_sample(w) if packed else w)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
@@ -710,8 +756,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--mode", choices=["train", "decode"], default="train",
-                    help="train: fwd+bwd step (the headline); decode: one KV-cache decode step")
+    ap.add_argument("--mode", choices=["train", "decode", "varlen"], default="train",
+                    help="train: fwd+bwd step (the headline); decode: one KV-cache decode step; "
+                         "varlen: fwd+bwd over a packed batch of unequal samples")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seq", type=int, default=1024,
@@ -720,7 +767,15 @@ def main(argv=None):
     ap.add_argument("--profile-run", action="store_true",
                     help="one warm-up and one fwd+bwd step, no timing (for ncu captures)")
     args = ap.parse_args(argv)
-    from causal_gqa_attention_xt_gb300.inputs import WORKLOADS
+    from causal_gqa_attention_xt_gb300.inputs import PACKED_WORKLOADS, WORKLOADS
+    if args.mode == "varlen":
+        w = PACKED_WORKLOADS[args.workload or VARLEN_WORKLOAD]
+        if args.warmup < 3:
+            ap.error("--warmup must be >= 3")
+        if args.impl == "reference":
+            return bench_reference(args, longest_sample(w), metric=VARLEN_METRIC,
+                                   workload_name=w.name)
+        return bench_ours(args, w)
     w = WORKLOADS[args.workload or (DECODE_WORKLOAD if args.mode == "decode" else DEFAULT_WORKLOAD)]
     if args.batch is not None:
         w = w.with_(B=args.batch, name=f"{w.name}_B{args.batch}")
