@@ -98,7 +98,7 @@ int validate_shape(int B, int S, int H, int G, int D, int dtype) {
     if (dtype != XT_F32 && dtype != XT_BF16) return XT_EINVAL;
     const double big = (double)B * (double)S * (double)H * (double)D;
     if (big >= 2147483648.0) return XT_EINVAL;
-    if (dtype == XT_BF16 && D != 64 && D != 128) return XT_EUNSUPPORTED;
+    if (dtype == XT_BF16 && D != 32 && D != 64 && D != 128) return XT_EUNSUPPORTED;
     if (dtype == XT_F32 && (D % 8 != 0 || D > 128)) return XT_EUNSUPPORTED;
     if (H + G > kMaxHeads) return XT_EUNSUPPORTED;
     if (dtype == XT_F32 && (long)B * H > 65535) return XT_EUNSUPPORTED;   // grid.y of the fp32 path

@@ -68,9 +68,12 @@ constexpr int kThreadsBwd = 32 * (kWarpMma + 1);
 constexpr int kMaxStages = 8;
 
 template <int D> struct BwdCfg {
-    static constexpr int kChunks = D / 64;
-    static constexpr int kTileBytes = kChunks * 16384;   // 128 rows x D bf16
-    static constexpr int kHalfBytes = kChunks * 8192;    // 64 rows x D bf16
+    using A = Atoms<D>;
+    static constexpr int kChunks = A::kPerRow;            // swizzle atoms (TMA boxes) per row
+    static constexpr int kBox = A::box_bytes(kTile);      // one box of 128 rows
+    static constexpr int kHalfBox = A::box_bytes(kTile / 2);
+    static constexpr int kTileBytes = kChunks * kBox;     // 128 rows x D bf16
+    static constexpr int kHalfBytes = kChunks * kHalfBox; // 64 rows x D bf16
     // dQ kernel: a stage holds a K and a V tile
     static constexpr int kStages = (D == 128) ? 2 : 4;
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;
@@ -126,13 +129,14 @@ __device__ __forceinline__ uint32_t packed_col(int kk) {
     return (uint32_t)((kk >> 1) * kWgCols + (kk & 1) * 8);
 }
 
-// Operand descriptors (128B swizzle, 8-row groups 1024 B apart): a K-major
-// operand advances 16 elements by +32 B inside a 64-column chunk (16 KB for
-// 128 rows, 8 KB for a 64-row half tile); an MN-major B operand advances 16
-// rows by +2048 B, its 64-column N chunks a chunk apart (in the descriptor).
-constexpr uint64_t kmajor_off(int kk) { return (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; }
-constexpr uint64_t kmajor_off_half(int kk) { return (uint64_t)((kk >> 2) * 8192 + (kk & 3) * 32) >> 4; }
-constexpr uint64_t mnmajor_off(int kk) { return (uint64_t)(kk * 2048) >> 4; }
+// Operand descriptor offsets (tc::Atoms: 128- or 64-byte swizzle rows, 8-row
+// groups): a K-major operand advances 16 elements by +32 B inside an atom
+// column, atom columns a box apart (128 rows, or 64 for a half tile); an
+// MN-major B operand advances 16 rows by 16 atom rows, its N atoms a box apart
+// (in the descriptor).
+template <int D> constexpr uint64_t kmajor_off(int kk) { return (uint64_t)Atoms<D>::kstep(kk, kTile) >> 4; }
+template <int D> constexpr uint64_t kmajor_off_half(int kk) { return (uint64_t)Atoms<D>::kstep(kk, kTile / 2) >> 4; }
+template <int D> constexpr uint64_t mnmajor_off(int kk) { return (uint64_t)Atoms<D>::mnstep(kk) >> 4; }
 
 // ---------------------------------------------------------------------------
 // dKhat, dV
@@ -184,9 +188,9 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             tma_prefetch_desc(&map_do);
             mbar_expect_tx(&bars.own_full, 2 * C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_3d(sK + c * 16384, &map_k, &bars.own_full, c * 64,
+                tma_load_3d(sK + c * C::kBox, &map_k, &bars.own_full, c * C::A::kCols,
                             sp.start + j * kTile, sp.plane * G + g);
-                tma_load_4d(sV + c * 16384, &map_v, &bars.own_full, c * 64, g,
+                tma_load_4d(sV + c * C::kBox, &map_v, &bars.own_full, c * C::A::kCols, g,
                             sp.start + j * kTile, sp.plane);
             }
         }
@@ -209,10 +213,10 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             if (lane == 0) {
                 mbar_expect_tx(&bars.st_full[hs], 2 * C::kHalfBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 8192, &map_q, &bars.st_full[hs], c * 64,
-                                sp.start + q0, sp.plane * H + h);
-                    tma_load_4d(base + C::kHalfBytes + c * 8192, &map_do, &bars.st_full[hs],
-                                c * 64, h, sp.start + q0, sp.plane);
+                    tma_load_3d(base + c * C::kHalfBox, &map_q, &bars.st_full[hs],
+                                c * C::A::kCols, sp.start + q0, sp.plane * H + h);
+                    tma_load_4d(base + C::kHalfBytes + c * C::kHalfBox, &map_do,
+                                &bars.st_full[hs], c * C::A::kCols, h, sp.start + q0, sp.plane);
                 }
             }
             float *sl = reinterpret_cast<float *>(base + 2 * C::kHalfBytes);
@@ -238,12 +242,14 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile / 2, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
-            const uint64_t dK = smem_desc(smem_u32(sK), 16, 1024, kSwizzle128B);
-            const uint64_t dV = smem_desc(smem_u32(sV), 16, 1024, kSwizzle128B);
-            const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
-            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 16, 1024, kSwizzle128B);
-            const uint64_t dQm0 = smem_desc(smem_u32(sStage), 8192, 1024, kSwizzle128B);
-            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 8192, 1024, kSwizzle128B);
+            using A = typename C::A;
+            const uint64_t dK = smem_desc(smem_u32(sK), 16, A::kSBO, A::kMode);
+            const uint64_t dV = smem_desc(smem_u32(sV), 16, A::kSBO, A::kMode);
+            const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, A::kSBO, A::kMode);
+            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 16, A::kSBO, A::kMode);
+            const uint64_t dQm0 = smem_desc(smem_u32(sStage), C::kHalfBox, A::kSBO, A::kMode);
+            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kHalfBytes), C::kHalfBox, A::kSBO,
+                                             A::kMode);
             constexpr uint64_t kStep = (uint64_t)C::kHStageBytes >> 4;
             // S^T = Khat Qhat^T and dP^T = V dO^T for the queries [64h, 64h+64) of
             // tile t, from half stage (2t + h) % HS
@@ -251,12 +257,12 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 const uint64_t so = (uint64_t)((2 * t + h) % HS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 64 * h, dK + kmajor_off(kk), dQk0 + so + kmajor_off_half(kk),
+                    mma_ss(tmem + 64 * h, dK + kmajor_off<D>(kk), dQk0 + so + kmajor_off_half<D>(kk),
                            idesc_s, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off(kk),
-                           dDOk0 + so + kmajor_off_half(kk), idesc_s, kk > 0);
+                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off<D>(kk),
+                           dDOk0 + so + kmajor_off_half<D>(kk), idesc_s, kk > 0);
                 mma_commit(&bars.s_full[h]);
             };
             bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
@@ -280,13 +286,13 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dV += P^T dO
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off(k4),
+                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off<D>(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dKhat += dS^T Qhat
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off(k4),
+                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off<D>(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(&bars.st_empty[hs]);       // this half stage may be reloaded
@@ -477,10 +483,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 uint8_t *base = sStage + st * C::kStageBytes;
                 mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * 16384, &map_k, &bars.st_full[st], c * 64,
+                    tma_load_3d(base + c * C::kBox, &map_k, &bars.st_full[st], c * C::A::kCols,
                                 sp.start + t * kTile, sp.plane * G + g);
-                    tma_load_4d(base + C::kTileBytes + c * 16384, &map_v, &bars.st_full[st],
-                                c * 64, g, sp.start + t * kTile, sp.plane);
+                    tma_load_4d(base + C::kTileBytes + c * C::kBox, &map_v, &bars.st_full[st],
+                                c * C::A::kCols, g, sp.start + t * kTile, sp.plane);
                 }
                 issued = t + 1;
             }
@@ -492,9 +498,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
-            const uint64_t dKk0 = smem_desc(smem_u32(sStage), 16, 1024, kSwizzle128B);
-            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, 1024, kSwizzle128B);
-            const uint64_t dKm0 = smem_desc(smem_u32(sStage), 16384, 1024, kSwizzle128B);
+            using A = typename C::A;
+            const uint64_t dKk0 = smem_desc(smem_u32(sStage), 16, A::kSBO, A::kMode);
+            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, A::kSBO, A::kMode);
+            const uint64_t dKm0 = smem_desc(smem_u32(sStage), C::kBox, A::kSBO, A::kMode);
             constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
             // S = Qhat Khat^T and dP = dO V^T (A in TMEM), full 128-key tiles: the
             // TS form at N = 128 runs at the full MMA rate (N = 64 does not)
@@ -502,13 +509,13 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off(kk), idesc_s, kk > 0);
+                    mma_ts(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off<D>(kk), idesc_s, kk > 0);
             };
             auto issue_dp = [&](int t) {
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off(kk), idesc_s,
+                    mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off<D>(kk), idesc_s,
                            kk > 0);
                 mma_commit(&bars.s_full[0]);         // S and dP of tile t are in TMEM
             };
@@ -538,7 +545,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off(kk),
+                    mma_ts(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off<D>(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&bars.st_empty[st]);
                 if (t + 1 < T) issue_dp(t + 1);
@@ -573,7 +580,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             }
             const uint32_t dst = tmem + (wg == 0 ? kTQ : kTDO) + lane_off;
             if constexpr (D == 128) tmem_st64_sync(dst, xa);
-            else tmem_st32_sync(dst, xa);
+            else if constexpr (D == 64) tmem_st32_sync(dst, xa);
+            else tmem_st16_sync(dst, xa);
             tc_fence_before();
             mbar_arrive(&bars.own_full);
         }
@@ -660,35 +668,40 @@ struct BwdMaps {
 };
 
 // Qhat [B*H, S, D] / Khat [B*G, S, D] as 3-D maps; V [B, S, G, D] and
-// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of 64 columns x 128 rows
-// (K, V: whole tiles) or x 64 rows (Qhat, dO: the dK/dV kernel's half tiles).
+// dO [B, S, H, D] as 4-D maps (D, heads, S, B); boxes of one swizzle atom's
+// columns (tc::Atoms) x 128 rows (K, V: whole tiles) or x 64 rows (Qhat, dO:
+// the dK/dV kernel's half tiles).
+template <int DD>
 cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, const void *v,
                       const void *dout, BwdMaps &m) {
+    using A = Atoms<DD>;
     const uint64_t esz = 2, D = (uint64_t)p.D;
+    const uint32_t bc = (uint32_t)A::kCols;
+    const int sw = A::kSwizzleBytes;
     cudaError_t e;
     {
         const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, (uint32_t)kTile / 2, 1};
-        if ((e = encode_tmap_bf16(&m.q, qhat, 3, dims, strides, box)) != cudaSuccess) return e;
+        const uint32_t box[3] = {bc, (uint32_t)kTile / 2, 1};
+        if ((e = encode_tmap_bf16(&m.q, qhat, 3, dims, strides, box, sw)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.G};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, (uint32_t)kTile, 1};
-        if ((e = encode_tmap_bf16(&m.k, khat, 3, dims, strides, box)) != cudaSuccess) return e;
+        const uint32_t box[3] = {bc, (uint32_t)kTile, 1};
+        if ((e = encode_tmap_bf16(&m.k, khat, 3, dims, strides, box, sw)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[4] = {D, (uint64_t)p.G, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.G * D * esz, (uint64_t)p.S * p.G * D * esz};
-        const uint32_t box[4] = {64, 1, (uint32_t)kTile, 1};
-        if ((e = encode_tmap_bf16(&m.v, v, 4, dims, strides, box)) != cudaSuccess) return e;
+        const uint32_t box[4] = {bc, 1, (uint32_t)kTile, 1};
+        if ((e = encode_tmap_bf16(&m.v, v, 4, dims, strides, box, sw)) != cudaSuccess) return e;
     }
     {
         const uint64_t dims[4] = {D, (uint64_t)p.H, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.H * D * esz, (uint64_t)p.S * p.H * D * esz};
-        const uint32_t box[4] = {64, 1, (uint32_t)kTile / 2, 1};
-        if ((e = encode_tmap_bf16(&m.dout, dout, 4, dims, strides, box)) != cudaSuccess) return e;
+        const uint32_t box[4] = {bc, 1, (uint32_t)kTile / 2, 1};
+        if ((e = encode_tmap_bf16(&m.dout, dout, 4, dims, strides, box, sw)) != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
@@ -724,28 +737,44 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t run_dkdv(const Problem &p, const void *qhat, const void *khat, const void *v,
+                     const void *dout, const float *lse, const float *dlt, float *dkhat, void *dv,
+                     unsigned int *err, cudaStream_t st) {
+    BwdMaps m;
+    cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
+    if (e != cudaSuccess) return e;
+    return launch_dkdv_d<D>(p, m, lse, dlt, dkhat, dv, err, st);
+}
+
+template <int D>
+cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const void *v,
+                   const void *dout, const float *lse, const float *dlt, float *dqhat,
+                   unsigned int *err, cudaStream_t st) {
+    BwdMaps m;
+    cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
+    if (e != cudaSuccess) return e;
+    return launch_dq_d<D>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
+}
+
 }  // namespace
 
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
                                const float *dlt, float *dkhat, void *dv, unsigned int *err,
                                cudaStream_t st) {
-    BwdMaps m;
-    cudaError_t e = make_maps(p, qhat, khat, v, dout, m);
-    if (e != cudaSuccess) return e;
-    if (p.D == 128) return launch_dkdv_d<128>(p, m, lse, dlt, dkhat, dv, err, st);
-    if (p.D == 64) return launch_dkdv_d<64>(p, m, lse, dlt, dkhat, dv, err, st);
+    if (p.D == 128) return run_dkdv<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
+    if (p.D == 64) return run_dkdv<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
+    if (p.D == 32) return run_dkdv<32>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                              const void *dout, const float *lse, const float *dlt, float *dqhat,
                              unsigned int *err, cudaStream_t st) {
-    BwdMaps m;
-    cudaError_t e = make_maps(p, qhat, khat, v, dout, m);
-    if (e != cudaSuccess) return e;
-    if (p.D == 128) return launch_dq_d<128>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
-    if (p.D == 64) return launch_dq_d<64>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
+    if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
+    if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
+    if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
     return cudaErrorInvalidValue;
 }
 

@@ -580,11 +580,15 @@ cudaError_t run_decode_attn(const Problem &p, const DecodePlan &d, const int *po
 cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int *pos,
                                const float *qhat, const void *kc, const void *vc, float *part_o,
                                float *part_ml, unsigned int *err, cudaStream_t st) {
-    if (p.dtype == 1)
-        return p.D == 128 ? run_decode_attn<bf16, 128, true>(p, d, pos, qhat, kc, vc, part_o,
-                                                             part_ml, err, st)
-                          : run_decode_attn<bf16, 64, true>(p, d, pos, qhat, kc, vc, part_o,
-                                                            part_ml, err, st);
+    if (p.dtype == 1) {
+        if (p.D == 128)
+            return run_decode_attn<bf16, 128, true>(p, d, pos, qhat, kc, vc, part_o, part_ml, err,
+                                                    st);
+        if (p.D == 64)
+            return run_decode_attn<bf16, 64, true>(p, d, pos, qhat, kc, vc, part_o, part_ml, err,
+                                                   st);
+        return run_decode_attn<bf16, 64, false>(p, d, pos, qhat, kc, vc, part_o, part_ml, err, st);
+    }
     if (p.D > 64)
         return run_decode_attn<float, 128, false>(p, d, pos, qhat, kc, vc, part_o, part_ml, err, st);
     if (p.D > 32)

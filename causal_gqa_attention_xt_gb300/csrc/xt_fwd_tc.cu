@@ -41,9 +41,11 @@ constexpr int kThreadsFwd = 320;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int D> struct FwdCfg {
-    static constexpr int kChunks = D / 64;                 // 64-column swizzle atoms per row
-    static constexpr int kTileBytes = kChunks * 16384;     // one 128-row tile
-    static constexpr int kStages = (D == 128) ? 2 : 4;     // K/V ring depth
+    using A = Atoms<D>;
+    static constexpr int kChunks = A::kPerRow;              // swizzle atoms (TMA boxes) per row
+    static constexpr int kBox = A::box_bytes(128);          // one box of a 128-row tile
+    static constexpr int kTileBytes = kChunks * kBox;       // one 128-row tile
+    static constexpr int kStages = (D == 128) ? 2 : 4;      // K/V ring depth
     static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + 1024;
 };
 
@@ -125,8 +127,8 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             mbar_expect_tx(&bars.q_full, nq * C::kTileBytes);
             for (int i = 0; i < nq; ++i)
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sQ + i * C::kTileBytes + c * 16384, &map_q, &bars.q_full, c * 64,
-                                sp.start + (2 * pair + i) * kBM, qplane);
+                    tma_load_3d(sQ + i * C::kTileBytes + c * C::kBox, &map_q, &bars.q_full,
+                                c * C::A::kCols, sp.start + (2 * pair + i) * kBM, qplane);
             int issued = 0;
             for (int j = 0; j < n_iter; ++j) {
                 const int st = j % C::kStages;
@@ -139,11 +141,11 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                 uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
                 mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + c * 16384, &map_k, &bars.k_full[st], c * 64,
+                    tma_load_3d(sK + c * C::kBox, &map_k, &bars.k_full[st], c * C::A::kCols,
                                 sp.start + j * kBN, kplane);
                 mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sV + c * 16384, &map_v, &bars.v_full[st], c * 64, g,
+                    tma_load_4d(sV + c * C::kBox, &map_v, &bars.v_full[st], c * C::A::kCols, g,
                                 sp.start + j * kBN, sp.plane);
                 issued = j + 1;
             }
@@ -168,9 +170,10 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             const uint32_t tO[2] = {tmem + 256, tmem + 384};
             // Descriptors are built once; per MMA only a compile-time offset (>> 4, the
             // start-address field) is added, which keeps the single issuing thread fast.
-            const uint64_t dQ0 = smem_desc(smem_u32(sQ), 16, 1024, kSwizzle128B);
-            const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, 1024, kSwizzle128B);
-            const uint64_t dV0 = smem_desc(smem_u32(sKV + C::kTileBytes), 16384, 1024, kSwizzle128B);
+            using A = typename C::A;
+            const uint64_t dQ0 = smem_desc(smem_u32(sQ), 16, A::kSBO, A::kMode);
+            const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, A::kSBO, A::kMode);
+            const uint64_t dV0 = smem_desc(smem_u32(sKV + C::kTileBytes), C::kBox, A::kSBO, A::kMode);
             constexpr uint64_t kStageStep = (uint64_t)(2 * C::kTileBytes) >> 4;
             constexpr uint64_t kQStep = (uint64_t)C::kTileBytes >> 4;
             auto issue_s = [&](int i, int st) {
@@ -178,7 +181,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                 const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint64_t off = (uint64_t)A::kstep(kk, kBM) >> 4;
                     mma_ss(tS[i], dQ + off, dK + off, idesc_s, kk > 0);
                 }
                 mma_commit(&bars.s_full[i]);
@@ -201,7 +204,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)((kk * 2048) >> 4), idesc_o,
+                        mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)(A::mnstep(kk) >> 4), idesc_o,
                                (j > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&bars.o_done[i]);
                     if (j + 1 < n_kv[i]) {
@@ -344,22 +347,22 @@ cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat
     {
         const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.H};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, kBM, 1};
-        cudaError_t e = encode_tmap_bf16(&mq, qhat, 3, dims, strides, box);
+        const uint32_t box[3] = {(uint32_t)C::A::kCols, kBM, 1};
+        cudaError_t e = encode_tmap_bf16(&mq, qhat, 3, dims, strides, box, C::A::kSwizzleBytes);
         if (e != cudaSuccess) return e;
     }
     {
         const uint64_t dims[3] = {(uint64_t)D, (uint64_t)p.S, (uint64_t)p.B * p.G};
         const uint64_t strides[2] = {D * esz, (uint64_t)p.S * D * esz};
-        const uint32_t box[3] = {64, kBN, 1};
-        cudaError_t e = encode_tmap_bf16(&mk, khat, 3, dims, strides, box);
+        const uint32_t box[3] = {(uint32_t)C::A::kCols, kBN, 1};
+        cudaError_t e = encode_tmap_bf16(&mk, khat, 3, dims, strides, box, C::A::kSwizzleBytes);
         if (e != cudaSuccess) return e;
     }
     {
         const uint64_t dims[4] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)p.S, (uint64_t)p.B};
         const uint64_t strides[3] = {D * esz, (uint64_t)p.G * D * esz, (uint64_t)p.S * p.G * D * esz};
-        const uint32_t box[4] = {64, 1, kBN, 1};
-        cudaError_t e = encode_tmap_bf16(&mv, v, 4, dims, strides, box);
+        const uint32_t box[4] = {(uint32_t)C::A::kCols, 1, kBN, 1};
+        cudaError_t e = encode_tmap_bf16(&mv, v, 4, dims, strides, box, C::A::kSwizzleBytes);
         if (e != cudaSuccess) return e;
     }
     const int n_qtiles = (p.max_len + kBM - 1) / kBM;
@@ -379,6 +382,7 @@ cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, 
                           void *out, float *lse, unsigned int *err, cudaStream_t st) {
     if (p.D == 128) return launch_fwd_tc_d<128>(p, qhat, khat, v, out, lse, err, st);
     if (p.D == 64) return launch_fwd_tc_d<64>(p, qhat, khat, v, out, lse, err, st);
+    if (p.D == 32) return launch_fwd_tc_d<32>(p, qhat, khat, v, out, lse, err, st);
     return cudaErrorInvalidValue;
 }
 

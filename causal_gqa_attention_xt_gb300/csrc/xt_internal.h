@@ -94,8 +94,10 @@ cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const f
                                   const float *part_ml, void *out, float *lse, cudaStream_t st);
 
 // ---- TMA tensor maps (xt_tmap.cu) ----
+// swizzle_bytes: 128 or 64 (the smem row width of the box, see tc::Atoms).
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                             const uint64_t *strides_bytes, const uint32_t *box);
+                             const uint64_t *strides_bytes, const uint32_t *box,
+                             int swizzle_bytes);
 
 // ---- bf16 tcgen05 kernels ----
 cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,

@@ -382,6 +382,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
 // byte offset >> 4 in [32,46), descriptor version 1 at bit 46, base offset 0,
 // swizzle mode in [61,64) (2 = 128-byte swizzle).
 constexpr uint64_t kSwizzle128B = 2;
+constexpr uint64_t kSwizzle64B = 4;
+
+// Shared-memory layout of a bf16 operand tile whose rows hold D elements, as
+// TMA writes it: 128-byte swizzle atoms of 64 columns for D >= 64, 64-byte
+// atoms of 32 columns for D = 32; a tile of R rows is D / kCols boxes of
+// R x kCols, one after another.
+template <int D> struct Atoms {
+    static constexpr int kCols = D >= 64 ? 64 : 32;
+    static constexpr int kRowBytes = 2 * kCols;
+    static constexpr int kPerRow = D / kCols;
+    static constexpr uint64_t kMode = D >= 64 ? kSwizzle128B : kSwizzle64B;
+    static constexpr uint32_t kSBO = 8 * kRowBytes;            // 8-row groups
+    static constexpr int kSwizzleBytes = kRowBytes;            // for the tensor map
+    __host__ __device__ static constexpr int box_bytes(int rows) { return rows * kRowBytes; }
+    // K-major operand of `rows` rows: byte offset of k-step kk (16 columns)
+    __host__ __device__ static constexpr uint32_t kstep(int kk, int rows) {
+        return (uint32_t)((kk / (kCols / 16)) * rows * kRowBytes + (kk % (kCols / 16)) * 32);
+    }
+    // MN-major operand (its rows run along K): byte offset of k-step kk (16 rows)
+    __host__ __device__ static constexpr uint32_t mnstep(int kk) {
+        return (uint32_t)(kk * 16 * kRowBytes);
+    }
+};
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint64_t swizzle) {

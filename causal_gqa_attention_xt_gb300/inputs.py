@@ -68,6 +68,8 @@ WORKLOADS = {
     "dim768_gqa_bf16": Workload("dim768_gqa_bf16", 32, 1024, 12, 4, 64, 1e4, 1e-5, "bf16"),
     "qwen3_like_bf16": Workload("qwen3_like_bf16", 4, 4096, 32, 8, 128, 1e6, 1e-6, "bf16"),
     "mqa_long_bf16": Workload("mqa_long_bf16", 1, 16384, 16, 1, 128, 1e6, 1e-6, "bf16"),
+    # the pages' own dim768 run: 24 heads x head_dim 32 at seq 256, per-rank batch 32
+    "dim768_hd32_bf16": Workload("dim768_hd32_bf16", 32, 256, 24, 24, 32, 1e4, 1e-5, "bf16"),
     # decode: 32 sequences, each the next token against a full 4096-row cache
     "qwen3_like_decode_bf16": Workload("qwen3_like_decode_bf16", 32, 4096, 32, 8, 128, 1e6, 1e-6,
                                        "bf16"),

@@ -43,7 +43,7 @@
  * identical inputs give bitwise identical outputs.
  *
  * Supported shapes: B, S, H, G >= 1, H % G == 0, H + G <= 8192; dtype
- * XT_BF16 with head_dim 64 or 128 (tensor-core path), dtype XT_F32 with
+ * XT_BF16 with head_dim 32, 64 or 128 (tensor-core path), dtype XT_F32 with
  * head_dim a multiple of 8 up to 128 and B * H <= 65535 (fp32 CUDA-core
  * path). Every tensor must hold fewer than 2^31 elements.
  *

@@ -59,7 +59,7 @@ def _fwd(L, B=1, S=16, H=2, G=2, D=16, eps=1e-5, theta=1e4, dtype=0, ptr=16):
     (dict(theta=0.0), xt.XT_EINVAL), (dict(eps=float("nan")), xt.XT_EINVAL),
     (dict(ptr=0), xt.XT_EINVAL), (dict(ptr=8), xt.XT_EINVAL),
     (dict(B=1 << 16, S=1 << 16, H=1, G=1, D=16), xt.XT_EINVAL),
-    (dict(D=32, dtype=1), xt.XT_EUNSUPPORTED), (dict(D=136), xt.XT_EUNSUPPORTED),
+    (dict(D=48, dtype=1), xt.XT_EUNSUPPORTED), (dict(D=136), xt.XT_EUNSUPPORTED),
     (dict(D=12), xt.XT_EUNSUPPORTED),
 ])
 def test_forward_validation_rejects_before_launch(L, kw, code):
@@ -106,7 +106,7 @@ def test_decode_validation_and_workspace(L):
     need = xt.xt_attn_decode_workspace_bytes(2, 64, 4, 2, 16, 0)
     assert need > 0 and need % 256 == 0
     assert xt.xt_attn_decode_workspace_bytes(2, 64, 3, 2, 16, 0) == 0
-    assert xt.xt_attn_decode_workspace_bytes(2, 64, 4, 2, 32, 1) == 0   # bf16 wants D 64 / 128
+    assert xt.xt_attn_decode_workspace_bytes(2, 64, 4, 2, 48, 1) == 0   # bf16 wants D 32 / 64 / 128
     args = [2, 64, 4, 2, 16, 1e-5, 1e4]
     tail = [p] * 5 + [0] + [p] * 4
     assert L.xt_attn_decode(*args, p, *tail, p, need - 1, None) == xt.XT_EWORKSPACE
@@ -134,7 +134,7 @@ def _fwd_varlen(L, total=64, nseq=3, max_seqlen=32, H=4, G=2, D=64, dtype=1, cu=
     (dict(nseq=0), xt.XT_EINVAL), (dict(max_seqlen=0), xt.XT_EINVAL),
     (dict(max_seqlen=65), xt.XT_EINVAL), (dict(cu=0), xt.XT_EINVAL), (dict(cu=18), xt.XT_EINVAL),
     (dict(total=0), xt.XT_EINVAL), (dict(H=3), xt.XT_EINVAL), (dict(ptr=8), xt.XT_EINVAL),
-    (dict(D=32), xt.XT_EUNSUPPORTED),
+    (dict(D=48), xt.XT_EUNSUPPORTED),
     (dict(nseq=20000, D=16, dtype=0), xt.XT_EUNSUPPORTED),   # fp32 grid limit: nseq * H
 ])
 def test_varlen_validation_rejects_before_launch(L, kw, code):

@@ -33,9 +33,11 @@ def _gpu():
 CASES = [
     (Workload("dec_gqa_bf16", 3, 300, 8, 2, 64, 1e4, 1e-5, "bf16"), [0, 150, 299]),
     (Workload("dec_d128_bf16", 2, 1000, 32, 8, 128, 1e6, 1e-6, "bf16"), [999, 517]),
-    # a group of 40 query heads: three head chunks per kv head
+    # a group of 40 query heads: ten head chunks per kv head
     (Workload("dec_mqa_group40_bf16", 1, 5000, 40, 1, 128, 1e6, 1e-6, "bf16"), [4321]),
     (Workload("dec_f32", 2, 77, 4, 4, 32, 1e4, 1e-5, "f32"), [76, 5]),
+    # head_dim 32 in bf16 (half of each lane group's 16-byte chunks lie past the row)
+    (Workload("dec_d32_bf16", 2, 400, 6, 2, 32, 1e4, 1e-5, "bf16"), [399, 17]),
 ]
 
 

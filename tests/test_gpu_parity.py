@@ -76,6 +76,11 @@ SMALL = [
     Workload("chunks_h20_g5_bf16", 1, 150, 20, 5, 64, 1e4, 1e-5, "bf16"),
     Workload("chunks_h48_g16_d128_bf16", 1, 140, 48, 16, 128, 1e6, 1e-6, "bf16"),
     Workload("chunks_h12_g4_f32", 1, 70, 12, 4, 64, 1e4, 1e-5, "f32"),
+    # head_dim 32 on the tensor cores (64-byte swizzled tiles)
+    Workload("d32_group3_ragged_bf16", 2, 200, 6, 2, 32, 1e4, 1e-5, "bf16"),
+    Workload("d32_mqa_bf16", 1, 520, 8, 1, 32, 1e6, 1e-6, "bf16"),
+    Workload("d32_one_tile_bf16", 3, 128, 4, 4, 32, 1e4, 1e-5, "bf16"),
+    WORKLOADS["dim768_hd32_bf16"],
 ]
 
 

@@ -48,6 +48,7 @@ CASES = [
     PackedWorkload("varlen_mha_d128_bf16", (300, 17, 129), 4, 4, 128, 1e6, 1e-6, "bf16"),
     PackedWorkload("varlen_mqa_d128_bf16", (520, 200, 128), 16, 1, 128, 1e6, 1e-6, "bf16"),
     PackedWorkload("varlen_group2_d32_f32", (33, 1, 70), 4, 2, 32, 1e4, 1e-5, "f32"),
+    PackedWorkload("varlen_group2_d32_bf16", (33, 1, 300, 130), 4, 2, 32, 1e4, 1e-5, "bf16"),
     PackedWorkload("varlen_d128_f32", (140, 0, 65), 2, 1, 128, 1e6, 1e-6, "f32"),
 ]
 
