@@ -43,7 +43,7 @@ const char *kKernelNames[KID_COUNT] = {
     "prologue_qknorm_rope", "fwd_simt_f32", "fwd_tcgen05_bf16", "bwd_pre_dlt",
     "bwd_dq_simt_f32",      "bwd_dkdv_simt_f32", "bwd_dq_tcgen05_bf16",
     "bwd_dkdv_tcgen05_bf16", "bwd_epilogue_rope_norm", "bwd_dgamma_reduce",
-    "rope_table", "decode_rows", "decode_attn", "decode_combine"};
+    "rope_table", "decode_rows", "decode_attn", "decode_combine", "bwd_dkdv_reduce"};
 
 void drain_locked() {
     for (auto &p : g_timing.pending) {
@@ -119,7 +119,7 @@ size_t fwd_workspace(const Problem &p) { return align_up(rope_table_bytes(p)); }
 // Backward scratch: the RoPE cos/sin table, Dlt, fp32 dQhat and dKhat, and the
 // epilogue's per-CTA dgamma partials (at most kMaxNormParts rows each).
 struct BwdWorkspace {
-    size_t off_tab, off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, total;
+    size_t off_tab, off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, off_dkdv, total;
 };
 
 BwdWorkspace bwd_layout(const Problem &p) {
@@ -131,6 +131,7 @@ BwdWorkspace bwd_layout(const Problem &p) {
     w.off_dkhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.G * p.S * p.D);
     w.off_part_q = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
     w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
+    w.off_dkdv = o;   o = align_up(o + (p.dtype == XT_BF16 ? dkdv_part_bytes(p) : 0));
     w.total = o;
     return w;
 }
@@ -234,10 +235,18 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
     });
     if (st != XT_OK) return st;
     if (p.dtype == XT_BF16) {
+        float *part_dkdv = (float *)(ws + w.off_dkdv);
         st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
-            return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, err, s);
+            return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, part_dkdv,
+                                      err, s);
         });
         if (st != XT_OK) return st;
+        if (dkdv_part_bytes(p) > 0) {
+            st = timed_launch(KID_DKDV_REDUCE, s, [&] {
+                return launch_dkdv_reduce(p, part_dkdv, dkhat, dv, s);
+            });
+            if (st != XT_OK) return st;
+        }
         st = timed_launch(KID_BWD_DQ_TC, s, [&] {
             return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, err, s);
         });

@@ -50,6 +50,8 @@
 // its warp's quarter); 16 TMA producer; 17 TMEM allocator + MMA issuer.
 #include <type_traits>
 
+#include <algorithm>
+
 #include "xt_common.cuh"
 #include "xt_internal.h"
 #include "xt_tc.cuh"
@@ -141,13 +143,23 @@ template <int D> constexpr uint64_t mnmajor_off(int kk) { return (uint64_t)Atoms
 // ---------------------------------------------------------------------------
 // dKhat, dV
 // ---------------------------------------------------------------------------
+// Work split. Key tile j of a (unit, kv head) has group * (n_q - j) (head,
+// query tile) iterations; when that is more than `chunk` (chunk > 0), the
+// iterations are cut into chunks of `chunk`, one CTA each, whose fp32 dKhat/dV
+// partials go to `part` and are summed in chunk order by k_dkdv_reduce (so the
+// group sum stays in a fixed order). Work items of a (unit, kv head) are
+// numbered key tile by key tile, chunks in order: nw of them.
+__host__ __device__ inline int dkdv_chunks(int iters, int chunk) {
+    return (chunk > 0 && iters > chunk) ? (iters + chunk - 1) / chunk : 1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
               const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
               const float *__restrict__ lse, const float *__restrict__ dlt,
-              float *__restrict__ dkhat, bf16 *__restrict__ dv, const SeqRows sr, int H, int G,
-              int n_kvt, unsigned int *err) {
+              float *__restrict__ dkhat, bf16 *__restrict__ dv, float *__restrict__ part,
+              const SeqRows sr, int H, int G, int n_kvt, int chunk, int nw, unsigned int *err) {
     using C = BwdCfg<D>;
     constexpr int HS = C::kHStages;
     extern __shared__ uint8_t smem_raw[];
@@ -158,16 +170,24 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     uint8_t *sStage = smem + 2 * C::kTileBytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BG = gridDim.x / n_kvt;
-    const int j = (int)(blockIdx.x / BG);          // key tile, longest first
+    const int BG = gridDim.x / nw;
+    const int witem = (int)(blockIdx.x / BG);      // work item, longest first
     const int bg = blockIdx.x % BG;
     const int unit = bg / G, g = bg - unit * G, group = H / G;
+    int j = 0, cidx = witem, nc = 1;               // key tile, chunk of it, its chunk count
+    for (;;) {
+        nc = dkdv_chunks(group * (n_kvt - j), chunk);
+        if (cidx < nc || j + 1 >= n_kvt) break;
+        cidx -= nc;
+        ++j;
+    }
     const SeqSpan sp = seq_span(sr, unit);
     const int S = sp.len;                           // rows of this unit
     const int n_q = (S + kTile - 1) / kTile;
-    if (j >= n_q) return;                           // a packed sample shorter than this tile
+    if (j >= n_q || cidx >= nc) return;             // a packed sample shorter than this tile
     const int nU = n_q - j;                         // query tiles at/after the keys, per head
-    const int T = group * nU;
+    const int t0 = nc > 1 ? cidx * chunk : 0;       // this CTA's iterations [t0, t0 + T)
+    const int T = nc > 1 ? min(chunk, group * nU - t0) : group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, HS, true);
@@ -197,7 +217,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         // half tile x = 2 t + hf: rows [64 hf, 64 hf + 64) of streamed tile t
         int issued = 0;
         for (int x = 0; x < 2 * T; ++x) {
-            const int hs = x % HS, t = x >> 1, hf = x & 1;
+            const int hs = x % HS, t = t0 + (x >> 1), hf = x & 1;
             bool ok = true;
             if (x >= HS && lane == 0)
                 ok = mbar_wait(&bars.st_empty[hs], ((x / HS) - 1) & 1, abort_flag);
@@ -319,7 +339,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                                              mbar_wait(&bars.st_full[hs], (x / HS) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const int u = j + (t % nU);
+            const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
             // statistics of the half: lse at [0,64), Dlt at [64,128)
@@ -381,13 +401,26 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 const float scale = rsqrtf((float)D);
                 bf16 *dvrow = dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D;
                 float *dkrow = dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D;
+                // a chunk of a split key tile: fp32 partials [dV | dKhat][row][D]
+                float *prow = nc > 1 ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D
+                                     : nullptr;
 #pragma unroll
                 for (int cc = wg; cc < 2 * (D / 32); cc += kSoftmaxWGs) {
                     const bool isv = cc < D / 32;
                     const int c = isv ? cc : cc - D / 32;
                     uint32_t a[32];
                     tmem_ld32_sync(tmem + (isv ? 256 : 384) + lane_off + 32 * c, a);
-                    if (kp < S) {
+                    if (kp < S && prow != nullptr) {
+                        const float sc = isv ? 1.f : scale;
+                        float *dst = prow + (isv ? 0 : (size_t)kTile * D) + 32 * c;
+#pragma unroll
+                        for (int q4 = 0; q4 < 8; ++q4)
+                            *reinterpret_cast<float4 *>(dst + 4 * q4) =
+                                make_float4(__uint_as_float(a[q4 * 4 + 0]) * sc,
+                                            __uint_as_float(a[q4 * 4 + 1]) * sc,
+                                            __uint_as_float(a[q4 * 4 + 2]) * sc,
+                                            __uint_as_float(a[q4 * 4 + 3]) * sc);
+                    } else if (kp < S) {
                         if (isv) {
 #pragma unroll
                             for (int q8 = 0; q8 < 4; ++q8) {
@@ -420,6 +453,34 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     if (warp == kWarpMma) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// Sums the chunk partials of the split key tiles in chunk order: block =
+// (split key tile j, unit x kv head), threads over the tile's rows x D.
+__global__ void __launch_bounds__(256)
+k_dkdv_reduce(const float *__restrict__ part, float *__restrict__ dkhat, bf16 *__restrict__ dv,
+              const SeqRows sr, int H, int G, int D, int n_kvt, int chunk, int nw) {
+    const int j = blockIdx.x, bg = blockIdx.y;
+    const int unit = bg / G, g = bg - unit * G, group = H / G;
+    int w0 = 0;
+    for (int i = 0; i < j; ++i) w0 += dkdv_chunks(group * (n_kvt - i), chunk);
+    const int nc = dkdv_chunks(group * (n_kvt - j), chunk);
+    if (nc <= 1) return;
+    const SeqSpan sp = seq_span(sr, unit);
+    const size_t stride = (size_t)2 * kTile * D;   // one chunk's [dV | dKhat]
+    const float *base = part + ((size_t)bg * nw + w0) * stride;
+    for (int e = threadIdx.x; e < kTile * D; e += blockDim.x) {
+        const int r = e / D, d = e - r * D;
+        const int kp = j * kTile + r;
+        if (kp >= sp.len) break;
+        float sv = 0.f, sk = 0.f;
+        for (int c = 0; c < nc; ++c) {
+            sv += base[c * stride + e];
+            sk += base[c * stride + (size_t)kTile * D + e];
+        }
+        dv[(((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D + d] = __float2bfloat16_rn(sv);
+        dkhat[(((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D + d] = sk;
     }
 }
 
@@ -706,18 +767,59 @@ cudaError_t make_maps(const Problem &p, const void *qhat, const void *khat, cons
     return cudaSuccess;
 }
 
+// Chunk size of the dK/dV work split (0: no split). When the longest key
+// tile's iterations exceed half of an SM's share of the whole work (few kv
+// heads with long sequences and large groups, e.g. MQA: the makespan is then
+// set by single CTAs), key tiles are cut into chunks of a quarter of that
+// share; otherwise nothing is split (its partials and reduce would only cost).
+// Plain batches only (a packed batch's sample lengths are on the device).
+struct DkdvPlan {
+    int n_kvt, chunk, nw, n_split;   // key tiles, chunk, work items per (unit, kv head), split tiles
+    size_t part_bytes;
+};
+
+DkdvPlan dkdv_plan(const Problem &p) {
+    DkdvPlan pl = {};
+    pl.n_kvt = (p.max_len + kTile - 1) / kTile;
+    const int group = p.H / p.G;
+    const long bgs = (long)p.units * p.G;
+    if (p.cu == nullptr) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1)
+            sms = 148;
+        long total = 0;
+        for (int j = 0; j < pl.n_kvt; ++j) total += (long)group * (pl.n_kvt - j);
+        total *= bgs;
+        const long share = total / sms;
+        const long target = (total + 4L * sms - 1) / (4L * sms);
+        if (2L * group * pl.n_kvt > share && target < (1L << 30))
+            pl.chunk = (int)std::max<long>(8, target);
+    }
+    pl.nw = 0;
+    for (int j = 0; j < pl.n_kvt; ++j) {
+        const int nc = dkdv_chunks(group * (pl.n_kvt - j), pl.chunk);
+        pl.nw += nc;
+        if (nc > 1) pl.n_split = j + 1;
+    }
+    pl.part_bytes = pl.n_split > 0
+        ? (size_t)bgs * pl.nw * 2 * kTile * p.D * sizeof(float) : 0;
+    return pl;
+}
+
 template <int D>
 cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, const float *dlt,
-                          float *dkhat, void *dv, unsigned int *err, cudaStream_t st) {
+                          float *dkhat, void *dv, float *part, unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
-    const int n_kvt = (p.max_len + kTile - 1) / kTile;
-    const long blocks = (long)p.units * p.G * n_kvt;
+    const DkdvPlan pl = dkdv_plan(p);
+    const long blocks = (long)p.units * p.G * pl.nw;
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemA);
     if (e != cudaSuccess) return e;
     k_bwd_dkdv_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
-        m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, SeqRows{p.cu, p.S, p.max_len}, p.H,
-        p.G, n_kvt, err);
+        m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, part, SeqRows{p.cu, p.S, p.max_len},
+        p.H, p.G, pl.n_kvt, pl.chunk, pl.nw, err);
     return cudaGetLastError();
 }
 
@@ -740,11 +842,11 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
 template <int D>
 cudaError_t run_dkdv(const Problem &p, const void *qhat, const void *khat, const void *v,
                      const void *dout, const float *lse, const float *dlt, float *dkhat, void *dv,
-                     unsigned int *err, cudaStream_t st) {
+                     float *part, unsigned int *err, cudaStream_t st) {
     BwdMaps m;
     cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
     if (e != cudaSuccess) return e;
-    return launch_dkdv_d<D>(p, m, lse, dlt, dkhat, dv, err, st);
+    return launch_dkdv_d<D>(p, m, lse, dlt, dkhat, dv, part, err, st);
 }
 
 template <int D>
@@ -759,14 +861,26 @@ cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const v
 
 }  // namespace
 
+size_t dkdv_part_bytes(const Problem &p) { return dkdv_plan(p).part_bytes; }
+
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
-                               const float *dlt, float *dkhat, void *dv, unsigned int *err,
-                               cudaStream_t st) {
-    if (p.D == 128) return run_dkdv<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
-    if (p.D == 64) return run_dkdv<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
-    if (p.D == 32) return run_dkdv<32>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, err, st);
+                               const float *dlt, float *dkhat, void *dv, float *part,
+                               unsigned int *err, cudaStream_t st) {
+    if (p.D == 128) return run_dkdv<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
+    if (p.D == 64) return run_dkdv<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
+    if (p.D == 32) return run_dkdv<32>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat, void *dv,
+                               cudaStream_t st) {
+    const DkdvPlan pl = dkdv_plan(p);
+    if (pl.n_split == 0) return cudaSuccess;
+    dim3 grid((unsigned)pl.n_split, (unsigned)((long)p.units * p.G));
+    k_dkdv_reduce<<<grid, 256, 0, st>>>(part, dkhat, (bf16 *)dv, SeqRows{p.cu, p.S, p.max_len},
+                                         p.H, p.G, p.D, pl.n_kvt, pl.chunk, pl.nw);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,

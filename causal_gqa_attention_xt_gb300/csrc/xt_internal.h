@@ -26,6 +26,7 @@ enum KernelId {
     KID_DECODE_ROWS,      // decode: the new token's rows normed, rotated, cached
     KID_DECODE_ATTN,      // decode: split attention over the cache
     KID_DECODE_COMBINE,   // decode: fixed-order merge of the splits
+    KID_DKDV_REDUCE,      // fixed-order sum of split dK/dV tiles' chunk partials
     KID_COUNT
 };
 
@@ -102,9 +103,15 @@ cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const
 // ---- bf16 tcgen05 kernels ----
 cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                           void *out, float *lse, unsigned int *err, cudaStream_t st);
+// part: fp32 scratch of dkdv_part_bytes(p) for the chunk partials of key
+// tiles whose work is split over several CTAs (none when that is 0);
+// launch_dkdv_reduce then sums them in chunk order into dkhat and dv.
+size_t dkdv_part_bytes(const Problem &p);
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
-                               const float *dlt, float *dkhat, void *dv, unsigned int *err,
+                               const float *dlt, float *dkhat, void *dv, float *part,
+                               unsigned int *err, cudaStream_t st);
+cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat, void *dv,
                                cudaStream_t st);
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                              const void *dout, const float *lse, const float *dlt, float *dqhat,

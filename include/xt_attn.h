@@ -78,7 +78,11 @@ typedef enum {
  * call needs for this problem; 0 on invalid arguments. The forward's scratch
  * is the RoPE table, S * head_dim/2 (cos, sin) fp32 pairs (rounded up to 256
  * bytes); the backward's holds that table too, plus Dlt [B, H, S], fp32 dQhat
- * and dKhat, and 2 * 1024 * head_dim floats of dgamma partials. */
+ * and dKhat, 2 * 1024 * head_dim floats of dgamma partials and, for bf16
+ * problems whose key/value heads carry far more work than there are blocks
+ * to share it (few kv heads and long sequences, e.g. MQA), fp32 partials of
+ * the dK/dV tiles whose work is split over several thread blocks. The size
+ * depends on the current device's SM count. */
 size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                                int dtype, int backward);
 

@@ -81,6 +81,10 @@ SMALL = [
     Workload("d32_mqa_bf16", 1, 520, 8, 1, 32, 1e6, 1e-6, "bf16"),
     Workload("d32_one_tile_bf16", 3, 128, 4, 4, 32, 1e4, 1e-5, "bf16"),
     WORKLOADS["dim768_hd32_bf16"],
+    # one kv head for many query heads: the dK/dV work of a key tile is split over
+    # several CTAs and their partials summed in a fixed order
+    Workload("split_mqa_d128_bf16", 1, 2048, 16, 1, 128, 1e6, 1e-6, "bf16"),
+    Workload("split_mqa_ragged_d64_bf16", 1, 1000, 8, 1, 64, 1e4, 1e-5, "bf16"),
 ]
 
 
