@@ -153,7 +153,9 @@ __host__ __device__ inline int dkdv_chunks(int iters, int chunk) {
     return (chunk > 0 && iters > chunk) ? (iters + chunk - 1) / chunk : 1;
 }
 
-template <int D>
+// kSplit: the chunked work split is on (a separate instantiation keeps the
+// unsplit kernel free of its index arithmetic).
+template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
               const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
@@ -174,20 +176,24 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const int witem = (int)(blockIdx.x / BG);      // work item, longest first
     const int bg = blockIdx.x % BG;
     const int unit = bg / G, g = bg - unit * G, group = H / G;
-    int j = 0, cidx = witem, nc = 1;               // key tile, chunk of it, its chunk count
-    for (;;) {
-        nc = dkdv_chunks(group * (n_kvt - j), chunk);
-        if (cidx < nc || j + 1 >= n_kvt) break;
-        cidx -= nc;
-        ++j;
+    int j = witem, cidx = 0, nc = 1;               // key tile, chunk of it, its chunk count
+    if constexpr (kSplit) {
+        j = 0;
+        cidx = witem;
+        for (;;) {
+            nc = dkdv_chunks(group * (n_kvt - j), chunk);
+            if (cidx < nc || j + 1 >= n_kvt) break;
+            cidx -= nc;
+            ++j;
+        }
     }
     const SeqSpan sp = seq_span(sr, unit);
     const int S = sp.len;                           // rows of this unit
     const int n_q = (S + kTile - 1) / kTile;
     if (j >= n_q || cidx >= nc) return;             // a packed sample shorter than this tile
     const int nU = n_q - j;                         // query tiles at/after the keys, per head
-    const int t0 = nc > 1 ? cidx * chunk : 0;       // this CTA's iterations [t0, t0 + T)
-    const int T = nc > 1 ? min(chunk, group * nU - t0) : group * nU;
+    const int t0 = kSplit && nc > 1 ? cidx * chunk : 0;   // this CTA's iterations [t0, t0 + T)
+    const int T = kSplit && nc > 1 ? min(chunk, group * nU - t0) : group * nU;
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, HS, true);
@@ -402,8 +408,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 bf16 *dvrow = dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D;
                 float *dkrow = dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D;
                 // a chunk of a split key tile: fp32 partials [dV | dKhat][row][D]
-                float *prow = nc > 1 ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D
-                                     : nullptr;
+                float *prow = kSplit && nc > 1
+                    ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D : nullptr;
 #pragma unroll
                 for (int cc = wg; cc < 2 * (D / 32); cc += kSoftmaxWGs) {
                     const bool isv = cc < D / 32;
@@ -814,10 +820,11 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
     using C = BwdCfg<D>;
     const DkdvPlan pl = dkdv_plan(p);
     const long blocks = (long)p.units * p.G * pl.nw;
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dkdv_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = pl.n_split > 0 ? k_bwd_dkdv_tc<D, true> : k_bwd_dkdv_tc<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemA);
     if (e != cudaSuccess) return e;
-    k_bwd_dkdv_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
+    kern<<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
         m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, part, SeqRows{p.cu, p.S, p.max_len},
         p.H, p.G, pl.n_kvt, pl.chunk, pl.nw, err);
     return cudaGetLastError();
