@@ -276,7 +276,8 @@ def bench_ours(args, w):
                                          dd["cu_seqlens"], w.max_len, saved_, dd["dout"], w.eps,
                                          w.theta, **kw)
 
-        ws_bytes = xt.xt_attn_varlen_workspace_bytes(w.T, w.max_len, w.H, w.G, w.D, code, True)
+        ws_bytes = xt.xt_attn_varlen_workspace_bytes(w.T, len(w.lens), w.max_len, w.H, w.G, w.D, code,
+                                                     True)
     else:
         wr = w.with_(seed=shard_seed(w.seed, rank))
         cpu = make_inputs(wr)

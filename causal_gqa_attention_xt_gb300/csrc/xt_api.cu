@@ -116,8 +116,10 @@ size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 // Forward scratch: the RoPE cos/sin table.
 size_t fwd_workspace(const Problem &p) { return align_up(rope_table_bytes(p)); }
 
-// Backward scratch: the RoPE cos/sin table, Dlt, fp32 dQhat and dKhat, and the
-// epilogue's per-CTA dgamma partials (at most kMaxNormParts rows each).
+// Backward scratch: the RoPE cos/sin table, Dlt, fp32 dKhat (and dQhat for
+// fp32 problems), the dgamma partials (the epilogue's, at most kMaxNormParts
+// rows; for bf16 the q rows' come from the dQ kernel, one row per CTA) and
+// the split dK/dV partials.
 struct BwdWorkspace {
     size_t off_tab, off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, off_dkdv, total;
 };
@@ -127,9 +129,13 @@ BwdWorkspace bwd_layout(const Problem &p) {
     size_t o = 0;
     w.off_tab = o;    o = align_up(o + rope_table_bytes(p));
     w.off_dlt = o;    o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S);
-    w.off_dqhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S * p.D);
+    // bf16: the dQ kernel finishes dq itself (no fp32 dQhat), one dgamma_q
+    // partial per CTA of it
+    const bool tc = p.dtype == XT_BF16;
+    w.off_dqhat = o;  o = align_up(o + (tc ? 0 : sizeof(float) * (size_t)p.B * p.H * p.S * p.D));
     w.off_dkhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.G * p.S * p.D);
-    w.off_part_q = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
+    w.off_part_q = o;
+    o = align_up(o + sizeof(float) * (tc ? dq_part_count(p) : (size_t)kMaxNormParts) * p.D);
     w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
     w.off_dkdv = o;   o = align_up(o + (p.dtype == XT_BF16 ? dkdv_part_bytes(p) : 0));
     w.total = o;
@@ -247,8 +253,9 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
             });
             if (st != XT_OK) return st;
         }
+        const DqEpilogue ep = {q, gamma_q, rstd_q, tab, dq, part_q};
         st = timed_launch(KID_BWD_DQ_TC, s, [&] {
-            return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, dqhat, err, s);
+            return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, ep, err, s);
         });
         if (st != XT_OK) return st;
     } else {
@@ -262,13 +269,15 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
         if (st != XT_OK) return st;
     }
     int nparts = 0;
+    const bool tc = p.dtype == XT_BF16;
     st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
-        return launch_epilogue(p, dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q, rstd_k, tab, dq,
-                               dk, part_q, part_k, &nparts, err, s);
+        return launch_epilogue(p, tc ? nullptr : dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q,
+                               rstd_k, tab, dq, dk, part_q, part_k, &nparts, err, s);
     });
     if (st != XT_OK) return st;
+    const int nparts_q = tc ? (int)dq_part_count(p) : nparts;
     return timed_launch(KID_DGAMMA_REDUCE, s, [&] {
-        return launch_dgamma_reduce(p, part_q, part_k, nparts, nparts, dgamma_q, dgamma_k, s);
+        return launch_dgamma_reduce(p, part_q, part_k, nparts_q, nparts, dgamma_q, dgamma_k, s);
     });
 }
 
@@ -314,11 +323,13 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim, double 
                    dq, dk, dv, dgamma_q, dgamma_k, workspace, workspace_bytes, stream);
 }
 
-size_t xt_attn_varlen_workspace_bytes(int total, int max_seqlen, int n_heads, int n_kv_heads,
-                                      int head_dim, int dtype, int backward) {
+size_t xt_attn_varlen_workspace_bytes(int total, int nseq, int max_seqlen, int n_heads,
+                                      int n_kv_heads, int head_dim, int dtype, int backward) {
     if (validate_shape(1, total, n_heads, n_kv_heads, head_dim, dtype) != XT_OK) return 0;
-    if (max_seqlen <= 0 || max_seqlen > total) return 0;
-    const Problem p = make_problem(1, total, n_heads, n_kv_heads, head_dim, 0.0, 1.0, dtype);
+    if (nseq <= 0 || max_seqlen <= 0 || max_seqlen > total) return 0;
+    // the sizes depend on the offsets only through nseq and max_seqlen
+    const Problem p = make_packed_problem(total, nseq, max_seqlen, nullptr, n_heads, n_kv_heads,
+                                          head_dim, 0.0, 1.0, dtype);
     return backward ? bwd_layout(p).total : fwd_workspace(p);
 }
 

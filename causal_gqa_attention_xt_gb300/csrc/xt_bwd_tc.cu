@@ -14,7 +14,10 @@
 //    query tiles at or after its keys, accumulating dV += P^T dO and
 //    dKhat += dS^T Qhat in TMEM: the group sum happens inside the CTA.
 //  * k_bwd_dq_tc: a CTA owns 128 query rows of one (batch, head) and walks
-//    the 128-row key tiles at or before them, accumulating dQhat += dS Khat.
+//    the 128-row key tiles at or before them, accumulating dQhat += dS Khat;
+//    its epilogue finishes dq (RoPE backward, then RMSNorm backward: Mint
+//    project report 5.4.4 and 5.5.2) and writes the CTA's dgamma_q partial,
+//    so dQhat never leaves TMEM.
 // Both recompute S from the saved Qhat, Khat and lse.
 //
 // TMEM: S (or S^T) in columns [0,128), dP (or dP^T) in [128,256), the
@@ -79,7 +82,12 @@ template <int D> struct BwdCfg {
     // dQ kernel: a stage holds a K and a V tile
     static constexpr int kStages = (D == 128) ? 2 : 4;
     static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-    static constexpr int kSmemB = kStages * kStageBytes + 1024;
+    // the dq epilogue's inputs: the owned rows of q (one tile, its own region)
+    // and their RoPE (cos, sin) rows, D/32 boxes of 128 rows x 128 bytes of the
+    // fp32 table, loaded into the stage after the last K/V tile
+    static constexpr int kCsBytes = (D / 32) * kTile * 128;
+    static_assert(kCsBytes <= kStageBytes, "cos/sin rows must fit one stage");
+    static constexpr int kSmemB = kStages * kStageBytes + kTileBytes + 1024;
     // dK/dV kernel: a ring of half tiles, each the Qhat and dO rows of one half
     // of a streamed query tile plus their 2 x 64 row statistics, so that a half
     // is reloaded as soon as its own MMAs are done
@@ -94,6 +102,7 @@ struct BwdBarriers {
     uint64_t s_full[2], p_full[2];   // per half of the streamed tile (columns [64h, 64h+64))
     uint64_t acc_done;
     uint64_t drain;
+    uint64_t x_full;                 // dQ kernel: the owned rows of q are in shared memory
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -121,6 +130,7 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     }
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.x_full, 1);
     fence_barrier_init();
 }
 
@@ -491,15 +501,55 @@ k_dkdv_reduce(const float *__restrict__ part, float *__restrict__ dkhat, bf16 *_
 }
 
 // ---------------------------------------------------------------------------
-// dQhat
+// dQhat and the dq epilogue
 // ---------------------------------------------------------------------------
+// Scratch of the dq epilogue: per-warpgroup parts of each row's norm dot
+// product, and per-(warpgroup, row quarter) column sums of the dgamma terms.
+struct EpiScratch {
+    float dot[kSoftmaxWGs][kTile];
+    float g[kSoftmaxWGs][4][32];
+    float rstd[kTile];               // rstd_q of the owned rows (0 past the end)
+    float gamma[kTile];              // gamma_q (D <= kTile)
+};
+
+// The 512 softmax threads (warps 0-15) only.
+__device__ __forceinline__ void softmax_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kSoftmaxWGs) : "memory");
+}
+
+// Element e of 32 bf16 packed two per word (the lower index in the low half).
+__device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[16], int e) {
+    const uint32_t v = w[e >> 1];
+    return __uint_as_float((e & 1) ? (v & 0xffff0000u) : (v << 16));
+}
+
+// Transposing butterfly: every lane holds 32 values v[c] (c = column); after
+// five exchange steps lane l holds the sum over the 32 lanes of column l (each
+// step a lane keeps half of its columns, sends the other half to the partner
+// lane and adds the partner's copy of the kept half). Fixed association.
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int n = 16; n >= 1; n >>= 1) {
+        const bool up = (lane & n) != 0;
+#pragma unroll
+        for (int e = 0; e < n; ++e) {
+            const float send = up ? v[e] : v[e + n];
+            const float keep = up ? v[e + n] : v[e];
+            v[e] = keep + __shfl_xor_sync(0xffffffffu, send, n);
+        }
+    }
+    return v[0];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+            const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
             const bf16 *__restrict__ qhat, const bf16 *__restrict__ dout,
             const float *__restrict__ lse, const float *__restrict__ dlt,
-            float *__restrict__ dqhat, const SeqRows sr, int H, int G, int n_qt,
-            unsigned int *err) {
+            const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
+            bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
+            int n_qt, unsigned int *err) {
     using C = BwdCfg<D>;
     constexpr int ST = C::kStages;
     // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), and the
@@ -507,8 +557,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     constexpr uint32_t kTQ = 384, kTDO = 448;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
+    __shared__ EpiScratch escr;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sStage = smem;
+    uint8_t *sX = smem + ST * C::kStageBytes;          // owned rows of q (swizzled boxes)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = gridDim.x / n_qt;
@@ -517,7 +569,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int unit = bh / H, h = bh - unit * H, g = h / (H / G);
     const SeqSpan sp = seq_span(sr, unit);
     const int S = sp.len;                              // rows of this unit
-    if (i * kTile >= S) return;                        // a packed sample shorter than this tile
+    float *part = part_q + ((size_t)bh * n_qt + i) * D;   // this CTA's dgamma_q partial
+    if (i * kTile >= S) {                              // a packed sample shorter than this tile
+        for (int d = threadIdx.x; d < D; d += blockDim.x) part[d] = 0.f;
+        return;
+    }
     const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;   // [.., H, S, ..] rows
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
@@ -540,25 +596,41 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         if (lane == 0) {
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
+            tma_prefetch_desc(&map_x);
+            tma_prefetch_desc(&map_cs);
+            const int row0 = sp.start + i * kTile;
+            mbar_expect_tx(&bars.x_full, C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_4d(sX + c * C::kBox, &map_x, &bars.x_full, c * C::A::kCols, h, row0,
+                            sp.plane);
+            // tiles 0..T-1: K and V; "tile" T: the owned rows' (cos, sin) rows
             int issued = 0;
-            for (int t = 0; t < T; ++t) {
+            for (int t = 0; t <= T; ++t) {
                 const int st = t % ST;
                 if (t >= ST && !mbar_wait(&bars.st_empty[st], ((t / ST) - 1) & 1, abort_flag)) {
                     if (!*abort_flag) raise_error_b(err, abort_flag);
                     break;
                 }
                 uint8_t *base = sStage + st * C::kStageBytes;
-                mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_3d(base + c * C::kBox, &map_k, &bars.st_full[st], c * C::A::kCols,
-                                sp.start + t * kTile, sp.plane * G + g);
-                    tma_load_4d(base + C::kTileBytes + c * C::kBox, &map_v, &bars.st_full[st],
-                                c * C::A::kCols, g, sp.start + t * kTile, sp.plane);
+                if (t == T) {
+                    mbar_expect_tx(&bars.st_full[st], C::kCsBytes);
+                    for (int c = 0; c < D / 32; ++c)
+                        tma_load_2d(base + c * kTile * 128, &map_cs, &bars.st_full[st], 32 * c,
+                                    row0);
+                } else {
+                    mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(base + c * C::kBox, &map_k, &bars.st_full[st],
+                                    c * C::A::kCols, sp.start + t * kTile, sp.plane * G + g);
+                        tma_load_4d(base + C::kTileBytes + c * C::kBox, &map_v, &bars.st_full[st],
+                                    c * C::A::kCols, g, sp.start + t * kTile, sp.plane);
+                    }
                 }
                 issued = t + 1;
             }
             for (int t = max(0, issued - ST); t < issued; ++t)
                 mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
+            mbar_wait(&bars.x_full, 0, nullptr);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -651,6 +723,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             else tmem_st16_sync(dst, xa);
             tc_fence_before();
             mbar_arrive(&bars.own_full);
+        } else if (wg == kSoftmaxWGs - 1) {
+            // for the dq epilogue (read after its first named barrier; the writes
+            // and reads are ordered by that barrier)
+            escr.rstd[r] = tq < S ? rstd_q[((size_t)sp.plane * sr.S + sp.start + tq) * H + h] : 0.f;
+            if (r < D) escr.gamma[r] = gamma_q[r];
         }
         bool ok = true;
         for (int t = 0; t < T; ++t) {
@@ -692,30 +769,116 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tc_fence_before();
             mbar_arrive(ds_ready);
         }
-        if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
-            if (ok) {
-                tc_fence_after();
-                const float scale = rsqrtf((float)D);
-                float *dst = dqhat + (qrow0 + tq) * D;
-                // warpgroup w writes the 32-column chunks w, w + kSoftmaxWGs, ... of the row
+        // ---- epilogue: dq = RMSNorm_bwd(RoPE_bwd(dQhat)) for the owned rows, and the
+        // CTA's dgamma_q partial. Warpgroup w < D/32 takes the 16 RoPE pairs
+        // [16w, 16w+16) (columns 16w.. and D/2+16w..) of its thread's row, reading
+        // the row's q and (cos, sin) values from shared memory (loaded by the
+        // producer); the row's norm dot product is summed over those warpgroups
+        // in order. Every softmax thread passes the three named barriers,
+        // whatever `ok` is.
+        using A = typename C::A;
+        constexpr int kHalf = D / 2, kEpiWGs = D / 32;
+        const bool in_epi = wg < kEpiWGs;
+        const int i0 = wg * 16;
+        const bool row_ok = tq < S;
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag) &&
+                                                 mbar_wait(&bars.x_full, 0, abort_flag) &&
+                                                 mbar_wait(&bars.st_full[T % ST], (T / ST) & 1,
+                                                           abort_flag));
+        // q of the row: 8 words of the low pairs' columns, then 8 of the high
+        softmax_bar_sync();   // the stashed gamma and rstd are visible from here on
+        uint32_t xw[16];
+        float dy[32];   // dy[e] (e < 16): column i0 + e; dy[16 + e]: column D/2 + i0 + e
 #pragma unroll
-                for (int c = wg; c < D / 32; c += kSoftmaxWGs) {
-                    uint32_t a[32];
-                    tmem_ld32_sync(tmem + 256 + lane_off + 32 * c, a);
-                    if (tq < S) {
+        for (int e = 0; e < 32; ++e) dy[e] = 0.f;
 #pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) {
-                            float4 f;
-                            f.x = __uint_as_float(a[q4 * 4 + 0]) * scale;
-                            f.y = __uint_as_float(a[q4 * 4 + 1]) * scale;
-                            f.z = __uint_as_float(a[q4 * 4 + 2]) * scale;
-                            f.w = __uint_as_float(a[q4 * 4 + 3]) * scale;
-                            *reinterpret_cast<float4 *>(dst + 32 * c + 4 * q4) = f;
-                        }
-                    }
+        for (int e = 0; e < 16; ++e) xw[e] = 0u;
+        if (ok && in_epi) {
+            tc_fence_after();
+#pragma unroll
+            for (int part8 = 0; part8 < 4; ++part8) {
+                // 8-column chunks: i0, i0+8 (low), D/2+i0, D/2+i0+8 (high)
+                const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
+                const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                                r * A::kRowBytes + (col % A::kCols) * 2);
+                const uint4 v = *reinterpret_cast<const uint4 *>(
+                    sX + swizzled<A::kRowBytes>(off));
+                xw[4 * part8] = v.x; xw[4 * part8 + 1] = v.y;
+                xw[4 * part8 + 2] = v.z; xw[4 * part8 + 3] = v.w;
+            }
+            uint32_t a[16], b[16];
+            tmem_ld16_pair_sync(tmem + 256 + lane_off + i0, a, tmem + 256 + lane_off + kHalf + i0, b);
+            const float scale = rsqrtf((float)D);
+            // (cos, sin) of pairs i0.. of the row: box wg of the cos/sin stage
+            const uint8_t *csb = sStage + (T % ST) * C::kStageBytes + wg * kTile * 128;
+            float dotp = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                const float4 c2 = *reinterpret_cast<const float4 *>(
+                    csb + swizzled<128>((uint32_t)(r * 128 + e * 8)));
+                const float cv[2] = {c2.x, c2.z}, sv[2] = {c2.y, c2.w};
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const float gl = __uint_as_float(a[e + x]) * scale;
+                    const float gh = __uint_as_float(b[e + x]) * scale;
+                    // rotation by the negative angle
+                    const float dyl = gl * cv[x] + gh * sv[x];
+                    const float dyh = gh * cv[x] - gl * sv[x];
+                    dy[e + x] = dyl;
+                    dy[16 + e + x] = dyh;
+                    dotp = fmaf(escr.gamma[i0 + e + x] * dyl, bf16_lo_or_hi(xw, e + x), dotp);
+                    dotp = fmaf(escr.gamma[kHalf + i0 + e + x] * dyh,
+                                bf16_lo_or_hi(xw, 16 + e + x), dotp);
                 }
             }
+            escr.dot[wg][r] = dotp;
+        }
+        softmax_bar_sync();
+        if (ok && in_epi) {
+            float dot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kEpiWGs; ++w) dot += escr.dot[w][r];
+            const float rr = escr.rstd[r];
+            const float corr = dot * rr * rr * rr * (1.0f / (float)D);
+            uint32_t ow[16];
+#pragma unroll
+            for (int e = 0; e < 16; e += 2) {
+                float ol[2], oh[2];
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const float xl = bf16_lo_or_hi(xw, e + x), xh = bf16_lo_or_hi(xw, 16 + e + x);
+                    ol[x] = escr.gamma[i0 + e + x] * dy[e + x] * rr - xl * corr;
+                    oh[x] = escr.gamma[kHalf + i0 + e + x] * dy[16 + e + x] * rr - xh * corr;
+                    // the dgamma terms replace dy
+                    dy[e + x] = dy[e + x] * xl * rr;
+                    dy[16 + e + x] = dy[16 + e + x] * xh * rr;
+                }
+                ow[e / 2] = pack_bf16x2(ol[0], ol[1]);
+                ow[8 + e / 2] = pack_bf16x2(oh[0], oh[1]);
+            }
+            if (row_ok) {
+                uint4 *dst = reinterpret_cast<uint4 *>(
+                    dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D);
+                dst[i0 / 8] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                dst[i0 / 8 + 1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+                dst[(kHalf + i0) / 8] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
+                dst[(kHalf + i0) / 8 + 1] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
+            }
+            // column sums over the warp's 32 rows: lane l ends with column l of dy
+            escr.g[wg][quarter][lane] = transpose_sum32(dy, lane);
+        }
+        softmax_bar_sync();
+        if (threadIdx.x < D) {
+            // column d of the partial: the four row quarters of its warpgroup, in order
+            const int d = threadIdx.x;
+            const int w = (d < kHalf ? d : d - kHalf) / 16;
+            const int l = (d < kHalf ? 0 : 16) + (d & 15);
+            float sum = 0.f;
+            if (ok) {
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) sum += escr.g[w][qq][l];
+            }
+            part[d] = sum;
         }
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
     }
@@ -830,19 +993,50 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
     return cudaGetLastError();
 }
 
+// The dq epilogue's inputs: q [B, S, H, D] as a 4-D map with 128-row boxes of
+// one swizzle atom's columns (like dO), and the fp32 RoPE table [S, D/2]
+// (cos, sin) pairs as a 2-D map of D floats per row, boxes of 32 floats (16
+// pairs) x 128 rows with the 128-byte swizzle.
+template <int DD>
+cudaError_t make_epi_maps(const Problem &p, const DqEpilogue &ep, CUtensorMap &mx,
+                          CUtensorMap &mcs) {
+    using A = Atoms<DD>;
+    const uint64_t esz = 2, D = (uint64_t)p.D;
+    cudaError_t e;
+    {
+        const uint64_t dims[4] = {D, (uint64_t)p.H, (uint64_t)p.S, (uint64_t)p.B};
+        const uint64_t strides[3] = {D * esz, (uint64_t)p.H * D * esz, (uint64_t)p.S * p.H * D * esz};
+        const uint32_t box[4] = {(uint32_t)A::kCols, 1, (uint32_t)kTile, 1};
+        if ((e = encode_tmap_bf16(&mx, ep.q, 4, dims, strides, box, A::kSwizzleBytes)) !=
+            cudaSuccess)
+            return e;
+    }
+    {
+        const uint64_t dims[2] = {D, (uint64_t)p.S};
+        const uint64_t strides[1] = {D * sizeof(float)};
+        const uint32_t box[2] = {32, (uint32_t)kTile};
+        if ((e = encode_tmap_f32(&mcs, ep.tab, 2, dims, strides, box, 128)) != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
+}
+
 template <int D>
 cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, const void *dout,
-                        const float *lse, const float *dlt, float *dqhat, unsigned int *err,
-                        cudaStream_t st) {
+                        const float *lse, const float *dlt, const DqEpilogue &ep,
+                        unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
     const int n_qt = (p.max_len + kTile - 1) / kTile;
     const long blocks = (long)p.units * p.H * n_qt;
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemB);
+    CUtensorMap mx, mcs;
+    cudaError_t e = make_epi_maps<D>(p, ep, mx, mcs);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, dqhat,
-        SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
+        m.k, m.v, mx, mcs, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, ep.gamma_q,
+        ep.rstd_q, (bf16 *)ep.dq, ep.part_q, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
     return cudaGetLastError();
 }
 
@@ -858,12 +1052,12 @@ cudaError_t run_dkdv(const Problem &p, const void *qhat, const void *khat, const
 
 template <int D>
 cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const void *v,
-                   const void *dout, const float *lse, const float *dlt, float *dqhat,
+                   const void *dout, const float *lse, const float *dlt, const DqEpilogue &ep,
                    unsigned int *err, cudaStream_t st) {
     BwdMaps m;
     cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
     if (e != cudaSuccess) return e;
-    return launch_dq_d<D>(p, m, qhat, dout, lse, dlt, dqhat, err, st);
+    return launch_dq_d<D>(p, m, qhat, dout, lse, dlt, ep, err, st);
 }
 
 }  // namespace
@@ -890,12 +1084,16 @@ cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat
     return cudaGetLastError();
 }
 
+size_t dq_part_count(const Problem &p) {
+    return (size_t)p.units * p.H * ((p.max_len + kTile - 1) / kTile);
+}
+
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
-                             const void *dout, const float *lse, const float *dlt, float *dqhat,
-                             unsigned int *err, cudaStream_t st) {
-    if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
-    if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
-    if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, lse, dlt, dqhat, err, st);
+                             const void *dout, const float *lse, const float *dlt,
+                             const DqEpilogue &ep, unsigned int *err, cudaStream_t st) {
+    if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
+    if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
+    if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
     return cudaErrorInvalidValue;
 }
 

@@ -67,6 +67,8 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, float *dlt,
                            unsigned int *err, cudaStream_t st);
 // Writes the number of dgamma partial rows it produced (<= kMaxNormParts) to *nparts.
+// dqhat == nullptr: the k rows only (dq and its dgamma partials come from the
+// bf16 dQ kernel); part_q is then untouched.
 cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *dkhat,
                             const void *q, const void *k, const float *gq, const float *gk,
                             const float *rstd_q, const float *rstd_k, const void *tab, void *dq,
@@ -99,6 +101,9 @@ cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const f
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                              const uint64_t *strides_bytes, const uint32_t *box,
                              int swizzle_bytes);
+cudaError_t encode_tmap_f32(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                            const uint64_t *strides_bytes, const uint32_t *box,
+                            int swizzle_bytes);
 
 // ---- bf16 tcgen05 kernels ----
 cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
@@ -113,9 +118,21 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *k
                                unsigned int *err, cudaStream_t st);
 cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat, void *dv,
                                cudaStream_t st);
+// The dQ kernel finishes dq itself (RoPE backward and RMSNorm backward of
+// each owned row) and writes one dgamma_q partial row per CTA: dq_part_count(p)
+// rows of D floats at part_q (CTAs past a short sample write zeros).
+struct DqEpilogue {
+    const void *q;          // [.., S, H, D] bf16 forward input
+    const float *gamma_q;   // [D]
+    const float *rstd_q;    // [.., S, H]
+    const void *tab;        // RoPE table (float2 [rows, D/2])
+    void *dq;               // [.., S, H, D] bf16 out
+    float *part_q;          // [dq_part_count(p), D]
+};
+size_t dq_part_count(const Problem &p);
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
-                             const void *dout, const float *lse, const float *dlt, float *dqhat,
-                             unsigned int *err, cudaStream_t st);
+                             const void *dout, const float *lse, const float *dlt,
+                             const DqEpilogue &ep, unsigned int *err, cudaStream_t st);
 
 // ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
 cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,

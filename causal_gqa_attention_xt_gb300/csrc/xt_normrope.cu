@@ -390,6 +390,8 @@ k_bwd_pre(const T *__restrict__ out, const T *__restrict__ dout, float *__restri
 
 // ---------------------------------------------------------------- epilogue
 // dq = RMSNorm_bwd(RoPE_bwd(dqhat)), likewise dk; one dgamma partial per CTA.
+// With dqhat == nullptr (bf16: the dQ kernel finishes dq itself) the units
+// cover the k heads only.
 constexpr int kStagesEpi = 2;
 
 template <typename T>
@@ -514,7 +516,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     if (any_failed) return;
     float *red = reinterpret_cast<float *>(smem + ring_offset<NS>());
     const int nslots = kWarps * rpi, slot = warp * rpi + sub;
-    for (int pass = 0; pass < 2; ++pass) {   // pass 0: q, pass 1: k
+    for (int pass = geo.nqc > 0 ? 0 : 1; pass < 2; ++pass) {   // pass 0: q, pass 1: k
         const bool mine = (pass == 0) == wq;
         if (pass) __syncthreads();
         if (lane_has) {
@@ -546,8 +548,18 @@ k_dgamma_reduce(const float *__restrict__ part_q, const float *__restrict__ part
     const int c = threadIdx.x & 31, slice = threadIdx.x >> 5;
     const int d = blockIdx.x * 32 + c;
     float sum = 0.f;
-    if (d < D)
-        for (int p = slice; p < nparts; p += 32) sum += part[(size_t)p * D + d];
+    if (d < D) {
+        // eight loads in flight, added in the same order as one at a time
+        int p = slice;
+        for (; p + 32 * 7 < nparts; p += 32 * 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(p + 32 * u) * D + d];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) sum += v[u];
+        }
+        for (; p < nparts; p += 32) sum += part[(size_t)p * D + d];
+    }
     red[slice][c] = sum;
     __syncthreads();
     if (slice == 0 && d < D) {
@@ -678,8 +690,8 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
                             unsigned int *err, cudaStream_t st) {
     const size_t es = p.dtype == 1 ? 2 : 4;
     const int rpi = rows_per_iter(p.D, p.dtype, true);
-    const UnitGeo geo = make_geo(p, p.H, p.G, (size_t)p.D * es, (size_t)p.D * sizeof(float),
-                                 sizeof(float), true, rpi, 6400);
+    const UnitGeo geo = make_geo(p, dqhat ? p.H : 0, p.G, (size_t)p.D * es,
+                                 (size_t)p.D * sizeof(float), sizeof(float), true, rpi, 6400);
     size_t ring = (size_t)kWarps * kStagesEpi * geo.stage_bytes;
     const size_t red = (size_t)kWarps * rpi * p.D * sizeof(float);
     if (ring < red) ring = red;

@@ -98,6 +98,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)),
+          "r"(c0), "r"(c1)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
                                             int c0, int c1, int c2) {
     asm volatile(
@@ -405,6 +415,16 @@ template <int D> struct Atoms {
         return (uint32_t)(kk * 16 * kRowBytes);
     }
 };
+
+// Byte offset at which TMA's 128-byte (row_bytes = 128) or 64-byte
+// (row_bytes = 64) swizzle puts the 16-byte chunk at logical byte offset `off`
+// of a 1024-byte-aligned box: address bits [4, 7) (or [4, 6)) are XORed with
+// bits [7, 10) (or [7, 9)).
+template <int RowBytes>
+__device__ __forceinline__ uint32_t swizzled(uint32_t off) {
+    constexpr uint32_t m = RowBytes == 128 ? 7u : 3u;
+    return off ^ (((off >> 7) & m) << 4);
+}
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                               uint32_t sbo_bytes, uint64_t swizzle) {

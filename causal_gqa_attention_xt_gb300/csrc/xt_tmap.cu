@@ -33,23 +33,41 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-// bf16 tensor of `rank` dims (innermost first), byte strides of dims 1..rank-1,
-// box sizes per dim, 128- or 64-byte swizzle, zero fill out of bounds.
-cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
-                             const uint64_t *strides_bytes, const uint32_t *box,
-                             int swizzle_bytes) {
+namespace {
+
+cudaError_t encode_tmap(CUtensorMap *map, CUtensorMapDataType type, const void *base, int rank,
+                        const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                        int swizzle_bytes) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return cudaErrorNotSupported;
     cuuint64_t d[5], s[4];
     cuuint32_t b[5], es[5];
     for (int i = 0; i < rank; ++i) { d[i] = dims[i]; b[i] = box[i]; es[i] = 1; }
     for (int i = 0; i < rank - 1; ++i) s[i] = strides_bytes[i];
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank,
-                     const_cast<void *>(base), d, s, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    CUresult r = enc(map, type, (cuuint32_t)rank, const_cast<void *>(base), d, s, b, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
                      swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// A tensor of `rank` dims (innermost first), byte strides of dims 1..rank-1,
+// box sizes per dim, 128- or 64-byte swizzle, zero fill out of bounds.
+cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                             const uint64_t *strides_bytes, const uint32_t *box,
+                             int swizzle_bytes) {
+    return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides_bytes,
+                       box, swizzle_bytes);
+}
+
+cudaError_t encode_tmap_f32(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
+                            const uint64_t *strides_bytes, const uint32_t *box,
+                            int swizzle_bytes) {
+    return encode_tmap(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, rank, dims, strides_bytes,
+                       box, swizzle_bytes);
 }
 
 }  // namespace xt

@@ -55,7 +55,7 @@ def lib():
     L.xt_attn_bwd_noalloc.argtypes = [i, i, i, i, i, d, d, vp, vp, vp, vp, vp, i, vp, vp, vp, vp,
                                       vp, vp, vp, vp, vp, vp, vp, vp, vp]
     L.xt_attn_bwd_noalloc.restype = i
-    L.xt_attn_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i]
+    L.xt_attn_varlen_workspace_bytes.argtypes = [i, i, i, i, i, i, i, i]
     L.xt_attn_varlen_workspace_bytes.restype = sz
     L.xt_attn_fwd_varlen.argtypes = [i, i, i, i, i, i, d, d, vp, vp, vp, vp, vp, vp, i, vp, vp,
                                      vp, vp, vp, vp, vp, sz, vp]
@@ -201,10 +201,10 @@ def xt_attn_bwd_noalloc(q, k, v, gamma_q, gamma_k, saved, dout, eps, theta, *, d
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgamma_q, dgamma_k=dgamma_k)
 
 
-def xt_attn_varlen_workspace_bytes(total, max_seqlen, n_heads, n_kv_heads, head_dim, dtype,
-                                   backward) -> int:
+def xt_attn_varlen_workspace_bytes(total, nseq, max_seqlen, n_heads, n_kv_heads, head_dim,
+                                   dtype, backward) -> int:
     code = dtype if isinstance(dtype, int) else _dtype_code(dtype)
-    return int(lib().xt_attn_varlen_workspace_bytes(total, max_seqlen, n_heads, n_kv_heads,
+    return int(lib().xt_attn_varlen_workspace_bytes(total, nseq, max_seqlen, n_heads, n_kv_heads,
                                                     head_dim, code, int(bool(backward))))
 
 
@@ -235,7 +235,7 @@ def xt_attn_fwd_varlen(q, k, v, gamma_q, gamma_k, cu_seqlens, max_seqlen, eps, t
     rstd_q = rstd_q if rstd_q is not None else torch.empty((T, H), **f32)
     rstd_k = rstd_k if rstd_k is not None else torch.empty((T, G), **f32)
     code = _dtype_code(dt)
-    need = xt_attn_varlen_workspace_bytes(T, max_seqlen, H, G, D, code, False)
+    need = xt_attn_varlen_workspace_bytes(T, nseq, max_seqlen, H, G, D, code, False)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
     wbytes = workspace.numel() * workspace.element_size()
@@ -263,7 +263,7 @@ def xt_attn_bwd_varlen(q, k, v, gamma_q, gamma_k, cu_seqlens, max_seqlen, saved,
     dgamma_q = dgamma_q if dgamma_q is not None else torch.empty(D, device=dev, dtype=torch.float32)
     dgamma_k = dgamma_k if dgamma_k is not None else torch.empty(D, device=dev, dtype=torch.float32)
     code = _dtype_code(dt)
-    need = xt_attn_varlen_workspace_bytes(T, max_seqlen, H, G, D, code, True)
+    need = xt_attn_varlen_workspace_bytes(T, nseq, max_seqlen, H, G, D, code, True)
     if workspace is None:
         workspace = torch.empty(max(need, 16), device=dev, dtype=torch.uint8)
     wbytes = workspace.numel() * workspace.element_size()

@@ -77,8 +77,11 @@ typedef enum {
 /* Bytes of scratch the forward (backward = 0) or backward (backward != 0)
  * call needs for this problem; 0 on invalid arguments. The forward's scratch
  * is the RoPE table, S * head_dim/2 (cos, sin) fp32 pairs (rounded up to 256
- * bytes); the backward's holds that table too, plus Dlt [B, H, S], fp32 dQhat
- * and dKhat, 2 * 1024 * head_dim floats of dgamma partials and, for bf16
+ * bytes); the backward's holds that table too, plus Dlt [B, H, S], fp32
+ * dKhat, fp32 dQhat (fp32 problems only: the bf16 dQ kernel finishes dq
+ * itself), dgamma partials (1024 * head_dim floats for the k rows; for the q
+ * rows as many again in fp32, or one head_dim row per (b, head, 128-row query
+ * tile) in bf16) and, for bf16
  * problems whose key/value heads carry far more work than there are blocks
  * to share it (few kv heads and long sequences, e.g. MQA), fp32 partials of
  * the dK/dV tiles whose work is split over several thread blocks. The size
@@ -161,12 +164,14 @@ int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, int head_dim,
  * pointer (XT_EINVAL), and a device-side check of the offsets raises the
  * error word, which xt_attn_check() reports as XT_EINVAL (accesses stay in
  * bounds either way; results are then unspecified).
- * Workspace: xt_attn_varlen_workspace_bytes() (the forward's RoPE table has
- * one row per packed row). Grids are sized by max_seqlen: a short sample's
- * blocks past its end exit at once. dtype XT_F32 needs nseq * n_heads <= 65535.
+ * Workspace: xt_attn_varlen_workspace_bytes() for the same total, nseq and
+ * max_seqlen (the forward's RoPE table has one row per packed row; the bf16
+ * backward keeps one dgamma_q partial row per (sample, head, 128-row query
+ * tile of max_seqlen)); 0 for invalid sizes. Grids are sized by max_seqlen: a
+ * short sample's blocks past its end exit at once. dtype XT_F32 needs nseq * n_heads <= 65535.
  * Deterministic, like the batched calls. */
-size_t xt_attn_varlen_workspace_bytes(int total, int max_seqlen, int n_heads, int n_kv_heads,
-                                      int head_dim, int dtype, int backward);
+size_t xt_attn_varlen_workspace_bytes(int total, int nseq, int max_seqlen, int n_heads,
+                                      int n_kv_heads, int head_dim, int dtype, int backward);
 
 int xt_attn_fwd_varlen(int total, int nseq, int max_seqlen, int n_heads, int n_kv_heads,
                        int head_dim, double eps, double theta, const int *cu_seqlens,

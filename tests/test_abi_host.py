@@ -142,13 +142,17 @@ def test_varlen_validation_rejects_before_launch(L, kw, code):
 
 
 def test_varlen_workspace(L):
-    fneed = xt.xt_attn_varlen_workspace_bytes(1000, 300, 4, 2, 64, 1, False)
-    bneed = xt.xt_attn_varlen_workspace_bytes(1000, 300, 4, 2, 64, 1, True)
+    fneed = xt.xt_attn_varlen_workspace_bytes(1000, 5, 300, 4, 2, 64, 1, False)
+    bneed = xt.xt_attn_varlen_workspace_bytes(1000, 5, 300, 4, 2, 64, 1, True)
     assert fneed >= 1000 * 32 * 8 and bneed > fneed   # one (cos, sin) row per packed row
-    assert xt.xt_attn_varlen_workspace_bytes(1000, 1001, 4, 2, 64, 1, False) == 0
+    assert xt.xt_attn_varlen_workspace_bytes(1000, 5, 1001, 4, 2, 64, 1, False) == 0
+    assert xt.xt_attn_varlen_workspace_bytes(1000, 0, 300, 4, 2, 64, 1, True) == 0
+    # the bf16 backward keeps a dgamma_q partial row per (sample, head, query tile)
+    more = xt.xt_attn_varlen_workspace_bytes(1000, 9, 300, 4, 2, 64, 1, True)
+    assert more >= bneed + 4 * 4 * 3 * 64 * 4 - 256
     assert _fwd_varlen(L, ws=ctypes.c_void_p(16), wbytes=100) == xt.XT_EWORKSPACE
     p = ctypes.c_void_p(16)
-    need = xt.xt_attn_varlen_workspace_bytes(64, 32, 4, 2, 64, 1, True)
+    need = xt.xt_attn_varlen_workspace_bytes(64, 3, 32, 4, 2, 64, 1, True)
     args = [64, 3, 32, 4, 2, 64, 1e-5, 1e4, p] + [p] * 5 + [1] + [p] * 7 + [p] * 5
     assert L.xt_attn_bwd_varlen(*args, p, need - 1, None) == xt.XT_EWORKSPACE
     bad = list(args)
