@@ -116,10 +116,11 @@ size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 // Forward scratch: the RoPE cos/sin table.
 size_t fwd_workspace(const Problem &p) { return align_up(rope_table_bytes(p)); }
 
-// Backward scratch: the RoPE cos/sin table, Dlt, fp32 dKhat (and dQhat for
-// fp32 problems), the dgamma partials (the epilogue's, at most kMaxNormParts
-// rows; for bf16 the q rows' come from the dQ kernel, one row per CTA) and
-// the split dK/dV partials.
+// Backward scratch: the RoPE cos/sin table, Dlt, fp32 dQhat and dKhat where
+// a separate epilogue finishes dq / dk (fp32 problems; dk of bf16 problems
+// with split dK/dV tiles), the dgamma partials (the epilogue's, at most
+// kMaxNormParts rows, or one row per CTA of the bf16 kernels that finish
+// their rows themselves) and the split dK/dV partials.
 struct BwdWorkspace {
     size_t off_tab, off_dlt, off_dqhat, off_dkhat, off_part_q, off_part_k, off_dkdv, total;
 };
@@ -130,13 +131,16 @@ BwdWorkspace bwd_layout(const Problem &p) {
     w.off_tab = o;    o = align_up(o + rope_table_bytes(p));
     w.off_dlt = o;    o = align_up(o + sizeof(float) * (size_t)p.B * p.H * p.S);
     // bf16: the dQ kernel finishes dq itself (no fp32 dQhat), one dgamma_q
-    // partial per CTA of it
+    // partial per CTA of it; likewise the dK/dV kernel for dk unless it splits
     const bool tc = p.dtype == XT_BF16;
+    const bool fuse_k = tc && dkdv_part_bytes(p) == 0;
     w.off_dqhat = o;  o = align_up(o + (tc ? 0 : sizeof(float) * (size_t)p.B * p.H * p.S * p.D));
-    w.off_dkhat = o;  o = align_up(o + sizeof(float) * (size_t)p.B * p.G * p.S * p.D);
+    w.off_dkhat = o;
+    o = align_up(o + (fuse_k ? 0 : sizeof(float) * (size_t)p.B * p.G * p.S * p.D));
     w.off_part_q = o;
     o = align_up(o + sizeof(float) * (tc ? dq_part_count(p) : (size_t)kMaxNormParts) * p.D);
-    w.off_part_k = o; o = align_up(o + sizeof(float) * (size_t)kMaxNormParts * p.D);
+    w.off_part_k = o;
+    o = align_up(o + sizeof(float) * (fuse_k ? dk_part_count(p) : (size_t)kMaxNormParts) * p.D);
     w.off_dkdv = o;   o = align_up(o + (p.dtype == XT_BF16 ? dkdv_part_bytes(p) : 0));
     w.total = o;
     return w;
@@ -240,11 +244,14 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
         return launch_bwd_pre(p, out, dout, dlt, err, s);
     });
     if (st != XT_OK) return st;
-    if (p.dtype == XT_BF16) {
+    const bool tc = p.dtype == XT_BF16;
+    const bool fuse_k = tc && dkdv_part_bytes(p) == 0;   // the dK/dV kernel finishes dk
+    if (tc) {
         float *part_dkdv = (float *)(ws + w.off_dkdv);
+        const RowEpilogue ek = {k, gamma_k, rstd_k, tab, dk, part_k};
         st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
             return launch_bwd_dkdv_tc(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, part_dkdv,
-                                      err, s);
+                                      ek, err, s);
         });
         if (st != XT_OK) return st;
         if (dkdv_part_bytes(p) > 0) {
@@ -253,7 +260,7 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
             });
             if (st != XT_OK) return st;
         }
-        const DqEpilogue ep = {q, gamma_q, rstd_q, tab, dq, part_q};
+        const RowEpilogue ep = {q, gamma_q, rstd_q, tab, dq, part_q};
         st = timed_launch(KID_BWD_DQ_TC, s, [&] {
             return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, ep, err, s);
         });
@@ -269,15 +276,17 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
         if (st != XT_OK) return st;
     }
     int nparts = 0;
-    const bool tc = p.dtype == XT_BF16;
-    st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
-        return launch_epilogue(p, tc ? nullptr : dqhat, dkhat, q, k, gamma_q, gamma_k, rstd_q,
-                               rstd_k, tab, dq, dk, part_q, part_k, &nparts, err, s);
-    });
-    if (st != XT_OK) return st;
+    if (!fuse_k) {   // k rows (and, for fp32, q rows) not finished by the attention kernels
+        st = timed_launch(KID_BWD_EPILOGUE, s, [&] {
+            return launch_epilogue(p, tc ? nullptr : dqhat, dkhat, q, k, gamma_q, gamma_k,
+                                   rstd_q, rstd_k, tab, dq, dk, part_q, part_k, &nparts, err, s);
+        });
+        if (st != XT_OK) return st;
+    }
     const int nparts_q = tc ? (int)dq_part_count(p) : nparts;
+    const int nparts_k = fuse_k ? (int)dk_part_count(p) : nparts;
     return timed_launch(KID_DGAMMA_REDUCE, s, [&] {
-        return launch_dgamma_reduce(p, part_q, part_k, nparts_q, nparts, dgamma_q, dgamma_k, s);
+        return launch_dgamma_reduce(p, part_q, part_k, nparts_q, nparts_k, dgamma_q, dgamma_k, s);
     });
 }
 

@@ -94,7 +94,14 @@ template <int D> struct BwdCfg {
     static constexpr int kHStages = (D == 128) ? 4 : 8;
     static constexpr int kHStageBytes = 2 * kHalfBytes + 1024;
     static constexpr int kSmemA = 2 * kTileBytes + kHStages * kHStageBytes + 1024;
+    // the dk epilogue takes three half stages after the last streamed half: the
+    // k rows (a whole tile) and two 64-row halves of their (cos, sin) rows
+    static_assert(kTileBytes <= kHStageBytes && (D / 32) * 64 * 128 <= kHStageBytes &&
+                  kHStages >= 4, "dk epilogue inputs must fit the half stages");
 };
+
+// One piece of the dk epilogue's (cos, sin) rows: 64 rows x 16 pairs (128 bytes).
+constexpr int kCsPieceBytes = 64 * 128;
 
 struct BwdBarriers {
     uint64_t own_full;
@@ -163,19 +170,185 @@ __host__ __device__ inline int dkdv_chunks(int iters, int chunk) {
     return (chunk > 0 && iters > chunk) ? (iters + chunk - 1) / chunk : 1;
 }
 
+// Scratch of the row epilogue (finish_rows): per-warpgroup parts of each row's
+// norm dot product, per-(warpgroup, row quarter) column sums of the dgamma
+// terms, and the rows' rstd and gamma.
+struct EpiScratch {
+    float dot[kSoftmaxWGs][kTile];
+    float g[kSoftmaxWGs][4][32];
+    float rstd[kTile];               // rstd_q of the owned rows (0 past the end)
+    float gamma[kTile];              // gamma_q (D <= kTile)
+};
+
+// The 512 softmax threads (warps 0-15) only.
+__device__ __forceinline__ void softmax_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kSoftmaxWGs) : "memory");
+}
+
+// Element e of 32 bf16 packed two per word (the lower index in the low half).
+__device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[16], int e) {
+    const uint32_t v = w[e >> 1];
+    return __uint_as_float((e & 1) ? (v & 0xffff0000u) : (v << 16));
+}
+
+// Transposing butterfly: every lane holds 32 values v[c] (c = column); after
+// five exchange steps lane l holds the sum over the 32 lanes of column l (each
+// step a lane keeps half of its columns, sends the other half to the partner
+// lane and adds the partner's copy of the kept half). Fixed association.
+__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int n = 16; n >= 1; n >>= 1) {
+        const bool up = (lane & n) != 0;
+#pragma unroll
+        for (int e = 0; e < n; ++e) {
+            const float send = up ? v[e] : v[e + n];
+            const float keep = up ? v[e + n] : v[e];
+            v[e] = keep + __shfl_xor_sync(0xffffffffu, send, n);
+        }
+    }
+    return v[0];
+}
+
+
+// The epilogue that turns the gradient of 128 normed-and-rotated rows into the
+// gradient of the raw rows (Mint project report 5.4.4: RoPE backward, the
+// rotation by the negative angle; 5.5.2: RMSNorm backward with the shared
+// gamma) and the CTA's dgamma partial, for the 512 softmax threads (thread =
+// row r = TMEM lane). Inputs: the accumulator in TMEM columns [0, D) at `tacc`
+// (this warp's lanes; the gradient times sqrt(D)), the raw rows in shared
+// memory as D / kCols TMA boxes of 128 rows (tc::Atoms<D> layout), this
+// thread's (cos, sin) row of pairs [16 wg, 16 wg + 16) at `cs_row` (a 128-byte
+// row of a 128-byte-swizzled fp32 box, unswizzled start), and rstd and gamma
+// in escr (written before the call by other threads: the first named barrier
+// orders them). Warpgroup wg < D/32 takes the 16 pairs [16 wg, 16 wg + 16)
+// (columns 16 wg.. and D/2 + 16 wg..) of its row; the row's dot product is
+// summed over those warpgroups in order. The dgamma terms are summed over the
+// warp's rows by a transposing butterfly, then over the four row quarters in
+// order, into part[0, D). Every softmax thread must call this (it holds three
+// named barriers); with ok false it only writes a zero partial.
+template <int D>
+__device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int lane,
+                                            uint32_t tacc, const uint8_t *sX,
+                                            const uint8_t *cs_row, bool row_ok,
+                                            EpiScratch &escr, bf16 *dst_row, float *part) {
+    using A = Atoms<D>;
+    constexpr int kHalf = D / 2, kEpiWGs = D / 32;
+    const bool in_epi = wg < kEpiWGs;
+    const int i0 = wg * 16;
+    const int r = quarter * 32 + lane;
+    softmax_bar_sync();   // the stashed gamma and rstd are visible from here on
+    uint32_t xw[16];      // the row's x: 8 words of the low pairs' columns, then 8 of the high
+    float dy[32];         // dy[e] (e < 16): column i0 + e; dy[16 + e]: column D/2 + i0 + e
+#pragma unroll
+    for (int e = 0; e < 32; ++e) dy[e] = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) xw[e] = 0u;
+    if (ok && in_epi) {
+        tc_fence_after();
+#pragma unroll
+        for (int part8 = 0; part8 < 4; ++part8) {
+            // 8-column chunks: i0, i0+8 (low), D/2+i0, D/2+i0+8 (high)
+            const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
+            const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                            r * A::kRowBytes + (col % A::kCols) * 2);
+            const uint4 v = *reinterpret_cast<const uint4 *>(sX + swizzled<A::kRowBytes>(off));
+            xw[4 * part8] = v.x; xw[4 * part8 + 1] = v.y;
+            xw[4 * part8 + 2] = v.z; xw[4 * part8 + 3] = v.w;
+        }
+        uint32_t a[16], b[16];
+        tmem_ld16_pair_sync(tacc + i0, a, tacc + kHalf + i0, b);
+        const float scale = rsqrtf((float)D);
+        float dotp = 0.f;
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            // (cos, sin) of pairs e, e+1: the 16-byte chunk e/2 of the swizzled row
+            const float4 c2 = *reinterpret_cast<const float4 *>(cs_row + (((e >> 1) ^ (r & 7)) << 4));
+            const float cv[2] = {c2.x, c2.z}, sv[2] = {c2.y, c2.w};
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float gl = __uint_as_float(a[e + x]) * scale;
+                const float gh = __uint_as_float(b[e + x]) * scale;
+                // rotation by the negative angle
+                const float dyl = gl * cv[x] + gh * sv[x];
+                const float dyh = gh * cv[x] - gl * sv[x];
+                dy[e + x] = dyl;
+                dy[16 + e + x] = dyh;
+                dotp = fmaf(escr.gamma[i0 + e + x] * dyl, bf16_lo_or_hi(xw, e + x), dotp);
+                dotp = fmaf(escr.gamma[kHalf + i0 + e + x] * dyh, bf16_lo_or_hi(xw, 16 + e + x),
+                            dotp);
+            }
+        }
+        escr.dot[wg][r] = dotp;
+    }
+    softmax_bar_sync();
+    if (ok && in_epi) {
+        float dot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kEpiWGs; ++w) dot += escr.dot[w][r];
+        const float rr = escr.rstd[r];
+        const float corr = dot * rr * rr * rr * (1.0f / (float)D);
+        uint32_t ow[16];
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+            float ol[2], oh[2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                const float xl = bf16_lo_or_hi(xw, e + x), xh = bf16_lo_or_hi(xw, 16 + e + x);
+                ol[x] = escr.gamma[i0 + e + x] * dy[e + x] * rr - xl * corr;
+                oh[x] = escr.gamma[kHalf + i0 + e + x] * dy[16 + e + x] * rr - xh * corr;
+                // the dgamma terms replace dy
+                dy[e + x] = dy[e + x] * xl * rr;
+                dy[16 + e + x] = dy[16 + e + x] * xh * rr;
+            }
+            ow[e / 2] = pack_bf16x2(ol[0], ol[1]);
+            ow[8 + e / 2] = pack_bf16x2(oh[0], oh[1]);
+        }
+        if (row_ok) {
+            uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
+            dst[i0 / 8] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            dst[i0 / 8 + 1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+            dst[(kHalf + i0) / 8] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
+            dst[(kHalf + i0) / 8 + 1] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
+        }
+        // column sums over the warp's 32 rows: lane l ends with column l of dy
+        escr.g[wg][quarter][lane] = transpose_sum32(dy, lane);
+    }
+    softmax_bar_sync();
+    if (threadIdx.x < D) {
+        // column d of the partial: the four row quarters of its warpgroup, in order
+        const int d = threadIdx.x;
+        const int w = (d < kHalf ? d : d - kHalf) / 16;
+        const int l = (d < kHalf ? 0 : 16) + (d & 15);
+        float sum = 0.f;
+        if (ok) {
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) sum += escr.g[w][qq][l];
+        }
+        part[d] = sum;
+    }
+}
+
 // kSplit: the chunked work split is on (a separate instantiation keeps the
-// unsplit kernel free of its index arithmetic).
+// unsplit kernel free of its index arithmetic). The unsplit kernel finishes dk
+// itself (finish_rows on dKhat; one dgamma_k partial per CTA at part_k); the
+// split one writes fp32 dKhat (or chunk partials) for the reduce and the k-row
+// epilogue.
 template <int D, bool kSplit>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
               const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+              const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
               const float *__restrict__ lse, const float *__restrict__ dlt,
               float *__restrict__ dkhat, bf16 *__restrict__ dv, float *__restrict__ part,
-              const SeqRows sr, int H, int G, int n_kvt, int chunk, int nw, unsigned int *err) {
+              const float *__restrict__ gamma_k, const float *__restrict__ rstd_k,
+              bf16 *__restrict__ dk, float *__restrict__ part_k, const SeqRows sr, int H, int G,
+              int n_kvt, int chunk, int nw, unsigned int *err) {
     using C = BwdCfg<D>;
     constexpr int HS = C::kHStages;
+    constexpr bool kFuse = !kSplit;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
+    __shared__ EpiScratch escr;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sK = smem;
     uint8_t *sV = smem + C::kTileBytes;
@@ -200,7 +373,12 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     const SeqSpan sp = seq_span(sr, unit);
     const int S = sp.len;                           // rows of this unit
     const int n_q = (S + kTile - 1) / kTile;
-    if (j >= n_q || cidx >= nc) return;             // a packed sample shorter than this tile
+    float *pk = kFuse ? part_k + ((size_t)bg * nw + witem) * D : nullptr;   // dgamma_k partial
+    if (j >= n_q || cidx >= nc) {                   // a packed sample shorter than this tile
+        if constexpr (kFuse)
+            for (int d = threadIdx.x; d < D; d += blockDim.x) pk[d] = 0.f;
+        return;
+    }
     const int nU = n_q - j;                         // query tiles at/after the keys, per head
     const int t0 = kSplit && nc > 1 ? cidx * chunk : 0;   // this CTA's iterations [t0, t0 + T)
     const int T = kSplit && nc > 1 ? min(chunk, group * nU - t0) : group * nU;
@@ -266,6 +444,38 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.st_full[hs]);
             issued = x + 1;
+        }
+        if constexpr (kFuse) {
+            // the dk epilogue's inputs, in the next three half stages as they free up:
+            // the owned k rows (one 128-row tile), then their (cos, sin) rows in two
+            // 64-row halves (D/32 boxes of 64 rows x 16 pairs each)
+            for (int e = 0; issued == 2 * T + e && e < 3; ++e) {
+                const int x = 2 * T + e, hs = x % HS;
+                bool ok = true;
+                if (x >= HS && lane == 0)
+                    ok = mbar_wait(&bars.st_empty[hs], ((x / HS) - 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+                    break;
+                }
+                uint8_t *base = sStage + hs * C::kHStageBytes;
+                if (lane == 0) {
+                    if (e == 0) {
+                        mbar_expect_tx(&bars.st_full[hs], C::kTileBytes);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_4d(base + c * C::kBox, &map_x, &bars.st_full[hs],
+                                        c * C::A::kCols, g, sp.start + j * kTile, sp.plane);
+                    } else {
+                        mbar_expect_tx(&bars.st_full[hs], (D / 32) * kCsPieceBytes);
+                        for (int c = 0; c < D / 32; ++c)
+                            tma_load_2d(base + c * kCsPieceBytes, &map_cs, &bars.st_full[hs],
+                                        32 * c, sp.start + j * kTile + 64 * (e - 1));
+                    }
+                    mbar_arrive(&bars.st_full[hs]);
+                }
+                issued = x + 1;
+            }
         }
         if (lane == 0) {
             // drain: every copy issued by this CTA lands before it exits
@@ -347,6 +557,11 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         const int kp = j * kTile + r;                   // key position
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
+        if (kFuse && wg == kSoftmaxWGs - 1) {
+            // for the dk epilogue (read after its first named barrier)
+            escr.rstd[r] = kp < S ? rstd_k[((size_t)sp.plane * sr.S + sp.start + kp) * G + g] : 0.f;
+            if (r < D) escr.gamma[r] = gamma_k[r];
+        }
         bool ok = true;
         const int hf = wg >> 1;                         // this warpgroup's half of the tile
         for (int t = 0; t < T; ++t) {
@@ -421,7 +636,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 float *prow = kSplit && nc > 1
                     ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D : nullptr;
 #pragma unroll
-                for (int cc = wg; cc < 2 * (D / 32); cc += kSoftmaxWGs) {
+                for (int cc = wg; cc < (kFuse ? 1 : 2) * (D / 32); cc += kSoftmaxWGs) {
                     const bool isv = cc < D / 32;
                     const int c = isv ? cc : cc - D / 32;
                     uint32_t a[32];
@@ -461,6 +676,22 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                     }
                 }
             }
+        }
+        if constexpr (kFuse) {
+            // dk and the CTA's dgamma_k partial from dKhat in TMEM, with the k rows
+            // and their (cos, sin) rows that the producer loaded after the last half
+            const int x0 = 2 * T;
+            if (ok) ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&bars.st_full[x0 % HS], (x0 / HS) & 1, abort_flag) &&
+                                    mbar_wait(&bars.st_full[(x0 + 1) % HS], ((x0 + 1) / HS) & 1,
+                                              abort_flag) &&
+                                    mbar_wait(&bars.st_full[(x0 + 2) % HS], ((x0 + 2) / HS) & 1,
+                                              abort_flag));
+            const uint8_t *sX = sStage + (x0 % HS) * C::kHStageBytes;
+            const uint8_t *cs_row = sStage + ((x0 + 1 + (r >> 6)) % HS) * C::kHStageBytes +
+                                    wg * kCsPieceBytes + (r & 63) * 128;
+            finish_rows<D>(ok, wg, quarter, lane, tmem + 384 + lane_off, sX, cs_row, kp < S, escr,
+                           dk + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D, pk);
         }
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
     }
@@ -503,44 +734,6 @@ k_dkdv_reduce(const float *__restrict__ part, float *__restrict__ dkhat, bf16 *_
 // ---------------------------------------------------------------------------
 // dQhat and the dq epilogue
 // ---------------------------------------------------------------------------
-// Scratch of the dq epilogue: per-warpgroup parts of each row's norm dot
-// product, and per-(warpgroup, row quarter) column sums of the dgamma terms.
-struct EpiScratch {
-    float dot[kSoftmaxWGs][kTile];
-    float g[kSoftmaxWGs][4][32];
-    float rstd[kTile];               // rstd_q of the owned rows (0 past the end)
-    float gamma[kTile];              // gamma_q (D <= kTile)
-};
-
-// The 512 softmax threads (warps 0-15) only.
-__device__ __forceinline__ void softmax_bar_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kSoftmaxWGs) : "memory");
-}
-
-// Element e of 32 bf16 packed two per word (the lower index in the low half).
-__device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[16], int e) {
-    const uint32_t v = w[e >> 1];
-    return __uint_as_float((e & 1) ? (v & 0xffff0000u) : (v << 16));
-}
-
-// Transposing butterfly: every lane holds 32 values v[c] (c = column); after
-// five exchange steps lane l holds the sum over the 32 lanes of column l (each
-// step a lane keeps half of its columns, sends the other half to the partner
-// lane and adds the partner's copy of the kept half). Fixed association.
-__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
-#pragma unroll
-    for (int n = 16; n >= 1; n >>= 1) {
-        const bool up = (lane & n) != 0;
-#pragma unroll
-        for (int e = 0; e < n; ++e) {
-            const float send = up ? v[e] : v[e + n];
-            const float keep = up ? v[e + n] : v[e];
-            v[e] = keep + __shfl_xor_sync(0xffffffffu, send, n);
-        }
-    }
-    return v[0];
-}
-
 template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -769,117 +962,16 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tc_fence_before();
             mbar_arrive(ds_ready);
         }
-        // ---- epilogue: dq = RMSNorm_bwd(RoPE_bwd(dQhat)) for the owned rows, and the
-        // CTA's dgamma_q partial. Warpgroup w < D/32 takes the 16 RoPE pairs
-        // [16w, 16w+16) (columns 16w.. and D/2+16w..) of its thread's row, reading
-        // the row's q and (cos, sin) values from shared memory (loaded by the
-        // producer); the row's norm dot product is summed over those warpgroups
-        // in order. Every softmax thread passes the three named barriers,
-        // whatever `ok` is.
-        using A = typename C::A;
-        constexpr int kHalf = D / 2, kEpiWGs = D / 32;
-        const bool in_epi = wg < kEpiWGs;
-        const int i0 = wg * 16;
-        const bool row_ok = tq < S;
+        // ---- epilogue: dq and the CTA's dgamma_q partial from dQhat in TMEM; q rows
+        // (own region) and their (cos, sin) rows (the stage after the last K/V
+        // tile, box wg = pairs [16 wg, 16 wg + 16)) were loaded by the producer
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag) &&
                                                  mbar_wait(&bars.x_full, 0, abort_flag) &&
                                                  mbar_wait(&bars.st_full[T % ST], (T / ST) & 1,
                                                            abort_flag));
-        // q of the row: 8 words of the low pairs' columns, then 8 of the high
-        softmax_bar_sync();   // the stashed gamma and rstd are visible from here on
-        uint32_t xw[16];
-        float dy[32];   // dy[e] (e < 16): column i0 + e; dy[16 + e]: column D/2 + i0 + e
-#pragma unroll
-        for (int e = 0; e < 32; ++e) dy[e] = 0.f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) xw[e] = 0u;
-        if (ok && in_epi) {
-            tc_fence_after();
-#pragma unroll
-            for (int part8 = 0; part8 < 4; ++part8) {
-                // 8-column chunks: i0, i0+8 (low), D/2+i0, D/2+i0+8 (high)
-                const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
-                const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
-                                                r * A::kRowBytes + (col % A::kCols) * 2);
-                const uint4 v = *reinterpret_cast<const uint4 *>(
-                    sX + swizzled<A::kRowBytes>(off));
-                xw[4 * part8] = v.x; xw[4 * part8 + 1] = v.y;
-                xw[4 * part8 + 2] = v.z; xw[4 * part8 + 3] = v.w;
-            }
-            uint32_t a[16], b[16];
-            tmem_ld16_pair_sync(tmem + 256 + lane_off + i0, a, tmem + 256 + lane_off + kHalf + i0, b);
-            const float scale = rsqrtf((float)D);
-            // (cos, sin) of pairs i0.. of the row: box wg of the cos/sin stage
-            const uint8_t *csb = sStage + (T % ST) * C::kStageBytes + wg * kTile * 128;
-            float dotp = 0.f;
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                const float4 c2 = *reinterpret_cast<const float4 *>(
-                    csb + swizzled<128>((uint32_t)(r * 128 + e * 8)));
-                const float cv[2] = {c2.x, c2.z}, sv[2] = {c2.y, c2.w};
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const float gl = __uint_as_float(a[e + x]) * scale;
-                    const float gh = __uint_as_float(b[e + x]) * scale;
-                    // rotation by the negative angle
-                    const float dyl = gl * cv[x] + gh * sv[x];
-                    const float dyh = gh * cv[x] - gl * sv[x];
-                    dy[e + x] = dyl;
-                    dy[16 + e + x] = dyh;
-                    dotp = fmaf(escr.gamma[i0 + e + x] * dyl, bf16_lo_or_hi(xw, e + x), dotp);
-                    dotp = fmaf(escr.gamma[kHalf + i0 + e + x] * dyh,
-                                bf16_lo_or_hi(xw, 16 + e + x), dotp);
-                }
-            }
-            escr.dot[wg][r] = dotp;
-        }
-        softmax_bar_sync();
-        if (ok && in_epi) {
-            float dot = 0.f;
-#pragma unroll
-            for (int w = 0; w < kEpiWGs; ++w) dot += escr.dot[w][r];
-            const float rr = escr.rstd[r];
-            const float corr = dot * rr * rr * rr * (1.0f / (float)D);
-            uint32_t ow[16];
-#pragma unroll
-            for (int e = 0; e < 16; e += 2) {
-                float ol[2], oh[2];
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const float xl = bf16_lo_or_hi(xw, e + x), xh = bf16_lo_or_hi(xw, 16 + e + x);
-                    ol[x] = escr.gamma[i0 + e + x] * dy[e + x] * rr - xl * corr;
-                    oh[x] = escr.gamma[kHalf + i0 + e + x] * dy[16 + e + x] * rr - xh * corr;
-                    // the dgamma terms replace dy
-                    dy[e + x] = dy[e + x] * xl * rr;
-                    dy[16 + e + x] = dy[16 + e + x] * xh * rr;
-                }
-                ow[e / 2] = pack_bf16x2(ol[0], ol[1]);
-                ow[8 + e / 2] = pack_bf16x2(oh[0], oh[1]);
-            }
-            if (row_ok) {
-                uint4 *dst = reinterpret_cast<uint4 *>(
-                    dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D);
-                dst[i0 / 8] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                dst[i0 / 8 + 1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-                dst[(kHalf + i0) / 8] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
-                dst[(kHalf + i0) / 8 + 1] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
-            }
-            // column sums over the warp's 32 rows: lane l ends with column l of dy
-            escr.g[wg][quarter][lane] = transpose_sum32(dy, lane);
-        }
-        softmax_bar_sync();
-        if (threadIdx.x < D) {
-            // column d of the partial: the four row quarters of its warpgroup, in order
-            const int d = threadIdx.x;
-            const int w = (d < kHalf ? d : d - kHalf) / 16;
-            const int l = (d < kHalf ? 0 : 16) + (d & 15);
-            float sum = 0.f;
-            if (ok) {
-#pragma unroll
-                for (int qq = 0; qq < 4; ++qq) sum += escr.g[w][qq][l];
-            }
-            part[d] = sum;
-        }
+        const uint8_t *cs_row = sStage + (T % ST) * C::kStageBytes + wg * kTile * 128 + r * 128;
+        finish_rows<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
+                       dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D, part);
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
     }
     tc_fence_before();
@@ -977,44 +1069,28 @@ DkdvPlan dkdv_plan(const Problem &p) {
     return pl;
 }
 
-template <int D>
-cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, const float *dlt,
-                          float *dkhat, void *dv, float *part, unsigned int *err, cudaStream_t st) {
-    using C = BwdCfg<D>;
-    const DkdvPlan pl = dkdv_plan(p);
-    const long blocks = (long)p.units * p.G * pl.nw;
-    auto kern = pl.n_split > 0 ? k_bwd_dkdv_tc<D, true> : k_bwd_dkdv_tc<D, false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemA);
-    if (e != cudaSuccess) return e;
-    kern<<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
-        m.k, m.v, m.q, m.dout, lse, dlt, dkhat, (bf16 *)dv, part, SeqRows{p.cu, p.S, p.max_len},
-        p.H, p.G, pl.n_kvt, pl.chunk, pl.nw, err);
-    return cudaGetLastError();
-}
-
-// The dq epilogue's inputs: q [B, S, H, D] as a 4-D map with 128-row boxes of
-// one swizzle atom's columns (like dO), and the fp32 RoPE table [S, D/2]
-// (cos, sin) pairs as a 2-D map of D floats per row, boxes of 32 floats (16
-// pairs) x 128 rows with the 128-byte swizzle.
+// The row epilogue's inputs: x (q or k) [B, S, heads, D] as a 4-D map with
+// 128-row boxes of one swizzle atom's columns, and the fp32 RoPE table
+// [S, D/2] (cos, sin) pairs as a 2-D map of D floats per row, boxes of 32
+// floats (16 pairs) x cs_rows rows with the 128-byte swizzle.
 template <int DD>
-cudaError_t make_epi_maps(const Problem &p, const DqEpilogue &ep, CUtensorMap &mx,
-                          CUtensorMap &mcs) {
+cudaError_t make_epi_maps(const Problem &p, const RowEpilogue &ep, int heads, int cs_rows,
+                          CUtensorMap &mx, CUtensorMap &mcs) {
     using A = Atoms<DD>;
-    const uint64_t esz = 2, D = (uint64_t)p.D;
+    const uint64_t esz = 2, D = (uint64_t)p.D, NH = (uint64_t)heads;
     cudaError_t e;
     {
-        const uint64_t dims[4] = {D, (uint64_t)p.H, (uint64_t)p.S, (uint64_t)p.B};
-        const uint64_t strides[3] = {D * esz, (uint64_t)p.H * D * esz, (uint64_t)p.S * p.H * D * esz};
+        const uint64_t dims[4] = {D, NH, (uint64_t)p.S, (uint64_t)p.B};
+        const uint64_t strides[3] = {D * esz, NH * D * esz, (uint64_t)p.S * NH * D * esz};
         const uint32_t box[4] = {(uint32_t)A::kCols, 1, (uint32_t)kTile, 1};
-        if ((e = encode_tmap_bf16(&mx, ep.q, 4, dims, strides, box, A::kSwizzleBytes)) !=
+        if ((e = encode_tmap_bf16(&mx, ep.x, 4, dims, strides, box, A::kSwizzleBytes)) !=
             cudaSuccess)
             return e;
     }
     {
         const uint64_t dims[2] = {D, (uint64_t)p.S};
         const uint64_t strides[1] = {D * sizeof(float)};
-        const uint32_t box[2] = {32, (uint32_t)kTile};
+        const uint32_t box[2] = {32, (uint32_t)cs_rows};
         if ((e = encode_tmap_f32(&mcs, ep.tab, 2, dims, strides, box, 128)) != cudaSuccess)
             return e;
     }
@@ -1022,37 +1098,59 @@ cudaError_t make_epi_maps(const Problem &p, const DqEpilogue &ep, CUtensorMap &m
 }
 
 template <int D>
+cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, const float *dlt,
+                          float *dkhat, void *dv, float *part, const RowEpilogue &ek,
+                          unsigned int *err, cudaStream_t st) {
+    using C = BwdCfg<D>;
+    const DkdvPlan pl = dkdv_plan(p);
+    const long blocks = (long)p.units * p.G * pl.nw;
+    const bool split = pl.n_split > 0;
+    CUtensorMap mx, mcs;
+    cudaError_t e = split ? cudaSuccess : make_epi_maps<D>(p, ek, p.G, 64, mx, mcs);
+    if (e != cudaSuccess) return e;
+    if (split) mx = mcs = m.k;   // unused by the split kernel
+    auto kern = split ? k_bwd_dkdv_tc<D, true> : k_bwd_dkdv_tc<D, false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
+    if (e != cudaSuccess) return e;
+    kern<<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
+        m.k, m.v, m.q, m.dout, mx, mcs, lse, dlt, dkhat, (bf16 *)dv, part, ek.gamma, ek.rstd,
+        (bf16 *)ek.out, ek.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, pl.n_kvt, pl.chunk,
+        pl.nw, err);
+    return cudaGetLastError();
+}
+
+template <int D>
 cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, const void *dout,
-                        const float *lse, const float *dlt, const DqEpilogue &ep,
+                        const float *lse, const float *dlt, const RowEpilogue &ep,
                         unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
     const int n_qt = (p.max_len + kTile - 1) / kTile;
     const long blocks = (long)p.units * p.H * n_qt;
     CUtensorMap mx, mcs;
-    cudaError_t e = make_epi_maps<D>(p, ep, mx, mcs);
+    cudaError_t e = make_epi_maps<D>(p, ep, p.H, kTile, mx, mcs);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, ep.gamma_q,
-        ep.rstd_q, (bf16 *)ep.dq, ep.part_q, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
+        m.k, m.v, mx, mcs, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, ep.gamma,
+        ep.rstd, (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
     return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t run_dkdv(const Problem &p, const void *qhat, const void *khat, const void *v,
                      const void *dout, const float *lse, const float *dlt, float *dkhat, void *dv,
-                     float *part, unsigned int *err, cudaStream_t st) {
+                     float *part, const RowEpilogue &ek, unsigned int *err, cudaStream_t st) {
     BwdMaps m;
     cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
     if (e != cudaSuccess) return e;
-    return launch_dkdv_d<D>(p, m, lse, dlt, dkhat, dv, part, err, st);
+    return launch_dkdv_d<D>(p, m, lse, dlt, dkhat, dv, part, ek, err, st);
 }
 
 template <int D>
 cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const void *v,
-                   const void *dout, const float *lse, const float *dlt, const DqEpilogue &ep,
+                   const void *dout, const float *lse, const float *dlt, const RowEpilogue &ep,
                    unsigned int *err, cudaStream_t st) {
     BwdMaps m;
     cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
@@ -1064,13 +1162,18 @@ cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const v
 
 size_t dkdv_part_bytes(const Problem &p) { return dkdv_plan(p).part_bytes; }
 
+size_t dk_part_count(const Problem &p) { return (size_t)p.units * p.G * dkdv_plan(p).nw; }
+
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
                                const float *dlt, float *dkhat, void *dv, float *part,
-                               unsigned int *err, cudaStream_t st) {
-    if (p.D == 128) return run_dkdv<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
-    if (p.D == 64) return run_dkdv<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
-    if (p.D == 32) return run_dkdv<32>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, err, st);
+                               const RowEpilogue &ek, unsigned int *err, cudaStream_t st) {
+    if (p.D == 128)
+        return run_dkdv<128>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, ek, err, st);
+    if (p.D == 64)
+        return run_dkdv<64>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, ek, err, st);
+    if (p.D == 32)
+        return run_dkdv<32>(p, qhat, khat, v, dout, lse, dlt, dkhat, dv, part, ek, err, st);
     return cudaErrorInvalidValue;
 }
 
@@ -1090,7 +1193,7 @@ size_t dq_part_count(const Problem &p) {
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                              const void *dout, const float *lse, const float *dlt,
-                             const DqEpilogue &ep, unsigned int *err, cudaStream_t st) {
+                             const RowEpilogue &ep, unsigned int *err, cudaStream_t st) {
     if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
     if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
     if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);

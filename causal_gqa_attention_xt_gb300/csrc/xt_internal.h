@@ -106,6 +106,23 @@ cudaError_t encode_tmap_f32(CUtensorMap *map, const void *base, int rank, const 
                             int swizzle_bytes);
 
 // ---- bf16 tcgen05 kernels ----
+// The bf16 backward kernels finish dq and dk themselves (RoPE backward and
+// RMSNorm backward of each owned row) and write one dgamma partial row of D
+// floats per CTA (CTAs past a short sample write zeros): the dQ kernel
+// dq_part_count(p) rows of dgamma_q; the dK/dV kernel, when dkdv_part_bytes(p)
+// is 0 (no split key tiles), dk_part_count(p) rows of dgamma_k (with split
+// tiles it writes fp32 dKhat and the k-row epilogue finishes dk).
+struct RowEpilogue {
+    const void *x;          // [.., S, heads, D] bf16 forward input (q or k)
+    const float *gamma;     // [D]
+    const float *rstd;      // [.., S, heads]
+    const void *tab;        // RoPE table (float2 [rows, D/2])
+    void *out;              // [.., S, heads, D] bf16: dq or dk
+    float *part;            // dgamma partial rows
+};
+size_t dq_part_count(const Problem &p);
+size_t dk_part_count(const Problem &p);
+
 cudaError_t launch_fwd_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                           void *out, float *lse, unsigned int *err, cudaStream_t st);
 // part: fp32 scratch of dkdv_part_bytes(p) for the chunk partials of key
@@ -115,24 +132,12 @@ size_t dkdv_part_bytes(const Problem &p);
 cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *khat,
                                const void *v, const void *dout, const float *lse,
                                const float *dlt, float *dkhat, void *dv, float *part,
-                               unsigned int *err, cudaStream_t st);
+                               const RowEpilogue &ek, unsigned int *err, cudaStream_t st);
 cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat, void *dv,
                                cudaStream_t st);
-// The dQ kernel finishes dq itself (RoPE backward and RMSNorm backward of
-// each owned row) and writes one dgamma_q partial row per CTA: dq_part_count(p)
-// rows of D floats at part_q (CTAs past a short sample write zeros).
-struct DqEpilogue {
-    const void *q;          // [.., S, H, D] bf16 forward input
-    const float *gamma_q;   // [D]
-    const float *rstd_q;    // [.., S, H]
-    const void *tab;        // RoPE table (float2 [rows, D/2])
-    void *dq;               // [.., S, H, D] bf16 out
-    float *part_q;          // [dq_part_count(p), D]
-};
-size_t dq_part_count(const Problem &p);
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
                              const void *dout, const float *lse, const float *dlt,
-                             const DqEpilogue &ep, unsigned int *err, cudaStream_t st);
+                             const RowEpilogue &ep, unsigned int *err, cudaStream_t st);
 
 // ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
 cudaError_t launch_fwd_simt(const Problem &p, const void *qhat, const void *khat, const void *v,
