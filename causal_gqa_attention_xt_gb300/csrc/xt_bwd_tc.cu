@@ -328,6 +328,79 @@ __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int la
     }
 }
 
+// finish_rows as a separate function: the dQ kernel calls it this way, which
+// keeps its main loop free of register spills (its live state there is at
+// the 96-register limit of 576-thread blocks).
+template <int D>
+__device__ __noinline__ void finish_rows_call(bool ok, int wg, int quarter, int lane,
+                                              uint32_t tacc, const uint8_t *sX,
+                                              const uint8_t *cs_row, bool row_ok,
+                                              EpiScratch &escr, bf16 *dst_row, float *part) {
+    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part);
+}
+
+// The dK/dV kernel's accumulator stores (a separate function, so that its
+// softmax loop keeps its registers): dV (bf16) and, unless the kernel
+// finishes dk itself, dKhat (fp32, scaled by 1/sqrt(D)) of this thread's key
+// row, or both as fp32 chunk partials when prow is set. 32-column chunks: dV
+// chunks 0..D/32-1, then dKhat; warpgroup w writes chunks w, w + 4, ...
+template <int D, bool kSplit>
+__device__ __noinline__ void store_dkdv_acc(int wg, uint32_t tacc, bool row_ok, bf16 *dvrow,
+                                            float *dkrow, float *prow) {
+    constexpr bool kFuse = !kSplit;
+    const float scale = rsqrtf((float)D);
+#pragma unroll
+    for (int cc = wg; cc < (kFuse ? 1 : 2) * (D / 32); cc += kSoftmaxWGs) {
+        const bool isv = cc < D / 32;
+        const int c = isv ? cc : cc - D / 32;
+        uint32_t a[32];
+        tmem_ld32_sync(tacc + (isv ? 256 : 384) + 32 * c, a);
+        if (row_ok && prow != nullptr) {
+            const float sc = isv ? 1.f : scale;
+            float *dst = prow + (isv ? 0 : (size_t)kTile * D) + 32 * c;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+                *reinterpret_cast<float4 *>(dst + 4 * q4) =
+                    make_float4(__uint_as_float(a[q4 * 4 + 0]) * sc,
+                                __uint_as_float(a[q4 * 4 + 1]) * sc,
+                                __uint_as_float(a[q4 * 4 + 2]) * sc,
+                                __uint_as_float(a[q4 * 4 + 3]) * sc);
+        } else if (row_ok) {
+            if (isv) {
+#pragma unroll
+                for (int q8 = 0; q8 < 4; ++q8) {
+                    uint4 v4;
+                    v4.x = pack_bf16x2(__uint_as_float(a[q8 * 8 + 0]), __uint_as_float(a[q8 * 8 + 1]));
+                    v4.y = pack_bf16x2(__uint_as_float(a[q8 * 8 + 2]), __uint_as_float(a[q8 * 8 + 3]));
+                    v4.z = pack_bf16x2(__uint_as_float(a[q8 * 8 + 4]), __uint_as_float(a[q8 * 8 + 5]));
+                    v4.w = pack_bf16x2(__uint_as_float(a[q8 * 8 + 6]), __uint_as_float(a[q8 * 8 + 7]));
+                    *reinterpret_cast<uint4 *>(dvrow + 32 * c + 8 * q8) = v4;
+                }
+            } else {
+#pragma unroll
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    float4 f;
+                    f.x = __uint_as_float(a[q4 * 4 + 0]) * scale;
+                    f.y = __uint_as_float(a[q4 * 4 + 1]) * scale;
+                    f.z = __uint_as_float(a[q4 * 4 + 2]) * scale;
+                    f.w = __uint_as_float(a[q4 * 4 + 3]) * scale;
+                    *reinterpret_cast<float4 *>(dkrow + 32 * c + 4 * q4) = f;
+                }
+            }
+        }
+    }
+}
+
+// finish_rows for the dK/dV kernel: its own out-of-line copy (sharing one
+// with the dQ kernel changes the dQ kernel's register allocation).
+template <int D>
+__device__ __noinline__ void finish_rows_dk(bool ok, int wg, int quarter, int lane,
+                                            uint32_t tacc, const uint8_t *sX,
+                                            const uint8_t *cs_row, bool row_ok,
+                                            EpiScratch &escr, bf16 *dst_row, float *part) {
+    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part);
+}
+
 // kSplit: the chunked work split is on (a separate instantiation keeps the
 // unsplit kernel free of its index arithmetic). The unsplit kernel finishes dk
 // itself (finish_rows on dKhat; one dgamma_k partial per CTA at part_k); the
@@ -627,54 +700,13 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag));
             if (ok) {
                 tc_fence_after();
-                // 32-column chunks: dV (bf16) chunks 0..D/32-1, then dKhat (fp32, scaled);
-                // warpgroup w writes chunks w, w + kSoftmaxWGs, ...
-                const float scale = rsqrtf((float)D);
-                bf16 *dvrow = dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D;
-                float *dkrow = dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D;
-                // a chunk of a split key tile: fp32 partials [dV | dKhat][row][D]
-                float *prow = kSplit && nc > 1
-                    ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D : nullptr;
-#pragma unroll
-                for (int cc = wg; cc < (kFuse ? 1 : 2) * (D / 32); cc += kSoftmaxWGs) {
-                    const bool isv = cc < D / 32;
-                    const int c = isv ? cc : cc - D / 32;
-                    uint32_t a[32];
-                    tmem_ld32_sync(tmem + (isv ? 256 : 384) + lane_off + 32 * c, a);
-                    if (kp < S && prow != nullptr) {
-                        const float sc = isv ? 1.f : scale;
-                        float *dst = prow + (isv ? 0 : (size_t)kTile * D) + 32 * c;
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4)
-                            *reinterpret_cast<float4 *>(dst + 4 * q4) =
-                                make_float4(__uint_as_float(a[q4 * 4 + 0]) * sc,
-                                            __uint_as_float(a[q4 * 4 + 1]) * sc,
-                                            __uint_as_float(a[q4 * 4 + 2]) * sc,
-                                            __uint_as_float(a[q4 * 4 + 3]) * sc);
-                    } else if (kp < S) {
-                        if (isv) {
-#pragma unroll
-                            for (int q8 = 0; q8 < 4; ++q8) {
-                                uint4 v4;
-                                v4.x = pack_bf16x2(__uint_as_float(a[q8 * 8 + 0]), __uint_as_float(a[q8 * 8 + 1]));
-                                v4.y = pack_bf16x2(__uint_as_float(a[q8 * 8 + 2]), __uint_as_float(a[q8 * 8 + 3]));
-                                v4.z = pack_bf16x2(__uint_as_float(a[q8 * 8 + 4]), __uint_as_float(a[q8 * 8 + 5]));
-                                v4.w = pack_bf16x2(__uint_as_float(a[q8 * 8 + 6]), __uint_as_float(a[q8 * 8 + 7]));
-                                *reinterpret_cast<uint4 *>(dvrow + 32 * c + 8 * q8) = v4;
-                            }
-                        } else {
-#pragma unroll
-                            for (int q4 = 0; q4 < 8; ++q4) {
-                                float4 f;
-                                f.x = __uint_as_float(a[q4 * 4 + 0]) * scale;
-                                f.y = __uint_as_float(a[q4 * 4 + 1]) * scale;
-                                f.z = __uint_as_float(a[q4 * 4 + 2]) * scale;
-                                f.w = __uint_as_float(a[q4 * 4 + 3]) * scale;
-                                *reinterpret_cast<float4 *>(dkrow + 32 * c + 4 * q4) = f;
-                            }
-                        }
-                    }
-                }
+                store_dkdv_acc<D, kSplit>(
+                    wg, tmem + lane_off, kp < S,
+                    dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D,
+                    dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D,
+                    kSplit && nc > 1
+                        ? part + ((size_t)bg * nw + witem) * 2 * kTile * D + (size_t)r * D
+                        : nullptr);
             }
         }
         if constexpr (kFuse) {
@@ -690,8 +722,9 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const uint8_t *sX = sStage + (x0 % HS) * C::kHStageBytes;
             const uint8_t *cs_row = sStage + ((x0 + 1 + (r >> 6)) % HS) * C::kHStageBytes +
                                     wg * kCsPieceBytes + (r & 63) * 128;
-            finish_rows<D>(ok, wg, quarter, lane, tmem + 384 + lane_off, sX, cs_row, kp < S, escr,
-                           dk + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D, pk);
+            finish_rows_dk<D>(ok, wg, quarter, lane, tmem + 384 + lane_off, sX, cs_row, kp < S,
+                              escr, dk + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D,
+                              pk);
         }
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
     }
@@ -970,8 +1003,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                                                  mbar_wait(&bars.st_full[T % ST], (T / ST) & 1,
                                                            abort_flag));
         const uint8_t *cs_row = sStage + (T % ST) * C::kStageBytes + wg * kTile * 128 + r * 128;
-        finish_rows<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
-                       dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D, part);
+        finish_rows_call<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
+                            dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D, part);
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
     }
     tc_fence_before();

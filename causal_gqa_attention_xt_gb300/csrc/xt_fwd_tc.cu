@@ -63,6 +63,32 @@ __device__ __forceinline__ void raise_error(unsigned int *err, volatile int *abo
     *abort_flag = 1;
 }
 
+// Epilogue of one query row: O / l from TMEM (this warp's lanes, columns
+// [tO, tO + D)) -> bf16 row `dst`; lse = (m + log2 l) ln 2. A separate
+// function, so that the softmax loop keeps its registers.
+template <int D>
+__device__ __noinline__ void write_out_row(uint32_t tO, float l, float m_used, bool row_ok,
+                                           bf16 *dst, float *lse_row) {
+    const float inv_l = 1.0f / l;
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32_sync(tO + c * 32, o);
+        if (row_ok) {
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+                uint4 v;
+                v.x = pack_bf16x2(__uint_as_float(o[q8 * 8 + 0]) * inv_l, __uint_as_float(o[q8 * 8 + 1]) * inv_l);
+                v.y = pack_bf16x2(__uint_as_float(o[q8 * 8 + 2]) * inv_l, __uint_as_float(o[q8 * 8 + 3]) * inv_l);
+                v.z = pack_bf16x2(__uint_as_float(o[q8 * 8 + 4]) * inv_l, __uint_as_float(o[q8 * 8 + 5]) * inv_l);
+                v.w = pack_bf16x2(__uint_as_float(o[q8 * 8 + 6]) * inv_l, __uint_as_float(o[q8 * 8 + 7]) * inv_l);
+                *reinterpret_cast<uint4 *>(dst + c * 32 + q8 * 8) = v;
+            }
+        }
+    }
+    if (row_ok) *lse_row = (m_used + __log2f(l)) * kLn2;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
 k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
@@ -303,27 +329,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             // epilogue: O / l -> bf16 rows of out [B, S, H, D]; lse = (m + log2 l) ln 2
             if (__all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (n - 1) & 1, abort_flag))) {
                 tc_fence_after();
-                const float inv_l = 1.0f / l;
                 const size_t row = (size_t)sp.plane * sr.S + sp.start + t;
-                bf16 *dst = out + (row * H + h) * D;
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32_sync(tO + c * 32, o);
-                    if (t < sp.len) {
-#pragma unroll
-                        for (int q8 = 0; q8 < 4; ++q8) {
-                            uint4 v;
-                            v.x = pack_bf16x2(__uint_as_float(o[q8 * 8 + 0]) * inv_l, __uint_as_float(o[q8 * 8 + 1]) * inv_l);
-                            v.y = pack_bf16x2(__uint_as_float(o[q8 * 8 + 2]) * inv_l, __uint_as_float(o[q8 * 8 + 3]) * inv_l);
-                            v.z = pack_bf16x2(__uint_as_float(o[q8 * 8 + 4]) * inv_l, __uint_as_float(o[q8 * 8 + 5]) * inv_l);
-                            v.w = pack_bf16x2(__uint_as_float(o[q8 * 8 + 6]) * inv_l, __uint_as_float(o[q8 * 8 + 7]) * inv_l);
-                            *reinterpret_cast<uint4 *>(dst + c * 32 + q8 * 8) = v;
-                        }
-                    }
-                }
-                if (t < sp.len)
-                    lse[(size_t)qplane * sr.S + sp.start + t] = (m_used + __log2f(l)) * kLn2;
+                write_out_row<D>(tO, l, m_used, t < sp.len, out + (row * H + h) * D,
+                                 lse + (size_t)qplane * sr.S + sp.start + t);
             } else {
                 ok = false;
             }
