@@ -646,10 +646,15 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            // statistics of the half: lse at [0,64), Dlt at [64,128)
+            // statistics of the half: lse at [0,64), Dlt at [64,128). Lane l takes
+            // column l's pair of this warpgroup's 32 columns (two conflict-free
+            // loads per warp); the others get them by shuffles, which leave the
+            // shared-memory banks to the MMA operands (broadcast 16-byte loads
+            // cost several bank wavefronts each).
             const float *sl = reinterpret_cast<const float *>(sStage + hs * C::kHStageBytes +
                                                               2 * C::kHalfBytes) +
                               32 * (wg & 1);
+            const float my_l = sl[lane], my_d = sl[64 + lane];
             const uint32_t tS = tmem + lane_off + c0;         // S^T columns
             const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
             // no masking when every query of these columns is at/after every owned key and < S
@@ -663,20 +668,18 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 auto body = [&](auto masked) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        const float4 l4 = *reinterpret_cast<const float4 *>(sl + e);
-                        const float4 d4 = *reinterpret_cast<const float4 *>(sl + 64 + e);
-                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-                        const float dlv[4] = {d4.x, d4.y, d4.z, d4.w};
                         float pv[4], dsv[4];
 #pragma unroll
                         for (int x = 0; x < 4; ++x) {
-                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lv[x]));
+                            const float lvx = __shfl_sync(0xffffffffu, my_l, e + x);
+                            const float dlx = __shfl_sync(0xffffffffu, my_d, e + x);
+                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lvx));
                             if constexpr (decltype(masked)::value) {
                                 const int q = q0 + e + x;
                                 if (!(q >= kp && q < S)) p = 0.f;
                             }
                             pv[x] = p;
-                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlv[x]);
+                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlx);
                         }
                         pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
                         pp[(e >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
