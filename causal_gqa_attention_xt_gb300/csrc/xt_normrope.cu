@@ -536,35 +536,37 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
 }
 
 // dgamma[d] = sum over partials p of part[p][d], in a fixed association:
-// slice s (of 32) sums p = s, s+32, s+64, ... in order, then slices 0..31 are
-// added in order. Block (x = 32-column group, y = q or k), 1024 threads.
+// slice s (of 128) sums p = s, s+128, s+256, ... in order, then slices
+// 0..127 are added in order. Block (x = 8-column group, y = q or k), 1024
+// threads: thread = (slice, column); a warp reads 4 partial rows x 32 bytes.
 __global__ void __launch_bounds__(1024)
 k_dgamma_reduce(const float *__restrict__ part_q, const float *__restrict__ part_k,
                 int nparts_q, int nparts_k, int D, float *__restrict__ dgq, float *__restrict__ dgk) {
-    __shared__ float red[32][33];
+    constexpr int kCols = 8, kSlices = 128;
+    __shared__ float red[kSlices][kCols + 1];
     const float *part = blockIdx.y == 0 ? part_q : part_k;
     const int nparts = blockIdx.y == 0 ? nparts_q : nparts_k;
     float *out = blockIdx.y == 0 ? dgq : dgk;
-    const int c = threadIdx.x & 31, slice = threadIdx.x >> 5;
-    const int d = blockIdx.x * 32 + c;
+    const int c = threadIdx.x % kCols, slice = threadIdx.x / kCols;
+    const int d = blockIdx.x * kCols + c;
     float sum = 0.f;
     if (d < D) {
         // eight loads in flight, added in the same order as one at a time
         int p = slice;
-        for (; p + 32 * 7 < nparts; p += 32 * 8) {
+        for (; p + kSlices * 7 < nparts; p += kSlices * 8) {
             float v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(p + 32 * u) * D + d];
+            for (int u = 0; u < 8; ++u) v[u] = part[(size_t)(p + kSlices * u) * D + d];
 #pragma unroll
             for (int u = 0; u < 8; ++u) sum += v[u];
         }
-        for (; p < nparts; p += 32) sum += part[(size_t)p * D + d];
+        for (; p < nparts; p += kSlices) sum += part[(size_t)p * D + d];
     }
     red[slice][c] = sum;
     __syncthreads();
     if (slice == 0 && d < D) {
         float total = 0.f;
-        for (int sl = 0; sl < 32; ++sl) total += red[sl][c];
+        for (int sl = 0; sl < kSlices; ++sl) total += red[sl][c];
         out[d] = total;
     }
 }
@@ -718,8 +720,8 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
 cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
                                  int nparts_q, int nparts_k, float *dgq, float *dgk,
                                  cudaStream_t st) {
-    k_dgamma_reduce<<<dim3((p.D + 31) / 32, 2), 1024, 0, st>>>(part_q, part_k, nparts_q, nparts_k,
-                                                               p.D, dgq, dgk);
+    k_dgamma_reduce<<<dim3((p.D + 7) / 8, 2), 1024, 0, st>>>(part_q, part_k, nparts_q, nparts_k,
+                                                             p.D, dgq, dgk);
     return cudaGetLastError();
 }
 
