@@ -511,8 +511,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int kq = lane + 32 * e, q = q0 + kq;
-                sl[kq] = q < S ? lse[row0 + q] * kLog2e : 0.f;
-                sl[64 + kq] = q < S ? dlt[row0 + q] : 0.f;
+                sl[kq] = q < S ? -lse[row0 + q] * kLog2e : 0.f;   // negated, for the f32x2 ops
+                sl[64 + kq] = q < S ? -dlt[row0 + q] : 0.f;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.st_full[hs]);
@@ -646,7 +646,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            // statistics of the half: lse at [0,64), Dlt at [64,128). Lane l takes
+            // statistics of the half: -lse (log2 units) at [0,64), -Dlt at [64,128). Lane l takes
             // column l's pair of this warpgroup's 32 columns (two conflict-free
             // loads per warp); the others get them by shuffles, which leave the
             // shared-memory banks to the MMA operands (broadcast 16-byte loads
@@ -668,23 +668,28 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 auto body = [&](auto masked) {
 #pragma unroll
                     for (int e = 0; e < 32; e += 4) {
-                        float pv[4], dsv[4];
+                        // column pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
 #pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            const float lvx = __shfl_sync(0xffffffffu, my_l, e + x);
-                            const float dlx = __shfl_sync(0xffffffffu, my_d, e + x);
-                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lvx));
+                        for (int x = 0; x < 4; x += 2) {
+                            const float2 nl = make_float2(__shfl_sync(0xffffffffu, my_l, e + x),
+                                                          __shfl_sync(0xffffffffu, my_l, e + x + 1));
+                            const float2 ndl = make_float2(__shfl_sync(0xffffffffu, my_d, e + x),
+                                                           __shfl_sync(0xffffffffu, my_d, e + x + 1));
+                            const float2 a = ffma2(make_float2(__uint_as_float(sv[e + x]),
+                                                               __uint_as_float(sv[e + x + 1])),
+                                                   make_float2(sl2, sl2), nl);
+                            float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
                             if constexpr (decltype(masked)::value) {
                                 const int q = q0 + e + x;
-                                if (!(q >= kp && q < S)) p = 0.f;
+                                if (!(q >= kp && q < S)) p.x = 0.f;
+                                if (!(q + 1 >= kp && q + 1 < S)) p.y = 0.f;
                             }
-                            pv[x] = p;
-                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dlx);
+                            const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e + x]),
+                                                                         __uint_as_float(dpv[e + x + 1])),
+                                                             ndl));
+                            pp[(e + x) >> 1] = pack_bf16x2(p.x, p.y);
+                            dd[(e + x) >> 1] = pack_bf16x2(ds.x, ds.y);
                         }
-                        pp[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-                        pp[(e >> 1) + 1] = pack_bf16x2(pv[2], pv[3]);
-                        dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
-                        dd[(e >> 1) + 1] = pack_bf16x2(dsv[2], dsv[3]);
                     }
                 };
                 if (interior) body(std::false_type{});
@@ -976,19 +981,23 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 tc_fence_before();
                 mbar_arrive(sdp_taken);                 // S(t+1) may now be issued
                 // only tiles that reach past the owned rows' diagonal take the select
+                // element pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
                 auto body = [&](auto masked) {
+                    const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2);
+                    const float2 ndl = make_float2(-dl, -dl);
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        float dsv[2];
-#pragma unroll
-                        for (int x = 0; x < 2; ++x) {
-                            float p = fast_exp2(fmaf(__uint_as_float(sv[e + x]), sl2, -lse2));
-                            if constexpr (decltype(masked)::value) {
-                                if (k0 + e + x > tq) p = 0.f;
-                            }
-                            dsv[x] = p * (__uint_as_float(dpv[e + x]) - dl);
+                        const float2 a = ffma2(make_float2(__uint_as_float(sv[e]),
+                                                           __uint_as_float(sv[e + 1])), sl2v, nl);
+                        float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                        if constexpr (decltype(masked)::value) {
+                            if (k0 + e > tq) p.x = 0.f;
+                            if (k0 + e + 1 > tq) p.y = 0.f;
                         }
-                        dd[e >> 1] = pack_bf16x2(dsv[0], dsv[1]);
+                        const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e]),
+                                                                     __uint_as_float(dpv[e + 1])),
+                                                         ndl));
+                        dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
                     }
                 };
                 if (interior) body(std::false_type{});

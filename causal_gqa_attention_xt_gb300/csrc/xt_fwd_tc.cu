@@ -306,20 +306,24 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                     tmem_st32_sync(tO + c * 32, o);
                 }
             }
-            const float neg_m = -m_used;
-            float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+            // element pairs through the packed fp32 pipe (f32x2 FMA / add)
+            const float2 nm2 = make_float2(-m_used, -m_used), sl2v = make_float2(sl2, sl2);
+            float2 rs01 = make_float2(0.f, 0.f), rs23 = make_float2(0.f, 0.f);
             uint32_t pk[64];
 #pragma unroll
             for (int e = 0; e < 128; e += 4) {
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sr[e]), sl2, neg_m));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sr[e + 1]), sl2, neg_m));
-                const float p2 = fast_exp2(fmaf(__uint_as_float(sr[e + 2]), sl2, neg_m));
-                const float p3 = fast_exp2(fmaf(__uint_as_float(sr[e + 3]), sl2, neg_m));
-                rs0 += p0; rs1 += p1; rs2 += p2; rs3 += p3;
-                pk[e >> 1] = pack_bf16x2(p0, p1);
-                pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
+                const float2 a01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                         sl2v, nm2);
+                const float2 a23 = ffma2(make_float2(__uint_as_float(sr[e + 2]),
+                                                     __uint_as_float(sr[e + 3])), sl2v, nm2);
+                const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
+                const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
+                rs01 = fadd2(rs01, p01);
+                rs23 = fadd2(rs23, p23);
+                pk[e >> 1] = pack_bf16x2(p01.x, p01.y);
+                pk[(e >> 1) + 1] = pack_bf16x2(p23.x, p23.y);
             }
-            const float rowsum = (rs0 + rs1) + (rs2 + rs3);
+            const float rowsum = (rs01.x + rs01.y) + (rs23.x + rs23.y);
             tmem_st64_sync(tS, pk);
             tc_fence_before();
             mbar_arrive(&bars.p_full[i]);

@@ -386,6 +386,38 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// Packed fp32 pair arithmetic (one f32x2 instruction for two lanes of data):
+// a * b + c, a * b and a + b, each element rounded as its scalar op would be.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 ra, ra, rb, rc;\n mov.b64 {%0, %1}, ra;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mul.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb;\n"
+        " mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 ra, ra, rb;\n mov.b64 {%0, %1}, ra;\n}\n"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // ------------------------------------------------------------------ descriptors
 // Shared-memory matrix descriptor (tcgen05): start address >> 4 in bits
 // [0,14), leading-dimension byte offset >> 4 in [16,30), stride-dimension
