@@ -77,15 +77,16 @@ typedef enum {
 /* Bytes of scratch the forward (backward = 0) or backward (backward != 0)
  * call needs for this problem; 0 on invalid arguments. The forward's scratch
  * is the RoPE table, S * head_dim/2 (cos, sin) fp32 pairs (rounded up to 256
- * bytes); the backward's holds that table too, plus Dlt [B, H, S], fp32
- * dKhat, fp32 dQhat (fp32 problems only: the bf16 dQ kernel finishes dq
- * itself), dgamma partials (1024 * head_dim floats for the k rows; for the q
- * rows as many again in fp32, or one head_dim row per (b, head, 128-row query
- * tile) in bf16) and, for bf16
- * problems whose key/value heads carry far more work than there are blocks
- * to share it (few kv heads and long sequences, e.g. MQA), fp32 partials of
- * the dK/dV tiles whose work is split over several thread blocks. The size
- * depends on the current device's SM count. */
+ * bytes); the backward's holds that table too, plus Dlt [B, H, S] and
+ * dgamma partial rows of head_dim floats. In fp32 it also holds fp32 dQhat
+ * and dKhat and 2 * 1024 partial rows. In bf16 the tensor-core kernels finish
+ * dq and dk themselves: one q partial row per (b, head, 128-row query tile)
+ * and one k partial row per (b, kv head, 128-row key tile); except that for
+ * problems whose key/value heads carry far more work than there are blocks to
+ * share it (few kv heads and long sequences, e.g. MQA) the dK/dV work of the
+ * longest key tiles is split over several thread blocks, and the scratch
+ * then holds their fp32 partials, fp32 dKhat and 1024 k partial rows. The
+ * size depends on the current device's SM count (which decides the split). */
 size_t xt_attn_workspace_bytes(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                                int dtype, int backward);
 
