@@ -214,7 +214,9 @@ int run_fwd(const Problem &p, const void *q, const void *k, const void *v, const
     });
 }
 
-// The backward pipeline: RoPE table, Dlt, dK/dV, dQ, epilogue, dgamma reduce.
+// The backward pipeline: RoPE table, Dlt, dK/dV (+ chunk reduce for split key
+// tiles), dQ, the row epilogue where the attention kernels do not finish the
+// rows themselves (fp32 problems; k rows of split bf16 problems), dgamma reduce.
 int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const float *gamma_q,
             const float *gamma_k, const void *out, const float *lse, const void *q_hat,
             const void *k_hat, const float *rstd_q, const float *rstd_k, const void *dout,
