@@ -141,6 +141,21 @@ def test_varlen_validation_rejects_before_launch(L, kw, code):
     assert _fwd_varlen(L, **kw) == code
 
 
+def test_bf16_backward_workspace_follows_the_dkdv_split(L):
+    # bf16: the tensor-core kernels finish dq and dk themselves, so no fp32 dQhat is kept and
+    # fp32 dKhat only where the dK/dV work of long key tiles is split (long MQA)
+    B, S, H, G, D = 4, 4096, 32, 8, 128
+    bf = xt.xt_attn_workspace_bytes(B, S, H, G, D, 1, True)
+    f32 = xt.xt_attn_workspace_bytes(B, S, H, G, D, 0, True)
+    dkhat = B * G * S * D * 4
+    assert 0 < bf < dkhat
+    assert f32 > B * H * S * D * 4 + dkhat
+    # table + Dlt + one dgamma_q row per (b, head, query tile) + one dgamma_k row per (b, kv head, key tile)
+    assert bf >= S * D // 2 * 8 + B * H * S * 4 + (B * H * 32 + B * G * 32) * D * 4
+    mqa = xt.xt_attn_workspace_bytes(1, 16384, 16, 1, D, 1, True)
+    assert mqa > 1 * 1 * 16384 * D * 4   # fp32 dKhat for the reduce and the k-row epilogue
+
+
 def test_varlen_workspace(L):
     fneed = xt.xt_attn_varlen_workspace_bytes(1000, 5, 300, 4, 2, 64, 1, False)
     bneed = xt.xt_attn_varlen_workspace_bytes(1000, 5, 300, 4, 2, 64, 1, True)
