@@ -198,6 +198,52 @@ def cpu_baseline(w, seconds_target=20.0):
             "sample": desc, "seconds": dt}
 
 
+def oracle_configs():
+    """The CPU oracle (fwd + bwd, fp64) timed on every configured workload on
+    this host's cores. The tiny fp32 and GQA bring-up shapes run whole, on one
+    thread and on all threads; the larger ones run a sample of one batch
+    element with as many query heads as there are threads (one head per
+    thread, whole kv groups, full sequence), and the whole config's time is
+    estimated from it by the number of such head waves. One JSON line per
+    workload."""
+    import math
+    import oracle
+    from causal_gqa_attention_xt_gb300.inputs import WORKLOADS, make_inputs, to_f64
+    oracle.build()
+    cores = host_cores()
+    for name in CONFIG_WORKLOADS:
+        w = WORKLOADS[name]
+        runs = []
+        if name in ("tiny_mha_f32", "gqa_bf16"):
+            x = to_f64(make_inputs(w))
+            for req in sorted({1, cores}):
+                threads = oracle.head_threads(req, w.S, 2, w.B * w.H)
+                t0 = time.perf_counter()
+                run_oracle_step(w, x, threads)
+                dt = time.perf_counter() - t0
+                runs.append({"threads": threads, "sample": "whole workload", "seconds": dt,
+                             "tflops": (w.fwd_flops + w.bwd_flops) / dt / 1e12,
+                             "est_full_seconds": dt})
+        else:
+            n_groups = max(1, min(w.G, cores // w.group))
+            sub = w.with_(B=1, H=n_groups * w.group, G=n_groups)
+            x = to_f64(make_inputs(sub))
+            threads = oracle.head_threads(min(cores, sub.H), sub.S, 2, sub.H)
+            t0 = time.perf_counter()
+            run_oracle_step(sub, x, threads)
+            dt = time.perf_counter() - t0
+            waves_sub = math.ceil(sub.H / threads)
+            waves_full = w.B * math.ceil(w.H / threads)
+            runs.append({"threads": threads,
+                         "sample": f"B=1, {sub.H} query heads / {sub.G} kv heads, S={w.S}",
+                         "seconds": dt, "tflops": (sub.fwd_flops + sub.bwd_flops) / dt / 1e12,
+                         "est_full_seconds": dt * waves_full / waves_sub})
+        print(json.dumps({"oracle_config": name, "B": w.B, "S": w.S, "n_heads": w.H,
+                          "n_kv_heads": w.G, "head_dim": w.D, "dtype_in": w.dtype,
+                          "arith": "f64", "host_cores": cores, "runs": runs}), flush=True)
+    return 0
+
+
 def longest_sample(w):
     """The longest sample of a packed batch as a one-element batched workload
     (what the oracle times for the packed mode's CPU numbers)."""
@@ -464,6 +510,10 @@ def bench_ours(args, w):
         "clocks": clk,
         "wall_s_timed_region": wall,
     }
+    if world == 1 and not packed and not args.no_configs:
+        # every configured workload, timed after the headline (outside its timed region)
+        line["configs"] = bench_configs(torch, xt, dev, flush, min(args.steps, 10),
+                                        max(3, min(args.warmup, 5)), peaks)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(longest_sample(w) if packed else w)
     if world > 1:
@@ -472,6 +522,87 @@ def bench_ours(args, w):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+# The workloads the attention core is specified on, timed beside the headline
+# (the tiny fp32 shape, GQA bring-up, dim768 MHA and GQA, Qwen3-like, long MQA)
+# plus the pages' own dim768 run (24 heads x 32 at S = 256).
+CONFIG_WORKLOADS = ("tiny_mha_f32", "gqa_bf16", "dim768_mha_bf16", "dim768_gqa_bf16",
+                    "qwen3_like_bf16", "mqa_long_bf16", "dim768_hd32_bf16")
+
+
+def bench_configs(torch, xt, dev, flush, steps, warmup, peaks):
+    """fwd / bwd / step times of every configured workload in this process: the
+    same calls, CUDA events on the launch stream and L2 flush between steps as
+    the headline; then a second pass with the library's per-launch events for
+    the per-kernel times (ms per launch). Inputs are seeded like the headline's."""
+    from causal_gqa_attention_xt_gb300.inputs import WORKLOADS, make_inputs
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in CONFIG_WORKLOADS:
+        w = WORKLOADS[name]
+        d = {k: v.to(dev) for k, v in make_inputs(w).items()}
+        code = 1 if w.dtype == "bf16" else 0
+        ws = torch.empty(max(16, xt.xt_attn_workspace_bytes(w.B, w.S, w.H, w.G, w.D, code, True)),
+                         device=dev, dtype=torch.uint8)
+        sv = xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
+                            workspace=ws)
+        gr = xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], sv, d["dout"],
+                            w.eps, w.theta, workspace=ws)
+
+        def fwd():
+            xt.xt_attn_fwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], w.eps, w.theta,
+                           workspace=ws, **sv)
+
+        def bwd():
+            xt.xt_attn_bwd(d["q"], d["k"], d["v"], d["gamma_q"], d["gamma_k"], sv, d["dout"],
+                           w.eps, w.theta, workspace=ws, **gr)
+
+        for _ in range(warmup):
+            flush.zero_()
+            fwd()
+            bwd()
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fwd()
+            ev[i][1].record(stream)
+            bwd()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        xt.xt_timing_reset()
+        xt.xt_timing_enable(True)
+        for i in range(steps):
+            flush.zero_()
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        xt.xt_timing_enable(False)
+        kern = {k: round(v[0] / v[1], 5) for k, v in xt.xt_timing_query().items() if v[1]}
+        if xt.xt_attn_check() != xt.XT_OK:
+            raise RuntimeError(f"device error flag raised while timing {name}")
+        f_ms = sum(a.elapsed_time(b) for a, b, _ in ev) / steps
+        b_ms = sum(b.elapsed_time(c) for _, b, c in ev) / steps
+
+        def rate(fl, ms):
+            return fl / (ms * 1e-3) / 1e12
+
+        res[name] = {
+            "B": w.B, "S": w.S, "n_heads": w.H, "n_kv_heads": w.G, "head_dim": w.D,
+            "dtype": w.dtype, "fwd_ms": f_ms, "bwd_ms": b_ms, "step_ms": f_ms + b_ms,
+            "fwd_tflops": rate(w.fwd_flops, f_ms), "bwd_tflops": rate(w.bwd_flops, b_ms),
+            "step_tflops": rate(w.fwd_flops + w.bwd_flops, f_ms + b_ms),
+            "step_frac_of_peak": rate(w.fwd_flops + w.bwd_flops, f_ms + b_ms) / peaks["tflops"],
+            "kernel_ms_per_launch": kern,
+        }
+        del d, ws, sv, gr
+    torch.cuda.empty_cache()
+    return {"steps": steps, "warmup": warmup,
+            "timing": "CUDA events per fwd / bwd call on the launch stream, L2 flushed between "
+                      "steps (512 MB write), inputs seeded like the headline's (seed 0)",
+            "peak_tflops": peaks["tflops"], "workloads": res}
 
 
 def pipelined_e2e(torch, steps, pin_in, dev_ins, compute, dev_outs, host_outs):
@@ -804,12 +935,18 @@ def main(argv=None):
                          "varlen: fwd+bwd over a packed batch of unequal samples")
     ap.add_argument("--workload", default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the per-workload timings that follow the headline (train mode)")
     ap.add_argument("--ref-seq", type=int, default=1024,
                     help="sequence length of the oracle's per-step sample (reference arm)")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size")
+    ap.add_argument("--oracle-configs", action="store_true",
+                    help="time the CPU oracle on every configured workload (host cores only)")
     ap.add_argument("--profile-run", action="store_true",
                     help="one warm-up and one fwd+bwd step, no timing (for ncu captures)")
     args = ap.parse_args(argv)
+    if args.oracle_configs:
+        return oracle_configs()
     from causal_gqa_attention_xt_gb300.inputs import PACKED_WORKLOADS, WORKLOADS
     if args.mode == "varlen":
         w = PACKED_WORKLOADS[args.workload or VARLEN_WORKLOAD]

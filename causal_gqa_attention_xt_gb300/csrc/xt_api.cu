@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -18,6 +19,7 @@ __device__ unsigned int g_error_word;
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<int> g_stall_mask{0};
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = (int)e;
@@ -293,6 +295,9 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
 }
 
 }  // namespace
+
+int test_stall_mask() { return g_stall_mask.load(std::memory_order_relaxed); }
+
 }  // namespace xt
 
 using namespace xt;
@@ -470,6 +475,12 @@ int xt_timing_query(int kernel_id, double *total_ms, long *launches) {
     drain_locked();
     *total_ms = g_timing.total_ms[kernel_id];
     *launches = g_timing.launches[kernel_id];
+    return XT_OK;
+}
+
+int xt_test_inject_stall(int kernel_mask) {
+    if (kernel_mask < 0 || (kernel_mask & ~STALL_ALL) != 0) return XT_EINVAL;
+    g_stall_mask.store(kernel_mask, std::memory_order_relaxed);
     return XT_OK;
 }
 

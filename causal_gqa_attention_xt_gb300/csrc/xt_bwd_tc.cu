@@ -110,6 +110,7 @@ struct BwdBarriers {
     uint64_t acc_done;
     uint64_t drain;
     uint64_t x_full;                 // dQ kernel: the owned rows of q are in shared memory
+    uint64_t stall;                  // never arrived on (xt_test_inject_stall)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -138,6 +139,7 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.x_full, 1);
+    mbar_init(&bars.stall, 1);
     fence_barrier_init();
 }
 
@@ -415,7 +417,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
               float *__restrict__ dkhat, bf16 *__restrict__ dv, float *__restrict__ part,
               const float *__restrict__ gamma_k, const float *__restrict__ rstd_k,
               bf16 *__restrict__ dk, float *__restrict__ part_k, const SeqRows sr, int H, int G,
-              int n_kvt, int chunk, int nw, unsigned int *err) {
+              int n_kvt, int chunk, int nw, unsigned int *err, int stall) {
     using C = BwdCfg<D>;
     constexpr int HS = C::kHStages;
     constexpr bool kFuse = !kSplit;
@@ -584,9 +586,10 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                            dDOk0 + so + kmajor_off_half<D>(kk), idesc_s, kk > 0);
                 mma_commit(&bars.s_full[h]);
             };
-            bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
-                      mbar_wait(&bars.st_full[0], 0, abort_flag) &&
-                      mbar_wait(&bars.st_full[1], 0, abort_flag);   // both halves of tile 0
+            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
+            ok = ok && mbar_wait(&bars.own_full, 0, abort_flag) &&
+                 mbar_wait(&bars.st_full[0], 0, abort_flag) &&
+                 mbar_wait(&bars.st_full[1], 0, abort_flag);   // both halves of tile 0
             if (ok) {
                 tc_fence_after();
                 issue_sp(0, 0);
@@ -783,7 +786,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const float *__restrict__ lse, const float *__restrict__ dlt,
             const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
             bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
-            int n_qt, unsigned int *err) {
+            int n_qt, unsigned int *err, int stall) {
     using C = BwdCfg<D>;
     constexpr int ST = C::kStages;
     // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), and the
@@ -892,8 +895,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                            kk > 0);
                 mma_commit(&bars.s_full[0]);         // S and dP of tile t are in TMEM
             };
-            bool ok = mbar_wait(&bars.own_full, 0, abort_flag) &&
-                      mbar_wait(&bars.st_full[0], 0, abort_flag);
+            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
+            ok = ok && mbar_wait(&bars.own_full, 0, abort_flag) &&
+                 mbar_wait(&bars.st_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -1160,7 +1164,7 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
     kern<<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
         m.k, m.v, m.q, m.dout, mx, mcs, lse, dlt, dkhat, (bf16 *)dv, part, ek.gamma, ek.rstd,
         (bf16 *)ek.out, ek.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, pl.n_kvt, pl.chunk,
-        pl.nw, err);
+        pl.nw, err, (test_stall_mask() & STALL_DKDV_TC) != 0);
     return cudaGetLastError();
 }
 
@@ -1179,7 +1183,8 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
         m.k, m.v, mx, mcs, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, ep.gamma,
-        ep.rstd, (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err);
+        ep.rstd, (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err,
+        (test_stall_mask() & STALL_DQ_TC) != 0);
     return cudaGetLastError();
 }
 

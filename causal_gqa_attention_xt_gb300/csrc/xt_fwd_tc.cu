@@ -54,6 +54,7 @@ struct FwdBarriers {
     uint64_t k_full[4], v_full[4], kv_empty[4];
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t drain;
+    uint64_t stall;   // never arrived on (xt_test_inject_stall)
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(kThreadsFwd, 1)
 k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
          const __grid_constant__ CUtensorMap map_v, bf16 *__restrict__ out,
          float *__restrict__ lse, const SeqRows sr, int H, int G, int n_pairs,
-         unsigned int *err) {
+         unsigned int *err, int stall) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBarriers bars;
@@ -133,6 +134,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             mbar_init(&bars.o_done[i], 1);
         }
         mbar_init(&bars.drain, 1);
+        mbar_init(&bars.stall, 1);
         fence_barrier_init();
     }
     if (warp == 9) {
@@ -212,8 +214,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                 }
                 mma_commit(&bars.s_full[i]);
             };
-            bool ok = mbar_wait(&bars.q_full, 0, abort_flag) &&
-                      mbar_wait(&bars.k_full[0], 0, abort_flag);
+            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
+            ok = ok && mbar_wait(&bars.q_full, 0, abort_flag) &&
+                 mbar_wait(&bars.k_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
                 for (int i = 0; i < 2; ++i)
@@ -384,7 +387,8 @@ cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     k_fwd_tc<D><<<(unsigned)blocks, kThreadsFwd, C::kSmemBytes, st>>>(
-        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_pairs, err);
+        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_pairs, err,
+        (test_stall_mask() & STALL_FWD_TC) != 0);
     return cudaGetLastError();
 }
 

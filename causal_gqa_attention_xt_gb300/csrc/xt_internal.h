@@ -48,6 +48,11 @@ struct Problem {
 // with every sample at most max_len rows.
 enum : unsigned int { ERR_TIMEOUT = 1u, ERR_BADPOS = 2u, ERR_BADSEQ = 4u };
 
+// Kernels that xt_test_inject_stall can make stall (bit mask), and the mask
+// currently set (0 in normal operation).
+enum : int { STALL_FWD_TC = 1, STALL_DKDV_TC = 2, STALL_DQ_TC = 4, STALL_ALL = 7 };
+int test_stall_mask();
+
 // ---- norm / RoPE kernels (xt_normrope.cu) ----
 // Persistent grids: at most this many CTAs, which bounds the number of
 // per-CTA dgamma partials the backward epilogue writes.

@@ -63,8 +63,12 @@ extern "C" int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, in
     void *scratch = nullptr;
     const int st = static_scratch_address(&scratch);
     if (st != XT_OK) return st;
-    // Every region of the backward's scratch is written before it is read, so
-    // the array needs no clearing between calls.
+    // On a call that completes normally every region of the backward's scratch
+    // is written before it is read, so the array needs no clearing between
+    // calls. A call whose bounded waits run out (xt_attn_check() reports
+    // XT_ETIMEOUT) stops writing partway: a later kernel of that call may then
+    // read the previous call's scratch, and every output of that call (dq, dk,
+    // dv, dgamma_q, dgamma_k) is unspecified.
     return xt_attn_bwd(B, S, n_heads, n_kv_heads, head_dim, eps, theta, q, k, v, gamma_q, gamma_k,
                        dtype, out, lse, q_hat, k_hat, rstd_q, rstd_k, dout, dq, dk, dv, dgamma_q,
                        dgamma_k, scratch, kStaticScratchBytes, stream);

@@ -53,18 +53,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // ~kWaitLimitNs (or as soon as *abort is set) and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 255u) == 0) {
             if (abort_flag && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+    return mbar_wait_for(bar, parity, abort_flag, kWaitLimitNs);
+}
+
+// Fault injection for the timeout path (xt_test_inject_stall): a kernel told to
+// stall makes its MMA-issuing thread wait, before its first MMA, on a barrier
+// that nothing arrives on, for this long; the wait runs out and the CTA takes
+// the regular timeout path (error word, abort flag, drain, TMEM freed).
+constexpr uint64_t kStallLimitNs = 20000000ull;   // 20 ms
 
 // Bounded wait whose polls carry a suspend-time hint: a thread whose phase is
 // not complete is parked by the hardware until the phase completes or about

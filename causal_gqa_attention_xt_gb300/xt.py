@@ -76,6 +76,8 @@ def lib():
     L.xt_timing_enable.argtypes = [i]
     L.xt_timing_query.argtypes = [i, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_long)]
     L.xt_kernel_count.restype = i
+    L.xt_test_inject_stall.argtypes = [i]
+    L.xt_test_inject_stall.restype = i
     L.xt_kernel_name.argtypes = [i]
     L.xt_kernel_name.restype = ctypes.c_char_p
     _lib = L
@@ -319,6 +321,16 @@ def xt_attn_check(stream=None) -> int:
 
 
 # ---- per-launch timing hooks -------------------------------------------
+
+STALL_FWD_TC, STALL_DKDV_TC, STALL_DQ_TC = 1, 2, 4
+
+
+def xt_test_inject_stall(kernel_mask: int) -> int:
+    """Fault injection for the timeout path (see include/xt_attn.h): the
+    tensor-core kernels in kernel_mask stall until their bounded wait runs
+    out; 0 turns it off."""
+    return lib().xt_test_inject_stall(int(kernel_mask))
+
 
 def xt_timing_enable(on: bool = True):
     lib().xt_timing_enable(int(bool(on)))

@@ -132,9 +132,14 @@ int xt_attn_bwd(int B, int S, int n_heads, int n_kv_heads, int head_dim,
  *    (cudaGetSymbolAddress, on the current device); make that first call
  *    before any stream capture begins.
  *  - All calls share the one array, which keeps the previous call's contents
- *    (the backward writes every scratch byte it reads, so nothing needs
- *    clearing). Calls whose GPU work overlaps in time -- on different streams,
- *    or from different host threads -- race on the array: serialize them. */
+ *    (a call that completes writes every scratch byte it reads, so nothing
+ *    needs clearing). Calls whose GPU work overlaps in time -- on different
+ *    streams, or from different host threads -- race on the array: serialize
+ *    them.
+ *  - After a call that xt_attn_check() reports as XT_ETIMEOUT, the contents of
+ *    dq, dk, dv, dgamma_q and dgamma_k are unspecified (a kernel that gave up
+ *    leaves its part of the scratch unwritten, and a later one may read the
+ *    previous call's). */
 int xt_attn_bwd_noalloc(int B, int S, int n_heads, int n_kv_heads, int head_dim,
                         double eps, double theta,
                         const void *q, const void *k, const void *v,
@@ -247,6 +252,23 @@ int xt_timing_reset(void);
 int xt_timing_query(int kernel_id, double *total_ms, long *launches);
 int xt_kernel_count(void);
 const char *xt_kernel_name(int kernel_id);
+
+/* Fault injection for the timeout path, for tests. The pages have no
+ * counterpart; it exercises what the Mint project report 9.7 (error
+ * handling) asks of GPU failures: they surface at a check point as an error
+ * and are neither swallowed nor left to hang the process. kernel_mask selects bf16
+ * tensor-core kernels: 1 the forward attention, 2 the dK/dV kernel, 4 the dQ
+ * kernel (0 = off, the default). Each CTA of a selected kernel launched while
+ * the mask is set makes its MMA-issuing thread wait, before its first MMA, on
+ * a barrier that nothing arrives on; after 20 ms the wait gives up and the CTA
+ * takes the same path as any timed-out wait: it raises the device error word,
+ * sets its abort flag so that its other warps stop waiting, lets every copy
+ * and MMA it issued land, frees its tensor memory and exits. The call that
+ * launched it returns XT_OK (the work was enqueued); xt_attn_check() then
+ * reports XT_ETIMEOUT and clears the word, and that call's outputs are
+ * unspecified. The mask is process-wide and read at launch time. Returns
+ * XT_EINVAL for bits outside 1|2|4. */
+int xt_test_inject_stall(int kernel_mask);
 
 #ifdef __cplusplus
 }

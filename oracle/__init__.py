@@ -108,6 +108,31 @@ def default_threads() -> int:
         return max(1, os.cpu_count() or 1)
 
 
+def host_available_bytes():
+    """MemAvailable of the host (bytes), or None where /proc/meminfo is absent."""
+    try:
+        with open("/proc/meminfo") as f:
+            for ln in f:
+                if ln.startswith("MemAvailable:"):
+                    return int(ln.split()[1]) * 1024
+    except (OSError, ValueError, IndexError):
+        pass
+    return None
+
+
+def head_threads(nthreads, S, n_square, n_heads):
+    """Thread count for a whole-head call: each thread holds n_square [S, S]
+    fp64 buffers, so the count is capped to keep them within half of the
+    host's available memory (the results do not depend on the count)."""
+    n = int(nthreads or default_threads())
+    n = max(1, min(n, int(n_heads)))
+    avail = host_available_bytes()
+    if avail is not None:
+        per_thread = n_square * 8 * int(S) * int(S) + (1 << 20)
+        n = max(1, min(n, int(0.5 * avail // per_thread)))
+    return n
+
+
 def _f64(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
 
@@ -216,7 +241,7 @@ def attn_fwd(q, k, v, gamma_q, gamma_k, eps, theta, nthreads=None):
     rk = np.empty((B, S, G))
     rc = _load().orc_attn_fwd(B, S, H, G, D, float(eps), float(theta), _p(q), _p(k), _p(v),
                               _p(gq), _p(gk), _p(out), _p(lse), _p(qhat), _p(khat), _p(rq),
-                              _p(rk), int(nthreads or default_threads()))
+                              _p(rk), head_threads(nthreads, S, 1, B * H))
     if rc:
         raise ValueError("oracle: invalid shape")
     return dict(out=out, lse=lse, qhat=qhat, khat=khat, rstd_q=rq, rstd_k=rk)
@@ -237,7 +262,7 @@ def attn_bwd(q, k, v, gamma_q, gamma_k, dout, eps, theta, nthreads=None):
     dgk = np.empty(D)
     rc = _load().orc_attn_bwd(B, S, H, G, D, float(eps), float(theta), _p(q), _p(k), _p(v),
                               _p(gq), _p(gk), _p(do), _p(dq), _p(dk), _p(dv), _p(dgq), _p(dgk),
-                              int(nthreads or default_threads()))
+                              head_threads(nthreads, S, 2, B * H))
     if rc:
         raise ValueError("oracle: invalid shape")
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgq, dgamma_k=dgk)
@@ -268,7 +293,7 @@ def attn_fwd_packed(q, k, v, gamma_q, gamma_k, cu_seqlens, eps, theta, nthreads=
     rc = _load().orc_attn_fwd_packed(len(cu) - 1, _lp(cu), H, G, D, float(eps), float(theta),
                                      _p(q), _p(k), _p(v), _p(gq), _p(gk), _p(out), _p(lse),
                                      _p(qhat), _p(khat), _p(rq), _p(rk),
-                                     int(nthreads or default_threads()))
+                                     head_threads(nthreads, T, 1, H))
     if rc:
         raise ValueError("oracle: invalid shape or offsets")
     return dict(out=out, lse=lse, qhat=qhat, khat=khat, rstd_q=rq, rstd_k=rk)
@@ -289,7 +314,7 @@ def attn_bwd_packed(q, k, v, gamma_q, gamma_k, cu_seqlens, dout, eps, theta, nth
     dgk = np.empty(D)
     rc = _load().orc_attn_bwd_packed(len(cu) - 1, _lp(cu), H, G, D, float(eps), float(theta),
                                      _p(q), _p(k), _p(v), _p(gq), _p(gk), _p(do), _p(dq), _p(dk),
-                                     _p(dv), _p(dgq), _p(dgk), int(nthreads or default_threads()))
+                                     _p(dv), _p(dgq), _p(dgk), head_threads(nthreads, T, 2, H))
     if rc:
         raise ValueError("oracle: invalid shape or offsets")
     return dict(dq=dq, dk=dk, dv=dv, dgamma_q=dgq, dgamma_k=dgk)

@@ -173,3 +173,11 @@ def test_varlen_workspace(L):
     bad = list(args)
     bad[2] = 0
     assert L.xt_attn_bwd_varlen(*bad, p, need, None) == xt.XT_EINVAL
+
+
+def test_stall_injection_mask_validation(L):
+    # the fault-injection hook of the timeout path takes kernel bits 1|2|4 only
+    assert L.xt_test_inject_stall(8) == 1
+    assert L.xt_test_inject_stall(-1) == 1
+    assert L.xt_test_inject_stall(7) == 0
+    assert L.xt_test_inject_stall(0) == 0

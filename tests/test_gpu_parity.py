@@ -3,10 +3,10 @@ same seeded inputs.
 
 Bars: max relative error (max |g - r| / max |r|) <= 1e-4 for fp32 and 2e-2
 for bf16 per output tensor, and the same argmax along every output row
-(near-ties excepted). Small shapes are compared element by element on every
-output; the full-size workloads are compared on exact sub-problems (one batch
-element and one key/value group form an independent problem), on rows the
-oracle computes one by one, and through sum rules that hold at any size.
+(near-ties excepted). Every workload (small shapes, dim768, Qwen3-like, long
+MQA) is compared element by element on every output against the whole
+oracle; the 2^21-position case, too long for the oracle's [S, S] matrices, is
+compared on rows the oracle computes one by one.
 """
 import numpy as np
 import pytest
@@ -123,6 +123,31 @@ def test_late_dominant_keys_force_running_max_jumps(dtype, D):
     compare_all(w, f, g, rf, rg)
 
 
+def _bf16_round(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy()
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_large_scores_bf16_against_the_oracle_with_bf16_hat_rows(D):
+    """bf16 with gammas near 3 (scores up to ~9 sqrt(D), ~100 at D = 128) and the
+    late-key construction above: running maxima jump by tens of log2 units past
+    the lazy-rescale threshold while every score is large. At these magnitudes
+    the bf16 storage of Q-hat and K-hat that the precision table of xtrain
+    "Phase T12" prescribes moves single probabilities by more than 2e-2, so the
+    reference is the oracle composed from its steps with its own Q-hat/K-hat
+    rounded to bf16 where the GPU stores them (tests/oracle_steps.py); every
+    other step stays in double, and the bar stays 2e-2 with the argmax rule."""
+    w = Workload(f"large_scores_bf16_d{D}", 1, 600, 4, 2, D, 1e4, 1e-5, "bf16", seed=8)
+    cpu = make_inputs(w, gamma_offset=3.0, gamma_scale=0.3)
+    u = cpu["q"][0, 0, 0].clone()
+    cpu["q"][:, ::2] = u                      # every other query row is u
+    cpu["k"][:, 256:] = u                     # late keys equal to it
+    f, g = run_gpu(w, cpu)
+    import oracle_steps
+    rf, rg = oracle_steps.forward_backward(to_f64(cpu), w.eps, w.theta, round_hat=_bf16_round)
+    compare_all(w, f, g, rf, rg)
+
+
 def test_forward_and_backward_are_bitwise_deterministic():
     w = WORKLOADS["gqa_bf16"]
     cpu = make_inputs(w)
@@ -169,83 +194,28 @@ def test_dim768_full_oracle(name):
     compare_all(w, f, g, rf, rg)
 
 
-def _sub_problem(x: dict, b: int, kvh: int, group: int):
-    """Inputs of one (batch element, kv group): an independent problem."""
-    hs = slice(kvh * group, (kvh + 1) * group)
-    return dict(q=x["q"][b:b + 1, :, hs], k=x["k"][b:b + 1, :, kvh:kvh + 1],
-                v=x["v"][b:b + 1, :, kvh:kvh + 1], dout=x["dout"][b:b + 1, :, hs],
-                gamma_q=x["gamma_q"], gamma_k=x["gamma_k"])
+def _gpu_to_host(f, g):
+    """The GPU results on the host (frees their device memory before the oracle runs)."""
+    f = {k: v.cpu() for k, v in f.items()}
+    g = {k: v.cpu() for k, v in g.items()}
+    torch.cuda.empty_cache()
+    return f, g
 
 
-def test_qwen3_like_full_size_sub_problem_and_rows():
-    w = WORKLOADS["qwen3_like_bf16"]
-    tol = TOL[w.dtype]
+@pytest.mark.parametrize("name", ["qwen3_like_bf16", "mqa_long_bf16"])
+def test_full_size_oracle_every_output(name):
+    """The Qwen3-like and the long-context MQA workloads at full size against the
+    whole oracle, element by element on every output (out, lse, q_hat, k_hat,
+    rstd_q, rstd_k, dq, dk, dv, dgamma_q, dgamma_k) with the argmax rule. At the
+    MQA shape the early key tiles go through the split dK/dV path (chunk
+    partials, their reduce and the separate k-row epilogue); dgamma sums
+    4096 x 32 + 4096 x 8 rows per batch element (Qwen3-like) and
+    16384 x 17 rows (MQA)."""
+    w = WORKLOADS[name]
     cpu = make_inputs(w)
-    f, g = run_gpu(w, cpu)
-    x = to_f64(cpu)
-    b, kvh = 3, 5
-    sub = _sub_problem(x, b, kvh, w.group)
-    ws = w.with_(B=1, H=w.group, G=1)
-    rf, rg = oracle_full(ws, sub)
-    hs = slice(kvh * w.group, (kvh + 1) * w.group)
-    assert_close("out", f["out"][b:b + 1, :, hs], rf["out"], tol)
-    assert_close("lse", f["lse"][b:b + 1, hs], rf["lse"], tol)
-    assert_close("dq", g["dq"][b:b + 1, :, hs], rg["dq"], tol)
-    assert_close("dk", g["dk"][b:b + 1, :, kvh:kvh + 1], rg["dk"], tol)
-    assert_close("dv", g["dv"][b:b + 1, :, kvh:kvh + 1], rg["dv"], tol)
-    # rows elsewhere, spread over batch, heads and tiles
-    rng = np.random.default_rng(0)
-    rows = [(int(rng.integers(w.B)), int(rng.integers(w.H)), int(t))
-            for t in rng.integers(0, w.S, size=24)] + [(0, 0, 0), (1, 31, w.S - 1)]
-    o, lse = oracle.attn_fwd_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], w.eps,
-                                  w.theta, rows)
-    dq = oracle.attn_dq_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
-                             w.eps, w.theta, rows)
-    go = np.stack([as_f64(f["out"][bb, t, h]) for bb, h, t in rows])
-    glse = np.array([float(f["lse"][bb, h, t]) for bb, h, t in rows])
-    gdq = np.stack([as_f64(g["dq"][bb, t, h]) for bb, h, t in rows])
-    assert max_rel_err(go, o) <= tol
-    assert max_rel_err(glse, lse) <= tol
-    assert max_rel_err(gdq, dq) <= tol
-    krows = [(0, 0, w.S - 1), (2, 7, w.S - 130), (1, 3, w.S - 300)]
-    dk, dv = oracle.attn_dkdv_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
-                                   w.eps, w.theta, krows)
-    gdk = np.stack([as_f64(g["dk"][bb, j, gg]) for bb, gg, j in krows])
-    gdv = np.stack([as_f64(g["dv"][bb, j, gg]) for bb, gg, j in krows])
-    assert max_rel_err(gdk, dk) <= tol
-    assert max_rel_err(gdv, dv) <= tol
-
-
-def test_mqa_long_full_size_rows_and_sum_rule():
-    w = WORKLOADS["mqa_long_bf16"]
-    tol = TOL[w.dtype]
-    cpu = make_inputs(w)
-    f, g = run_gpu(w, cpu)
-    x = to_f64(cpu)
-    rng = np.random.default_rng(1)
-    rows = [(0, int(rng.integers(w.H)), int(t)) for t in rng.integers(0, w.S, size=20)]
-    rows += [(0, 0, 0), (0, 15, w.S - 1), (0, 7, 8191)]
-    o, lse = oracle.attn_fwd_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], w.eps,
-                                  w.theta, rows)
-    dq = oracle.attn_dq_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
-                             w.eps, w.theta, rows)
-    go = np.stack([as_f64(f["out"][0, t, h]) for _, h, t in rows])
-    glse = np.array([float(f["lse"][0, h, t]) for _, h, t in rows])
-    gdq = np.stack([as_f64(g["dq"][0, t, h]) for _, h, t in rows])
-    assert max_rel_err(go, o) <= tol
-    assert max_rel_err(glse, lse) <= tol
-    assert max_rel_err(gdq, dq) <= tol
-    krows = [(0, 0, w.S - 1), (0, 0, w.S - 60)]
-    dk, dv = oracle.attn_dkdv_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
-                                   w.eps, w.theta, krows)
-    gdk = np.stack([as_f64(g["dk"][0, j, 0]) for _, _, j in krows])
-    gdv = np.stack([as_f64(g["dv"][0, j, 0]) for _, _, j in krows])
-    assert max_rel_err(gdk, dk) <= tol
-    assert max_rel_err(gdv, dv) <= tol
-    # rows of P sum to one, so summed over positions dV equals the group's summed dO
-    dv_total = as_f64(g["dv"])[0, :, 0].sum(0)
-    do_total = x["dout"][0].sum((0, 1))
-    assert max_rel_err(dv_total, do_total) <= tol
+    f, g = _gpu_to_host(*run_gpu(w, cpu))
+    rf, rg = oracle_full(w, to_f64(cpu))
+    compare_all(w, f, g, rf, rg)
 
 
 def test_positions_past_two_to_the_21():
@@ -272,13 +242,13 @@ def test_positions_past_two_to_the_21():
     go = np.stack([as_f64(f["out"][0, t, 0]) for _, _, t in rows])
     glse = np.array([float(f["lse"][0, 0, t]) for _, _, t in rows])
     gdq = np.stack([as_f64(g["dq"][0, t, 0]) for _, _, t in rows])
-    assert max_rel_err(go, o) <= tol
-    assert max_rel_err(glse, lse) <= tol
-    assert max_rel_err(gdq, dq) <= tol
+    assert_close("out rows", go, o, tol)
+    assert_close("lse rows", glse, lse, tol)
+    assert_close("dq rows", gdq, dq, tol)
     krows = [(0, 0, S - 1), (0, 0, (1 << 21) + 10)]
     dk, dv = oracle.attn_dkdv_rows(x["q"], x["k"], x["v"], x["gamma_q"], x["gamma_k"], x["dout"],
                                    w.eps, w.theta, krows)
     gdk = np.stack([as_f64(g["dk"][0, j, 0]) for _, _, j in krows])
     gdv = np.stack([as_f64(g["dv"][0, j, 0]) for _, _, j in krows])
-    assert max_rel_err(gdk, dk) <= tol
-    assert max_rel_err(gdv, dv) <= tol
+    assert_close("dk rows", gdk, dk, tol)
+    assert_close("dv rows", gdv, dv, tol)

@@ -342,3 +342,35 @@ def test_oracle_rejects_bad_shapes():
     q, k, v, do, gq, gk = _problem(1, 4, 3, 2, 8, seed=19)  # 3 % 2 != 0
     with pytest.raises(ValueError):
         oracle.attn_fwd(q, k, v, gq, gk, 1e-5, 1e4)
+
+
+def test_step_composition_equals_whole_pipeline_bitwise():
+    # tests/oracle_steps.py composes the oracle's single steps (used, with a bf16
+    # rounding of Q-hat and K-hat, by the large-score GPU stress test); without the
+    # rounding it must reproduce the whole-pipeline oracle exactly
+    import oracle_steps
+    B, S, H, G, D = 2, 19, 6, 2, 8
+    q, k, v, do, gq, gk = _problem(B, S, H, G, D, seed=20)
+    eps, theta = 1e-5, 1e4
+    x = dict(q=q, k=k, v=v, dout=do, gamma_q=gq, gamma_k=gk)
+    cf, cg = oracle_steps.forward_backward(x, eps, theta)
+    f = oracle.attn_fwd(q, k, v, gq, gk, eps, theta)
+    g = oracle.attn_bwd(q, k, v, gq, gk, do, eps, theta)
+    for key in f:
+        assert np.array_equal(cf[key], f[key]), key
+    for key in g:
+        assert np.array_equal(cg[key], g[key]), key
+
+
+def test_step_composition_rounding_reaches_the_attention():
+    # the rounding hook acts between the prologue and the attention: rounding
+    # Q-hat/K-hat to a coarse grid changes out, and the identity leaves it alone
+    import oracle_steps
+    q, k, v, do, gq, gk = _problem(1, 9, 2, 1, 8, seed=21)
+    x = dict(q=q, k=k, v=v, dout=do, gamma_q=gq, gamma_k=gk)
+    base, _ = oracle_steps.forward_backward(x, 1e-5, 1e4)
+    same, _ = oracle_steps.forward_backward(x, 1e-5, 1e4, round_hat=lambda a: a.copy())
+    coarse, _ = oracle_steps.forward_backward(x, 1e-5, 1e4, round_hat=lambda a: np.round(a, 1))
+    assert np.array_equal(same["out"], base["out"])
+    assert np.array_equal(coarse["qhat"], np.round(base["qhat"], 1))
+    assert not np.allclose(coarse["out"], base["out"], rtol=1e-6, atol=0)
