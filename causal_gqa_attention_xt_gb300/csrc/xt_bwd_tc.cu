@@ -649,49 +649,53 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            // statistics of the half: -lse (log2 units) at [0,64), -Dlt at [64,128). Lane l takes
-            // column l's pair of this warpgroup's 32 columns (two conflict-free
-            // loads per warp); the others get them by shuffles, which leave the
-            // shared-memory banks to the MMA operands (broadcast 16-byte loads
-            // cost several bank wavefronts each).
+            // statistics of the half: -lse (log2 units) at [0,64), -Dlt at [64,128), this
+            // warpgroup's 32 columns from 32 (wg & 1)
             const float *sl = reinterpret_cast<const float *>(sStage + hs * C::kHStageBytes +
                                                               2 * C::kHalfBytes) +
                               32 * (wg & 1);
-            const float my_l = sl[lane], my_d = sl[64 + lane];
             const uint32_t tS = tmem + lane_off + c0;         // S^T columns
             const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
             // no masking when every query of these columns is at/after every owned key and < S
             const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + kWgCols <= S);
+            // 16-lane TMEM shapes (xt_tc.cuh): this thread holds rows
+            // 16 L + lane/4 + 8 jh of its warp's 32 and the column pairs 8 k + 2 (lane % 4)
+            // of the warpgroup's 32, so it needs the statistics of 8 columns only: one
+            // 8-byte load per pair, 4 distinct conflict-free addresses per warp.
             uint32_t pp[kWgCols / 2], dd[kWgCols / 2];
             {
                 uint32_t sv[32], dpv[32];
-                tmem_ld32x2_sync(tS, sv, tP, dpv);
+                tmem_ld16x256b_x4_rows32_pair_sync(tS, sv, tP, dpv);
+                const int cp = 2 * (lane & 3);
                 // masked columns (the diagonal tile, the ragged end) take the select;
                 // interior tiles (all but about one in n_q) run without it
                 auto body = [&](auto masked) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        // column pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 nl = *reinterpret_cast<const float2 *>(sl + 8 * k + cp);
+                        const float2 ndl = *reinterpret_cast<const float2 *>(sl + 64 + 8 * k + cp);
 #pragma unroll
-                        for (int x = 0; x < 4; x += 2) {
-                            const float2 nl = make_float2(__shfl_sync(0xffffffffu, my_l, e + x),
-                                                          __shfl_sync(0xffffffffu, my_l, e + x + 1));
-                            const float2 ndl = make_float2(__shfl_sync(0xffffffffu, my_d, e + x),
-                                                           __shfl_sync(0xffffffffu, my_d, e + x + 1));
-                            const float2 a = ffma2(make_float2(__uint_as_float(sv[e + x]),
-                                                               __uint_as_float(sv[e + x + 1])),
-                                                   make_float2(sl2, sl2), nl);
-                            float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                            if constexpr (decltype(masked)::value) {
-                                const int q = q0 + e + x;
-                                if (!(q >= kp && q < S)) p.x = 0.f;
-                                if (!(q + 1 >= kp && q + 1 < S)) p.y = 0.f;
+                        for (int L = 0; L < 2; ++L) {
+#pragma unroll
+                            for (int jh = 0; jh < 2; ++jh) {
+                                // column pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
+                                const int e = 16 * L + 4 * k + 2 * jh;
+                                const float2 a = ffma2(make_float2(__uint_as_float(sv[e]),
+                                                                   __uint_as_float(sv[e + 1])),
+                                                       make_float2(sl2, sl2), nl);
+                                float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                                if constexpr (decltype(masked)::value) {
+                                    const int q = q0 + 8 * k + cp;
+                                    const int kr = j * kTile + quarter * 32 + 16 * L + (lane >> 2) + 8 * jh;
+                                    if (!(q >= kr && q < S)) p.x = 0.f;
+                                    if (!(q + 1 >= kr && q + 1 < S)) p.y = 0.f;
+                                }
+                                const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e]),
+                                                                             __uint_as_float(dpv[e + 1])),
+                                                                 ndl));
+                                pp[8 * L + 2 * k + jh] = pack_bf16x2(p.x, p.y);
+                                dd[8 * L + 2 * k + jh] = pack_bf16x2(ds.x, ds.y);
                             }
-                            const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e + x]),
-                                                                         __uint_as_float(dpv[e + x + 1])),
-                                                             ndl));
-                            pp[(e + x) >> 1] = pack_bf16x2(p.x, p.y);
-                            dd[(e + x) >> 1] = pack_bf16x2(ds.x, ds.y);
                         }
                     }
                 };
@@ -703,7 +707,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                                                        ((x + 2) / HS) & 1, abort_flag));
                 if (!ok) break;
             }
-            tmem_st16x2_sync(tS, pp, tP, dd);
+            tmem_st16x128b_x4_rows32_pair_sync(tS, pp, tP, dd);
             tc_fence_before();
             mbar_arrive(&bars.p_full[wg >> 1]);
         }

@@ -25,6 +25,8 @@
 //
 // Every barrier wait is bounded (xt_tc.cuh); on a timeout the CTA raises the
 // library's error word, drains its own copies and MMAs, frees TMEM and exits.
+#include <algorithm>
+
 #include "xt_common.cuh"
 #include "xt_internal.h"
 #include "xt_tc.cuh"
@@ -50,7 +52,7 @@ template <int D> struct FwdCfg {
 };
 
 struct FwdBarriers {
-    uint64_t q_full;
+    uint64_t q_full, q_empty;
     uint64_t k_full[4], v_full[4], kv_empty[4];
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t drain;
@@ -58,6 +60,34 @@ struct FwdBarriers {
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// Work item w: query tiles 2 pair and 2 pair + 1 of head h of unit `unit`.
+// Items run longest first (pair descending); consecutive items are
+// consecutive heads of one unit, so CTAs working at the same time share K/V
+// tiles in L2. n_kv[i]: key tiles of query tile i (0 past a short sample).
+struct FwdItem {
+    int pair, h, g;
+    SeqSpan sp;
+    int n_kv[2];
+};
+
+__device__ __forceinline__ FwdItem fwd_item(int w, int BH, int n_pairs, int H, int G,
+                                            const SeqRows &sr) {
+    FwdItem it;
+    it.pair = n_pairs - 1 - w / BH;
+    const int bh = w - (w / BH) * BH;
+    const int unit = bh / H;
+    it.h = bh - unit * H;
+    it.g = it.h / (H / G);
+    it.sp = seq_span(sr, unit);
+    const int n_qtiles = (it.sp.len + kBM - 1) / kBM;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int qt = 2 * it.pair + i;
+        it.n_kv[i] = qt < n_qtiles ? qt + 1 : 0;
+    }
+    return it;
+}
 
 __device__ __forceinline__ void raise_error(unsigned int *err, volatile int *abort_flag) {
     atomicOr(err, ERR_TIMEOUT);
@@ -94,8 +124,8 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsFwd, 1)
 k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
          const __grid_constant__ CUtensorMap map_v, bf16 *__restrict__ out,
-         float *__restrict__ lse, const SeqRows sr, int H, int G, int n_pairs,
-         unsigned int *err, int stall) {
+         float *__restrict__ lse, const SeqRows sr, int H, int G, int BH, int n_pairs,
+         int n_items, unsigned int *err, int stall) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBarriers bars;
@@ -104,25 +134,12 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     uint8_t *sKV = smem + 2 * C::kTileBytes;      // stage s: K at 2s, V at 2s+1
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = gridDim.x / n_pairs;
-    const int pair = n_pairs - 1 - (int)(blockIdx.x / BH);   // longest first
-    const int bh = blockIdx.x % BH;
-    const int unit = bh / H, h = bh - unit * H, g = h / (H / G);
-    const SeqSpan sp = seq_span(sr, unit);
-    const int n_qtiles = (sp.len + kBM - 1) / kBM;
-    int n_kv[2];
-    for (int i = 0; i < 2; ++i) {
-        const int qt = 2 * pair + i;
-        n_kv[i] = qt < n_qtiles ? qt + 1 : 0;
-    }
-    if (n_kv[0] == 0) return;   // a packed sample shorter than this pair's rows
-    const int n_iter = max(n_kv[0], n_kv[1]);
-    const int qplane = sp.plane * H + h, kplane = sp.plane * G + g;
     volatile int *abort_flag = &bars.abort_flag;
 
     if (threadIdx.x == 0) {
         bars.abort_flag = 0;
         mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
         for (int s = 0; s < C::kStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
             mbar_init(&bars.v_full[s], 1);
@@ -145,44 +162,59 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    // Every role walks the same items (w = blockIdx.x, + gridDim.x, ...) and
+    // skips the same empty ones; barrier phases are counted across items.
     if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
-            const int nq = (n_kv[1] > 0) ? 2 : 1;
-            mbar_expect_tx(&bars.q_full, nq * C::kTileBytes);
-            for (int i = 0; i < nq; ++i)
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sQ + i * C::kTileBytes + c * C::kBox, &map_q, &bars.q_full,
-                                c * C::A::kCols, sp.start + (2 * pair + i) * kBM, qplane);
-            int issued = 0;
-            for (int j = 0; j < n_iter; ++j) {
-                const int st = j % C::kStages;
-                if (j >= C::kStages &&
-                    !mbar_wait(&bars.kv_empty[st], ((j / C::kStages) - 1) & 1, abort_flag)) {
-                    if (!*abort_flag) raise_error(err, abort_flag);
+            int q_issued = 0, kv_issued = 0;
+            bool ok = true;
+            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+                const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
+                if (it.n_kv[0] == 0) continue;   // a packed sample shorter than this pair's rows
+                const int n_iter = max(it.n_kv[0], it.n_kv[1]);
+                const int qplane = it.sp.plane * H + it.h, kplane = it.sp.plane * G + it.g;
+                // the Q tiles are reloaded once the previous item's S MMAs have read them
+                if (q_issued > 0 &&
+                    !(ok = mbar_wait(&bars.q_empty, (q_issued - 1) & 1, abort_flag)))
                     break;
+                const int nq = (it.n_kv[1] > 0) ? 2 : 1;
+                mbar_expect_tx(&bars.q_full, nq * C::kTileBytes);
+                for (int i = 0; i < nq; ++i)
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sQ + i * C::kTileBytes + c * C::kBox, &map_q, &bars.q_full,
+                                    c * C::A::kCols, it.sp.start + (2 * it.pair + i) * kBM, qplane);
+                ++q_issued;
+                for (int j = 0; j < n_iter; ++j) {
+                    const int st = kv_issued % C::kStages;
+                    if (kv_issued >= C::kStages &&
+                        !(ok = mbar_wait(&bars.kv_empty[st], ((kv_issued / C::kStages) - 1) & 1,
+                                         abort_flag)))
+                        break;
+                    uint8_t *sK = sKV + (2 * st) * C::kTileBytes;
+                    uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
+                    mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(sK + c * C::kBox, &map_k, &bars.k_full[st], c * C::A::kCols,
+                                    it.sp.start + j * kBN, kplane);
+                    mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_4d(sV + c * C::kBox, &map_v, &bars.v_full[st], c * C::A::kCols,
+                                    it.g, it.sp.start + j * kBN, it.sp.plane);
+                    ++kv_issued;
                 }
-                uint8_t *sK = sKV + (2 * st) * C::kTileBytes;
-                uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
-                mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_3d(sK + c * C::kBox, &map_k, &bars.k_full[st], c * C::A::kCols,
-                                sp.start + j * kBN, kplane);
-                mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sV + c * C::kBox, &map_v, &bars.v_full[st], c * C::A::kCols, g,
-                                sp.start + j * kBN, sp.plane);
-                issued = j + 1;
             }
-            // Drain: every copy this CTA issued must land before it exits.
-            mbar_wait(&bars.q_full, 0, nullptr);
-            for (int j = max(0, issued - C::kStages); j < issued; ++j) {
-                const int st = j % C::kStages;
-                mbar_wait(&bars.k_full[st], (j / C::kStages) & 1, nullptr);
-                mbar_wait(&bars.v_full[st], (j / C::kStages) & 1, nullptr);
+            if (!ok && !*abort_flag) raise_error(err, abort_flag);
+            // Drain: every copy this CTA issued must land before it exits (at most the
+            // last Q load and the last kStages K/V tiles can still be in flight).
+            if (q_issued > 0) mbar_wait(&bars.q_full, (q_issued - 1) & 1, nullptr);
+            for (int x = max(0, kv_issued - C::kStages); x < kv_issued; ++x) {
+                const int st = x % C::kStages;
+                mbar_wait(&bars.k_full[st], (x / C::kStages) & 1, nullptr);
+                mbar_wait(&bars.v_full[st], (x / C::kStages) & 1, nullptr);
             }
         }
     } else if (warp == 9) {
@@ -190,7 +222,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         // Issue order per key tile j: PV_{j,0}, S_{j+1,0}, PV_{j,1}, S_{j+1,1}, so the
         // next S of query tile 0 queues right behind its PV while tile 1's softmax runs.
         // The MMA warp waits for data (TMA) and for P (softmax), never for its own
-        // MMAs: the tensor pipe executes one thread's MMAs in issue order.
+        // MMAs: the tensor pipe executes one thread's MMAs in issue order. The first
+        // PV of an item overwrites O_i: the softmax threads of tile i read the
+        // previous item's O_i (epilogue) before they signal that item's first P_i.
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
@@ -215,41 +249,53 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                 mma_commit(&bars.s_full[i]);
             };
             bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
-            ok = ok && mbar_wait(&bars.q_full, 0, abort_flag) &&
-                 mbar_wait(&bars.k_full[0], 0, abort_flag);
-            if (ok) {
+            int items = 0, kv_used = 0, p_cnt[2] = {0, 0};
+            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+                const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
+                if (it.n_kv[0] == 0) continue;
+                const int n_iter = max(it.n_kv[0], it.n_kv[1]);
+                const int st0 = kv_used % C::kStages;
+                ok = mbar_wait(&bars.q_full, items & 1, abort_flag) &&
+                     mbar_wait(&bars.k_full[st0], (kv_used / C::kStages) & 1, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
                 for (int i = 0; i < 2; ++i)
-                    if (n_kv[i] > 0) issue_s(i, 0);
-            }
-            for (int j = 0; ok && j < n_iter; ++j) {
-                const int st = j % C::kStages, st1 = (j + 1) % C::kStages;
-                const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
-                if (!(ok = mbar_wait(&bars.v_full[st], (j / C::kStages) & 1, abort_flag))) break;
-                bool k_next = false;
-                for (int i = 0; i < 2 && ok; ++i) {
-                    if (j >= n_kv[i]) continue;
-                    if (!(ok = mbar_wait(&bars.p_full[i], j & 1, abort_flag))) break;
-                    tc_fence_after();
+                    if (it.n_kv[i] > 0) issue_s(i, st0);
+                for (int j = 0; ok && j < n_iter; ++j) {
+                    const int x = kv_used + j;
+                    const int st = x % C::kStages, st1 = (x + 1) % C::kStages;
+                    const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
+                    if (!(ok = mbar_wait(&bars.v_full[st], (x / C::kStages) & 1, abort_flag))) break;
+                    bool k_next = false;
+                    for (int i = 0; i < 2 && ok; ++i) {
+                        if (j >= it.n_kv[i]) continue;
+                        if (!(ok = mbar_wait(&bars.p_full[i], p_cnt[i] & 1, abort_flag))) break;
+                        ++p_cnt[i];
+                        tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)(A::mnstep(kk) >> 4), idesc_o,
-                               (j > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&bars.o_done[i]);
-                    if (j + 1 < n_kv[i]) {
-                        if (!k_next) {
-                            if (!(ok = mbar_wait(&bars.k_full[st1], ((j + 1) / C::kStages) & 1,
-                                                 abort_flag)))
-                                break;
-                            k_next = true;
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)(A::mnstep(kk) >> 4),
+                                   idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        mma_commit(&bars.o_done[i]);
+                        if (j + 1 < it.n_kv[i]) {
+                            if (!k_next) {
+                                if (!(ok = mbar_wait(&bars.k_full[st1], ((x + 1) / C::kStages) & 1,
+                                                     abort_flag)))
+                                    break;
+                                k_next = true;
+                            }
+                            // No wait for PV_{j,i} to finish reading P_i: tcgen05.mma
+                            // operations issued by one thread execute in issue order.
+                            issue_s(i, st1);
                         }
-                        // No wait for PV_{j,i} to finish reading P_i: tcgen05.mma operations
-                        // issued by one thread execute in issue order.
-                        issue_s(i, st1);
                     }
+                    if (!ok) break;
+                    mma_commit(&bars.kv_empty[st]);
                 }
                 if (!ok) break;
-                mma_commit(&bars.kv_empty[st]);
+                mma_commit(&bars.q_empty);   // every S MMA of this item has read sQ
+                kv_used += n_iter;
+                ++items;
             }
             if (!ok && !*abort_flag) raise_error(err, abort_flag);
             // Drain: all MMAs issued by this thread complete before TMEM is freed.
@@ -261,87 +307,91 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         const int i = warp >> 2;                 // query tile of this warpgroup
         const int quarter = warp & 3;            // TMEM lanes [32*quarter, 32*quarter+32)
         const int r = quarter * 32 + lane;       // row within the tile
-        const int t = (2 * pair + i) * kBM + r;  // query position inside the unit
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem + i * 128 + lane_off;
         const uint32_t tO = tmem + 256 + i * 128 + lane_off;
         const float sl2 = kLog2e * rsqrtf((float)D);
-        float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        const int n = n_kv[i];
-        for (int j = 0; j < n; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[i], j & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            uint32_t sr[128];
-            tmem_ld128_sync(tS, sr);
-            if (j == n - 1) {
-                // diagonal tile: key column c is visible to row r iff c <= r
-#pragma unroll
-                for (int e = 0; e < 128; ++e)
-                    if (e > r) sr[e] = __float_as_uint(-INFINITY);
-            }
-            float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-            for (int e = 0; e < 128; e += 4) {
-                m0 = fmax3(m0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
-                m1 = fmax3(m1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
-            }
-            const float mx = fmaxf(m0, m1) * sl2;
-            const float m_new = fmaxf(m_used, mx);
-            const bool need = m_new - m_used > kRescaleThreshold;   // true on the first tile
-            float alpha = 1.f;
-            if (need) {
-                alpha = fast_exp2(m_used - m_new);
-                m_used = m_new;
-            }
-            // O rescale in TMEM (warp-uniform: tcgen05.ld/st are warp-collective)
-            if (j > 0 && __any_sync(0xffffffffu, need)) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (j - 1) & 1, abort_flag));
+        int s_cnt = 0;   // S_i tiles (and PV_i MMAs) of the previous items
+        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
+            const int n = it.n_kv[i];
+            if (n == 0) continue;                // no query tile i in this item
+            const int t = (2 * it.pair + i) * kBM + r;   // query position inside the unit
+            float m_used = -INFINITY, l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[i], (s_cnt + j) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
+                uint32_t sr[128];
+                tmem_ld128_sync(tS, sr);
+                if (j == n - 1) {
+                    // diagonal tile: key column c is visible to row r iff c <= r
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32_sync(tO + c * 32, o);
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32_sync(tO + c * 32, o);
+                    for (int e = 0; e < 128; ++e)
+                        if (e > r) sr[e] = __float_as_uint(-INFINITY);
                 }
-            }
-            // element pairs through the packed fp32 pipe (f32x2 FMA / add)
-            const float2 nm2 = make_float2(-m_used, -m_used), sl2v = make_float2(sl2, sl2);
-            float2 rs01 = make_float2(0.f, 0.f), rs23 = make_float2(0.f, 0.f);
-            uint32_t pk[64];
+                float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 128; e += 4) {
-                const float2 a01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
-                                         sl2v, nm2);
-                const float2 a23 = ffma2(make_float2(__uint_as_float(sr[e + 2]),
-                                                     __uint_as_float(sr[e + 3])), sl2v, nm2);
-                const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
-                const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
-                rs01 = fadd2(rs01, p01);
-                rs23 = fadd2(rs23, p23);
-                pk[e >> 1] = pack_bf16x2(p01.x, p01.y);
-                pk[(e >> 1) + 1] = pack_bf16x2(p23.x, p23.y);
+                for (int e = 0; e < 128; e += 4) {
+                    m0 = fmax3(m0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+                    m1 = fmax3(m1, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+                }
+                const float mx = fmaxf(m0, m1) * sl2;
+                const float m_new = fmaxf(m_used, mx);
+                const bool need = m_new - m_used > kRescaleThreshold;   // true on the first tile
+                float alpha = 1.f;
+                if (need) {
+                    alpha = fast_exp2(m_used - m_new);
+                    m_used = m_new;
+                }
+                // O rescale in TMEM (warp-uniform: tcgen05.ld/st are warp-collective)
+                if (j > 0 && __any_sync(0xffffffffu, need)) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (s_cnt + j - 1) & 1,
+                                                           abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32_sync(tO + c * 32, o);
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32_sync(tO + c * 32, o);
+                    }
+                }
+                // element pairs through the packed fp32 pipe (f32x2 FMA / add)
+                const float2 nm2 = make_float2(-m_used, -m_used), sl2v = make_float2(sl2, sl2);
+                float2 rs01 = make_float2(0.f, 0.f), rs23 = make_float2(0.f, 0.f);
+                uint32_t pk[64];
+#pragma unroll
+                for (int e = 0; e < 128; e += 4) {
+                    const float2 a01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                             sl2v, nm2);
+                    const float2 a23 = ffma2(make_float2(__uint_as_float(sr[e + 2]),
+                                                         __uint_as_float(sr[e + 3])), sl2v, nm2);
+                    const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
+                    const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
+                    rs01 = fadd2(rs01, p01);
+                    rs23 = fadd2(rs23, p23);
+                    pk[e >> 1] = pack_bf16x2(p01.x, p01.y);
+                    pk[(e >> 1) + 1] = pack_bf16x2(p23.x, p23.y);
+                }
+                const float rowsum = (rs01.x + rs01.y) + (rs23.x + rs23.y);
+                tmem_st64_sync(tS, pk);
+                tc_fence_before();
+                mbar_arrive(&bars.p_full[i]);
+                l = l * alpha + rowsum;
             }
-            const float rowsum = (rs01.x + rs01.y) + (rs23.x + rs23.y);
-            tmem_st64_sync(tS, pk);
-            tc_fence_before();
-            mbar_arrive(&bars.p_full[i]);
-            l = l * alpha + rowsum;
-        }
-        if (ok && n > 0) {
+            if (!ok) break;
             // epilogue: O / l -> bf16 rows of out [B, S, H, D]; lse = (m + log2 l) ln 2
-            if (__all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (n - 1) & 1, abort_flag))) {
-                tc_fence_after();
-                const size_t row = (size_t)sp.plane * sr.S + sp.start + t;
-                write_out_row<D>(tO, l, m_used, t < sp.len, out + (row * H + h) * D,
-                                 lse + (size_t)qplane * sr.S + sp.start + t);
-            } else {
-                ok = false;
-            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.o_done[i], (s_cnt + n - 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            const size_t row = (size_t)it.sp.plane * sr.S + it.sp.start + t;
+            write_out_row<D>(tO, l, m_used, t < it.sp.len, out + (row * H + it.h) * D,
+                             lse + ((size_t)it.sp.plane * H + it.h) * sr.S + it.sp.start + t);
+            s_cnt += n;
         }
         if (!ok && !*abort_flag) raise_error(err, abort_flag);
     }
@@ -382,13 +432,17 @@ cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat
     }
     const int n_qtiles = (p.max_len + kBM - 1) / kBM;
     const int n_pairs = (n_qtiles + 1) / 2;
-    const long blocks = (long)p.units * p.H * n_pairs;
+    const long BH = (long)p.units * p.H;
+    const long n_items = BH * n_pairs;
+    if (n_items >= (1L << 31)) return cudaErrorInvalidValue;
+    // persistent grid: one CTA per SM walks the items (one CTA fits an SM: 512 TMEM columns)
+    const long blocks = std::min<long>(n_items, sm_count());
     cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
     k_fwd_tc<D><<<(unsigned)blocks, kThreadsFwd, C::kSmemBytes, st>>>(
-        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_pairs, err,
-        (test_stall_mask() & STALL_FWD_TC) != 0);
+        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_pairs,
+        (int)n_items, err, (test_stall_mask() & STALL_FWD_TC) != 0);
     return cudaGetLastError();
 }
 

@@ -101,7 +101,9 @@ cudaError_t launch_decode_attn(const Problem &p, const DecodePlan &d, const int 
 cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const float *part_o,
                                   const float *part_ml, void *out, float *lse, cudaStream_t st);
 
-// ---- TMA tensor maps (xt_tmap.cu) ----
+// ---- TMA tensor maps and the SM count (xt_tmap.cu) ----
+// Multiprocessors of the current device (queried once per device).
+int sm_count();
 // swizzle_bytes: 128 or 64 (the smem row width of the box, see tc::Atoms).
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                              const uint64_t *strides_bytes, const uint32_t *box,

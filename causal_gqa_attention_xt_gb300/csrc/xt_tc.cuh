@@ -384,6 +384,46 @@ __device__ __forceinline__ void tmem_ld16_pair_sync(uint32_t ta, uint32_t (&a)[1
         : "memory");
 }
 
+// 16-lane shapes. 16x256b: per repetition of 8 columns, thread t receives
+// (lane base + t/4, columns 2(t%4) and 2(t%4)+1) in registers 0-1 and the same
+// columns of lane base + 8 + t/4 in registers 2-3; repetition k adds 8 to the
+// columns. 16x128b: per repetition of 4 columns, thread t holds (lane base +
+// t/4, column t%4) in register 0 and (lane base + 8 + t/4, column t%4) in
+// register 1; repetition k adds 4. (Checked on the GPU against 32x32b.)
+//
+// Four 16x256b.x4 loads (two TMEM regions, lane bases +0 and +16 of the
+// warp's quarter: 32 rows x 32 columns each) and one wait: a[16 L + 4 k + j]
+// is element (lanes +16 L, repetition k, register j) of region ta, b likewise
+// of region tb.
+__device__ __forceinline__ void tmem_ld16x256b_x4_rows32_pair_sync(uint32_t ta, uint32_t (&a)[32],
+                                                                   uint32_t tb, uint32_t (&b)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%64];\n"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%65];\n"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47}, [%66];\n"
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%67];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]), "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]), "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]), "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]), "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]), "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]), "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
+        : "r"(ta), "r"(ta + (16u << 16)), "r"(tb), "r"(tb + (16u << 16))
+        : "memory");
+}
+
+// Four 16x128b.x4 stores (two TMEM regions, lane bases +0 and +16: 32 rows x
+// 16 columns each) and one wait: a[8 L + 2 k + j] goes to (lanes +16 L,
+// repetition k, register j) of region ta, b likewise of region tb.
+__device__ __forceinline__ void tmem_st16x128b_x4_rows32_pair_sync(uint32_t ta, const uint32_t (&a)[16],
+                                                                   uint32_t tb, const uint32_t (&b)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%4, %5, %6, %7, %8, %9, %10, %11};\n"
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%1], {%12, %13, %14, %15, %16, %17, %18, %19};\n"
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%2], {%20, %21, %22, %23, %24, %25, %26, %27};\n"
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%3], {%28, %29, %30, %31, %32, %33, %34, %35};\n"
+        "tcgen05.wait::st.sync.aligned;"
+        :: "r"(ta), "r"(ta + (16u << 16)), "r"(tb), "r"(tb + (16u << 16)),
+           "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]), "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]), "r"(b[8]), "r"(b[9]), "r"(b[10]), "r"(b[11]), "r"(b[12]), "r"(b[13]), "r"(b[14]), "r"(b[15])
+        : "memory");
+}
+
 // Three-input max (sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;

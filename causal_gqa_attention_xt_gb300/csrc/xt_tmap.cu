@@ -1,6 +1,7 @@
 // xt_tmap.cu -- host-side TMA tensor-map encoding (cuTensorMapEncodeTiled,
 // reached through the runtime's driver entry-point query, so the library
-// needs no link-time dependency on libcuda).
+// needs no link-time dependency on libcuda), and the cached SM count that
+// sizes the persistent grids.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -53,6 +54,22 @@ cudaError_t encode_tmap(CUtensorMap *map, CUtensorMapDataType type, const void *
 }
 
 }  // namespace
+
+int sm_count() {
+    static int cache[64] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1)
+            return 148;
+        cache[dev] = sms;
+    }
+    return cache[dev];
+}
 
 // A tensor of `rank` dims (innermost first), byte strides of dims 1..rank-1,
 // box sizes per dim, 128- or 64-byte swizzle, zero fill out of bounds.
