@@ -560,7 +560,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
+            // the whole warp runs this loop; one elected lane issues each MMA / commit
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile / 2, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             using A = typename C::A;
@@ -578,18 +579,19 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 const uint64_t so = (uint64_t)((2 * t + h) % HS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 64 * h, dK + kmajor_off<D>(kk), dQk0 + so + kmajor_off_half<D>(kk),
+                    mma_ss_w(tmem + 64 * h, dK + kmajor_off<D>(kk), dQk0 + so + kmajor_off_half<D>(kk),
                            idesc_s, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ss(tmem + 128 + 64 * h, dV + kmajor_off<D>(kk),
+                    mma_ss_w(tmem + 128 + 64 * h, dV + kmajor_off<D>(kk),
                            dDOk0 + so + kmajor_off_half<D>(kk), idesc_s, kk > 0);
-                mma_commit(&bars.s_full[h]);
+                mma_commit_w(&bars.s_full[h]);
             };
-            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
-            ok = ok && mbar_wait(&bars.own_full, 0, abort_flag) &&
-                 mbar_wait(&bars.st_full[0], 0, abort_flag) &&
-                 mbar_wait(&bars.st_full[1], 0, abort_flag);   // both halves of tile 0
+            bool ok = !stall ||
+                      __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
+            ok = ok && mbar_wait_w(&bars.own_full, 0, abort_flag) &&
+                 mbar_wait_w(&bars.st_full[0], 0, abort_flag) &&
+                 mbar_wait_w(&bars.st_full[1], 0, abort_flag);   // both halves of tile 0
             if (ok) {
                 tc_fence_after();
                 issue_sp(0, 0);
@@ -603,28 +605,28 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 for (int h = 0; h < 2; ++h) {
                     const int hs = (2 * t + h) % HS;
                     const uint64_t so = (uint64_t)hs * kStep;
-                    if (!(ok = mbar_wait(&bars.p_full[h], t & 1, abort_flag))) break;
+                    if (!(ok = mbar_wait_w(&bars.p_full[h], t & 1, abort_flag))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dV += P^T dO
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off<D>(k4),
+                        mma_ts_w(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off<D>(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {   // dKhat += dS^T Qhat
                         const int kk = 4 * h + k4;
-                        mma_ts(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off<D>(k4),
+                        mma_ts_w(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off<D>(k4),
                                idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
                     }
-                    mma_commit(&bars.st_empty[hs]);       // this half stage may be reloaded
+                    mma_commit_w(&bars.st_empty[hs]);       // this half stage may be reloaded
                     if (t + 1 < T) issue_sp(t + 1, h);   // operands checked by the softmax warps
                 }
             }
-            if (ok) mma_commit(&bars.acc_done);
-            else if (!*abort_flag) raise_error_b(err, abort_flag);
-            mma_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0, nullptr);
+            if (ok) mma_commit_w(&bars.acc_done);
+            else if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+            mma_commit_w(&bars.drain);
+            mbar_wait_w(&bars.drain, 0, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
@@ -875,7 +877,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        {
+            // the whole warp runs this loop; one elected lane issues each MMA / commit
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             using A = typename C::A;
@@ -889,19 +892,20 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off<D>(kk), idesc_s, kk > 0);
+                    mma_ts_w(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off<D>(kk), idesc_s, kk > 0);
             };
             auto issue_dp = [&](int t) {
                 const uint64_t so = (uint64_t)(t % ST) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off<D>(kk), idesc_s,
+                    mma_ts_w(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off<D>(kk), idesc_s,
                            kk > 0);
-                mma_commit(&bars.s_full[0]);         // S and dP of tile t are in TMEM
+                mma_commit_w(&bars.s_full[0]);         // S and dP of tile t are in TMEM
             };
-            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
-            ok = ok && mbar_wait(&bars.own_full, 0, abort_flag) &&
-                 mbar_wait(&bars.st_full[0], 0, abort_flag);
+            bool ok = !stall ||
+                      __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
+            ok = ok && mbar_wait_w(&bars.own_full, 0, abort_flag) &&
+                 mbar_wait_w(&bars.st_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
@@ -915,26 +919,26 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 const int st = t % ST;
                 const uint64_t so = (uint64_t)st * kStep;
                 if (t + 1 < T) {
-                    if (!(ok = mbar_wait(sdp_taken, t & 1, abort_flag) &&
-                               mbar_wait(&bars.st_full[(t + 1) % ST], ((t + 1) / ST) & 1,
+                    if (!(ok = mbar_wait_w(sdp_taken, t & 1, abort_flag) &&
+                               mbar_wait_w(&bars.st_full[(t + 1) % ST], ((t + 1) / ST) & 1,
                                          abort_flag)))
                         break;
                     tc_fence_after();
                     issue_s(t + 1);
                 }
-                if (!(ok = mbar_wait(ds_ready, t & 1, abort_flag))) break;
+                if (!(ok = mbar_wait_w(ds_ready, t & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off<D>(kk),
+                    mma_ts_w(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off<D>(kk),
                            idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&bars.st_empty[st]);
+                mma_commit_w(&bars.st_empty[st]);
                 if (t + 1 < T) issue_dp(t + 1);
             }
-            if (ok) mma_commit(&bars.acc_done);
-            else if (!*abort_flag) raise_error_b(err, abort_flag);
-            mma_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0, nullptr);
+            if (ok) mma_commit_w(&bars.acc_done);
+            else if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+            mma_commit_w(&bars.drain);
+            mbar_wait_w(&bars.drain, 0, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue

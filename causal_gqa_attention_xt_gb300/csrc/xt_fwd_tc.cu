@@ -13,7 +13,7 @@
 // while the softmax warps work on the other:
 //   warps 0-3  softmax + epilogue of query tile 0 (thread = one query row)
 //   warps 4-7  softmax + epilogue of query tile 1
-//   warp  8    TMA producer: Q tiles once, then a ring of K/V tiles
+//   warp  8    TMA producer: each item's Q tiles, then K and V tiles into two rings
 //   warp  9    TMEM allocator and MMA issuer (one thread)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // S_i = Q_i K^T is an SS MMA (both operands K-major, 128B swizzle); the
@@ -47,13 +47,17 @@ template <int D> struct FwdCfg {
     static constexpr int kChunks = A::kPerRow;              // swizzle atoms (TMA boxes) per row
     static constexpr int kBox = A::box_bytes(128);          // one box of a 128-row tile
     static constexpr int kTileBytes = kChunks * kBox;       // one 128-row tile
-    static constexpr int kStages = (D == 128) ? 2 : 4;      // K/V ring depth
-    static constexpr int kSmemBytes = 2 * kTileBytes + kStages * 2 * kTileBytes + 1024;
+    // separate K and V rings: a K tile is released once the last S MMA that reads
+    // it has run (an iteration before its V tile), so each ring refills on its own
+    static constexpr int kKStages = (D == 128) ? 2 : 5;
+    static constexpr int kVStages = (D == 128) ? 3 : 5;
+    static constexpr int kSmemBytes = (2 + kKStages + kVStages) * kTileBytes + 1024;
 };
+constexpr int kMaxRing = 8;
 
 struct FwdBarriers {
     uint64_t q_full, q_empty;
-    uint64_t k_full[4], v_full[4], kv_empty[4];
+    uint64_t k_full[kMaxRing], k_empty[kMaxRing], v_full[kMaxRing], v_empty[kMaxRing];
     uint64_t s_full[2], p_full[2], o_done[2];
     uint64_t drain;
     uint64_t stall;   // never arrived on (xt_test_inject_stall)
@@ -130,8 +134,9 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     extern __shared__ uint8_t smem_raw[];
     __shared__ FwdBarriers bars;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sQ = smem;                           // 2 tiles
-    uint8_t *sKV = smem + 2 * C::kTileBytes;      // stage s: K at 2s, V at 2s+1
+    uint8_t *sQ = smem;                                   // 2 tiles
+    uint8_t *sK = smem + 2 * C::kTileBytes;               // kKStages tiles
+    uint8_t *sV = sK + C::kKStages * C::kTileBytes;       // kVStages tiles
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &bars.abort_flag;
@@ -140,10 +145,13 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         bars.abort_flag = 0;
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.q_empty, 1);
-        for (int s = 0; s < C::kStages; ++s) {
+        for (int s = 0; s < C::kKStages; ++s) {
             mbar_init(&bars.k_full[s], 1);
+            mbar_init(&bars.k_empty[s], 1);
+        }
+        for (int s = 0; s < C::kVStages; ++s) {
             mbar_init(&bars.v_full[s], 1);
-            mbar_init(&bars.kv_empty[s], 1);
+            mbar_init(&bars.v_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
@@ -170,7 +178,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             tma_prefetch_desc(&map_q);
             tma_prefetch_desc(&map_k);
             tma_prefetch_desc(&map_v);
-            int q_issued = 0, kv_issued = 0;
+            int q_issued = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
             for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
                 const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
@@ -189,33 +197,35 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
                                     c * C::A::kCols, it.sp.start + (2 * it.pair + i) * kBM, qplane);
                 ++q_issued;
                 for (int j = 0; j < n_iter; ++j) {
-                    const int st = kv_issued % C::kStages;
-                    if (kv_issued >= C::kStages &&
-                        !(ok = mbar_wait(&bars.kv_empty[st], ((kv_issued / C::kStages) - 1) & 1,
-                                         abort_flag)))
+                    const int x = v_issued;   // == k_issued here
+                    const int ks = x % C::kKStages, vs = x % C::kVStages;
+                    if (x >= C::kKStages &&
+                        !(ok = mbar_wait(&bars.k_empty[ks], ((x / C::kKStages) - 1) & 1, abort_flag)))
                         break;
-                    uint8_t *sK = sKV + (2 * st) * C::kTileBytes;
-                    uint8_t *sV = sKV + (2 * st + 1) * C::kTileBytes;
-                    mbar_expect_tx(&bars.k_full[st], C::kTileBytes);
+                    mbar_expect_tx(&bars.k_full[ks], C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(sK + c * C::kBox, &map_k, &bars.k_full[st], c * C::A::kCols,
-                                    it.sp.start + j * kBN, kplane);
-                    mbar_expect_tx(&bars.v_full[st], C::kTileBytes);
+                        tma_load_3d(sK + ks * C::kTileBytes + c * C::kBox, &map_k, &bars.k_full[ks],
+                                    c * C::A::kCols, it.sp.start + j * kBN, kplane);
+                    ++k_issued;
+                    if (x >= C::kVStages &&
+                        !(ok = mbar_wait(&bars.v_empty[vs], ((x / C::kVStages) - 1) & 1, abort_flag)))
+                        break;
+                    mbar_expect_tx(&bars.v_full[vs], C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_4d(sV + c * C::kBox, &map_v, &bars.v_full[st], c * C::A::kCols,
-                                    it.g, it.sp.start + j * kBN, it.sp.plane);
-                    ++kv_issued;
+                        tma_load_4d(sV + vs * C::kTileBytes + c * C::kBox, &map_v, &bars.v_full[vs],
+                                    c * C::A::kCols, it.g, it.sp.start + j * kBN, it.sp.plane);
+                    ++v_issued;
                 }
             }
             if (!ok && !*abort_flag) raise_error(err, abort_flag);
             // Drain: every copy this CTA issued must land before it exits (at most the
-            // last Q load and the last kStages K/V tiles can still be in flight).
+            // last Q load, the last kKStages K tiles and the last kVStages V tiles can
+            // still be in flight).
             if (q_issued > 0) mbar_wait(&bars.q_full, (q_issued - 1) & 1, nullptr);
-            for (int x = max(0, kv_issued - C::kStages); x < kv_issued; ++x) {
-                const int st = x % C::kStages;
-                mbar_wait(&bars.k_full[st], (x / C::kStages) & 1, nullptr);
-                mbar_wait(&bars.v_full[st], (x / C::kStages) & 1, nullptr);
-            }
+            for (int x = max(0, k_issued - C::kKStages); x < k_issued; ++x)
+                mbar_wait(&bars.k_full[x % C::kKStages], (x / C::kKStages) & 1, nullptr);
+            for (int x = max(0, v_issued - C::kVStages); x < v_issued; ++x)
+                mbar_wait(&bars.v_full[x % C::kVStages], (x / C::kVStages) & 1, nullptr);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issuer
@@ -225,7 +235,8 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         // MMAs: the tensor pipe executes one thread's MMAs in issue order. The first
         // PV of an item overwrites O_i: the softmax threads of tile i read the
         // previous item's O_i (epilogue) before they signal that item's first P_i.
-        if (lane == 0) {
+        {
+            // the whole warp runs this loop; one elected lane issues each MMA / commit
             const uint32_t idesc_s = idesc_bf16_f32(kBM, kBN, 0, 0);
             const uint32_t idesc_o = idesc_bf16_f32(kBM, D, 0, 1);
             const uint32_t tS[2] = {tmem, tmem + 128};
@@ -234,73 +245,75 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             // start-address field) is added, which keeps the single issuing thread fast.
             using A = typename C::A;
             const uint64_t dQ0 = smem_desc(smem_u32(sQ), 16, A::kSBO, A::kMode);
-            const uint64_t dK0 = smem_desc(smem_u32(sKV), 16, A::kSBO, A::kMode);
-            const uint64_t dV0 = smem_desc(smem_u32(sKV + C::kTileBytes), C::kBox, A::kSBO, A::kMode);
-            constexpr uint64_t kStageStep = (uint64_t)(2 * C::kTileBytes) >> 4;
-            constexpr uint64_t kQStep = (uint64_t)C::kTileBytes >> 4;
-            auto issue_s = [&](int i, int st) {
-                const uint64_t dQ = dQ0 + (uint64_t)i * kQStep;
-                const uint64_t dK = dK0 + (uint64_t)st * kStageStep;
+            const uint64_t dK0 = smem_desc(smem_u32(sK), 16, A::kSBO, A::kMode);
+            const uint64_t dV0 = smem_desc(smem_u32(sV), C::kBox, A::kSBO, A::kMode);
+            constexpr uint64_t kTileStep = (uint64_t)C::kTileBytes >> 4;
+            auto issue_s = [&](int i, int ks) {
+                const uint64_t dQ = dQ0 + (uint64_t)i * kTileStep;
+                const uint64_t dK = dK0 + (uint64_t)ks * kTileStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint64_t off = (uint64_t)A::kstep(kk, kBM) >> 4;
-                    mma_ss(tS[i], dQ + off, dK + off, idesc_s, kk > 0);
+                    mma_ss_w(tS[i], dQ + off, dK + off, idesc_s, kk > 0);
                 }
-                mma_commit(&bars.s_full[i]);
+                mma_commit_w(&bars.s_full[i]);
             };
-            bool ok = !stall || mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs);
+            bool ok = !stall ||
+                      __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
             int items = 0, kv_used = 0, p_cnt[2] = {0, 0};
             for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
                 const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
                 if (it.n_kv[0] == 0) continue;
                 const int n_iter = max(it.n_kv[0], it.n_kv[1]);
-                const int st0 = kv_used % C::kStages;
-                ok = mbar_wait(&bars.q_full, items & 1, abort_flag) &&
-                     mbar_wait(&bars.k_full[st0], (kv_used / C::kStages) & 1, abort_flag);
+                const int ks0 = kv_used % C::kKStages;
+                ok = mbar_wait_w(&bars.q_full, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.k_full[ks0], (kv_used / C::kKStages) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 for (int i = 0; i < 2; ++i)
-                    if (it.n_kv[i] > 0) issue_s(i, st0);
+                    if (it.n_kv[i] > 0) issue_s(i, ks0);
+                mma_commit_w(&bars.k_empty[ks0]);   // K tile 0 of the item is read by then
                 for (int j = 0; ok && j < n_iter; ++j) {
                     const int x = kv_used + j;
-                    const int st = x % C::kStages, st1 = (x + 1) % C::kStages;
-                    const uint64_t dV = dV0 + (uint64_t)st * kStageStep;
-                    if (!(ok = mbar_wait(&bars.v_full[st], (x / C::kStages) & 1, abort_flag))) break;
+                    const int vs = x % C::kVStages, ks1 = (x + 1) % C::kKStages;
+                    const uint64_t dV = dV0 + (uint64_t)vs * kTileStep;
+                    if (!(ok = mbar_wait_w(&bars.v_full[vs], (x / C::kVStages) & 1, abort_flag))) break;
                     bool k_next = false;
                     for (int i = 0; i < 2 && ok; ++i) {
                         if (j >= it.n_kv[i]) continue;
-                        if (!(ok = mbar_wait(&bars.p_full[i], p_cnt[i] & 1, abort_flag))) break;
+                        if (!(ok = mbar_wait_w(&bars.p_full[i], p_cnt[i] & 1, abort_flag))) break;
                         ++p_cnt[i];
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < kBN / 16; ++kk)
-                            mma_ts(tO[i], tS[i] + kk * 8, dV + (uint64_t)(A::mnstep(kk) >> 4),
+                            mma_ts_w(tO[i], tS[i] + kk * 8, dV + (uint64_t)(A::mnstep(kk) >> 4),
                                    idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-                        mma_commit(&bars.o_done[i]);
+                        mma_commit_w(&bars.o_done[i]);
                         if (j + 1 < it.n_kv[i]) {
                             if (!k_next) {
-                                if (!(ok = mbar_wait(&bars.k_full[st1], ((x + 1) / C::kStages) & 1,
+                                if (!(ok = mbar_wait_w(&bars.k_full[ks1], ((x + 1) / C::kKStages) & 1,
                                                      abort_flag)))
                                     break;
                                 k_next = true;
                             }
                             // No wait for PV_{j,i} to finish reading P_i: tcgen05.mma
                             // operations issued by one thread execute in issue order.
-                            issue_s(i, st1);
+                            issue_s(i, ks1);
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&bars.kv_empty[st]);
+                    mma_commit_w(&bars.v_empty[vs]);                // V tile j is read
+                    if (k_next) mma_commit_w(&bars.k_empty[ks1]);   // and K tile j + 1
                 }
                 if (!ok) break;
-                mma_commit(&bars.q_empty);   // every S MMA of this item has read sQ
+                mma_commit_w(&bars.q_empty);   // every S MMA of this item has read sQ
                 kv_used += n_iter;
                 ++items;
             }
-            if (!ok && !*abort_flag) raise_error(err, abort_flag);
-            // Drain: all MMAs issued by this thread complete before TMEM is freed.
-            mma_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0, nullptr);
+            if (!ok && lane == 0 && !*abort_flag) raise_error(err, abort_flag);
+            // Drain: all MMAs issued by this warp complete before TMEM is freed.
+            mma_commit_w(&bars.drain);
+            mbar_wait_w(&bars.drain, 0, nullptr);
         }
     } else {
         // ------------------------------------------------------------ softmax + epilogue
