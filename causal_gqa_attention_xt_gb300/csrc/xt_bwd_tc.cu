@@ -508,14 +508,25 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                                 &bars.st_full[hs], c * C::A::kCols, h, sp.start + q0, sp.plane);
                 }
             }
+            // the half's row statistics (lse at [0,64), Dlt at [64,128)) by 4-byte
+            // asynchronous copies that the stage's barrier waits for, so the producer
+            // never stalls on a global load; rows past the end read as 0
             float *sl = reinterpret_cast<float *>(base + 2 * C::kHalfBytes);
             const size_t row0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int kq = lane + 32 * e, q = q0 + kq;
-                sl[kq] = q < S ? -lse[row0 + q] * kLog2e : 0.f;   // negated, for the f32x2 ops
-                sl[64 + kq] = q < S ? -dlt[row0 + q] : 0.f;
+                if (q < S) {
+                    cp_async4(sl + kq, lse + row0 + q);
+                    cp_async4(sl + 64 + kq, dlt + row0 + q);
+                } else {
+                    sl[kq] = 0.f;
+                    sl[64 + kq] = 0.f;
+                }
             }
+            // each lane's copies become one pending arrival of the stage barrier
+            // (registered before lane 0's arrival below, hence the __syncwarp)
+            cp_async_mbar_arrive(&bars.st_full[hs]);
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars.st_full[hs]);
             issued = x + 1;
@@ -651,8 +662,8 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            // statistics of the half: -lse (log2 units) at [0,64), -Dlt at [64,128), this
-            // warpgroup's 32 columns from 32 (wg & 1)
+            // statistics of the half: lse at [0,64), Dlt at [64,128), this warpgroup's
+            // 32 columns from 32 (wg & 1)
             const float *sl = reinterpret_cast<const float *>(sStage + hs * C::kHStageBytes +
                                                               2 * C::kHalfBytes) +
                               32 * (wg & 1);
@@ -674,8 +685,10 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 auto body = [&](auto masked) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 nl = *reinterpret_cast<const float2 *>(sl + 8 * k + cp);
-                        const float2 ndl = *reinterpret_cast<const float2 *>(sl + 64 + 8 * k + cp);
+                        const float2 nl = fmul2(*reinterpret_cast<const float2 *>(sl + 8 * k + cp),
+                                                make_float2(-kLog2e, -kLog2e));
+                        const float2 ndl = fmul2(*reinterpret_cast<const float2 *>(sl + 64 + 8 * k + cp),
+                                                 make_float2(-1.f, -1.f));
 #pragma unroll
                         for (int L = 0; L < 2; ++L) {
 #pragma unroll
