@@ -79,15 +79,15 @@ template <int D> struct BwdCfg {
     static constexpr int kHalfBox = A::box_bytes(kTile / 2);
     static constexpr int kTileBytes = kChunks * kBox;     // 128 rows x D bf16
     static constexpr int kHalfBytes = kChunks * kHalfBox; // 64 rows x D bf16
-    // dQ kernel: a stage holds a K and a V tile
-    static constexpr int kStages = (D == 128) ? 2 : 4;
-    static constexpr int kStageBytes = 2 * kTileBytes + 1024;
-    // the dq epilogue's inputs: the owned rows of q (one tile, its own region)
-    // and their RoPE (cos, sin) rows, D/32 boxes of 128 rows x 128 bytes of the
-    // fp32 table, loaded into the stage after the last K/V tile
-    static constexpr int kCsBytes = (D / 32) * kTile * 128;
-    static_assert(kCsBytes <= kStageBytes, "cos/sin rows must fit one stage");
-    static constexpr int kSmemB = kStages * kStageBytes + kTileBytes + 1024;
+    // dQ kernel: a ring of K tiles and a ring of V tiles (a V tile is released
+    // after its dP MMA, a K tile only after its dQ MMA), plus the owned dO rows;
+    // the dq epilogue's inputs go into freed slots after the last tile: the owned
+    // q rows into the V ring, their RoPE (cos, sin) rows (two 64-row halves of
+    // D/32 boxes of 16 pairs) into two K slots
+    static constexpr int kKStages = (D == 128) ? 3 : 4;
+    static constexpr int kVStages = (D == 128) ? 2 : 3;
+    static_assert(kKStages >= 3, "the cos/sin rows take two K slots besides the last K tile");
+    static constexpr int kSmemB = (kKStages + kVStages + 1) * kTileBytes + 1024;
     // dK/dV kernel: a ring of half tiles, each the Qhat and dO rows of one half
     // of a streamed query tile plus their 2 x 64 row statistics, so that a half
     // is reloaded as soon as its own MMAs are done
@@ -106,6 +106,7 @@ constexpr int kCsPieceBytes = 64 * 128;
 struct BwdBarriers {
     uint64_t own_full;
     uint64_t st_full[kMaxStages], st_empty[kMaxStages];
+    uint64_t v_full[kMaxStages], v_empty[kMaxStages];   // dQ kernel: the V ring
     uint64_t s_full[2], p_full[2];   // per half of the streamed tile (columns [64h, 64h+64))
     uint64_t acc_done;
     uint64_t drain;
@@ -130,6 +131,8 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     for (int s = 0; s < stages; ++s) {
         mbar_init(&bars.st_full[s], st_full_count);
         mbar_init(&bars.st_empty[s], 1);
+        mbar_init(&bars.v_full[s], 1);
+        mbar_init(&bars.v_empty[s], 1);
     }
     for (int h = 0; h < 2; ++h) {
         mbar_init(&bars.s_full[h], 1);
@@ -801,22 +804,25 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
             const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
-            const bf16 *__restrict__ qhat, const bf16 *__restrict__ dout,
+            const __grid_constant__ CUtensorMap map_do, const bf16 *__restrict__ qhat,
             const float *__restrict__ lse, const float *__restrict__ dlt,
             const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
             bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
             int n_qt, unsigned int *err, int stall) {
     using C = BwdCfg<D>;
-    constexpr int ST = C::kStages;
-    // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), and the
-    // resident A operands Qhat at 384 and dO at 448 (D/2 packed columns each)
-    constexpr uint32_t kTQ = 384, kTDO = 448;
+    constexpr int KS = C::kKStages, VS = C::kVStages;
+    // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), the resident
+    // Qhat A operand at 384 (D/2 packed columns) and packed dS at 448 (64 columns:
+    // k-step kk of 16 keys at [448 + 8 kk, +8)), so that dS of one key tile and
+    // S/dP of the next live side by side
+    constexpr uint32_t kTQ = 384, kTDS = 448;
     extern __shared__ uint8_t smem_raw[];
     __shared__ BwdBarriers bars;
     __shared__ EpiScratch escr;
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t *sStage = smem;
-    uint8_t *sX = smem + ST * C::kStageBytes;          // owned rows of q (swizzled boxes)
+    uint8_t *sK = smem;                                // KS K tiles
+    uint8_t *sV = sK + KS * C::kTileBytes;             // VS V tiles
+    uint8_t *sDO = sV + VS * C::kTileBytes;            // owned rows of dO (the dP MMA's A)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int BH = gridDim.x / n_qt;
@@ -834,11 +840,13 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
     // p_full[0]: packed dS of tile t in TMEM; p_full[1]: every softmax thread
-    // has S(t) and dP(t) in registers (the S columns may be overwritten)
+    // has S(t) and dP(t) in registers (their columns may be overwritten);
+    // s_full[1]: dQ(t) has read dS(t) (its columns may be overwritten)
     uint64_t *ds_ready = &bars.p_full[0];
     uint64_t *sdp_taken = &bars.p_full[1];
+    uint64_t *ds_free = &bars.s_full[1];
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 256, 1, ST, false);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 128, 1, KS > VS ? KS : VS, false);
     if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -854,38 +862,59 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_v);
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_cs);
+            tma_prefetch_desc(&map_do);
             const int row0 = sp.start + i * kTile;
+            // the owned rows of dO (the first dP needs them)
             mbar_expect_tx(&bars.x_full, C::kTileBytes);
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sX + c * C::kBox, &map_x, &bars.x_full, c * C::A::kCols, h, row0,
+                tma_load_4d(sDO + c * C::kBox, &map_do, &bars.x_full, c * C::A::kCols, h, row0,
                             sp.plane);
-            // tiles 0..T-1: K and V; "tile" T: the owned rows' (cos, sin) rows
-            int issued = 0;
-            for (int t = 0; t <= T; ++t) {
-                const int st = t % ST;
-                if (t >= ST && !mbar_wait(&bars.st_empty[st], ((t / ST) - 1) & 1, abort_flag)) {
-                    if (!*abort_flag) raise_error_b(err, abort_flag);
+            // K ring uses: K tiles 0..T-1, then the two (cos, sin) halves; V ring uses:
+            // V tiles 0..T-1, then the owned q rows
+            int k_issued = 0, v_issued = 0;
+            bool ok = true;
+            for (int u = 0; ok && u < T + 2; ++u) {
+                const int ks = u % KS;
+                if (u >= KS &&
+                    !(ok = mbar_wait(&bars.st_empty[ks], ((u / KS) - 1) & 1, abort_flag)))
                     break;
-                }
-                uint8_t *base = sStage + st * C::kStageBytes;
-                if (t == T) {
-                    mbar_expect_tx(&bars.st_full[st], C::kCsBytes);
-                    for (int c = 0; c < D / 32; ++c)
-                        tma_load_2d(base + c * kTile * 128, &map_cs, &bars.st_full[st], 32 * c,
-                                    row0);
+                uint8_t *kb = sK + ks * C::kTileBytes;
+                if (u < T) {
+                    mbar_expect_tx(&bars.st_full[ks], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_3d(kb + c * C::kBox, &map_k, &bars.st_full[ks], c * C::A::kCols,
+                                    sp.start + u * kTile, sp.plane * G + g);
                 } else {
-                    mbar_expect_tx(&bars.st_full[st], 2 * C::kTileBytes);
-                    for (int c = 0; c < C::kChunks; ++c) {
-                        tma_load_3d(base + c * C::kBox, &map_k, &bars.st_full[st],
-                                    c * C::A::kCols, sp.start + t * kTile, sp.plane * G + g);
-                        tma_load_4d(base + C::kTileBytes + c * C::kBox, &map_v, &bars.st_full[st],
-                                    c * C::A::kCols, g, sp.start + t * kTile, sp.plane);
-                    }
+                    // (cos, sin) rows [64 e, 64 e + 64) of the owned rows: D/32 pieces
+                    mbar_expect_tx(&bars.st_full[ks], (D / 32) * kCsPieceBytes);
+                    for (int c = 0; c < D / 32; ++c)
+                        tma_load_2d(kb + c * kCsPieceBytes, &map_cs, &bars.st_full[ks], 32 * c,
+                                    row0 + 64 * (u - T));
                 }
-                issued = t + 1;
+                ++k_issued;
+                if (u > T) continue;
+                const int vs = u % VS;
+                if (u >= VS &&
+                    !(ok = mbar_wait(&bars.v_empty[vs], ((u / VS) - 1) & 1, abort_flag)))
+                    break;
+                uint8_t *vb = sV + vs * C::kTileBytes;
+                mbar_expect_tx(&bars.v_full[vs], C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    if (u < T)
+                        tma_load_4d(vb + c * C::kBox, &map_v, &bars.v_full[vs], c * C::A::kCols,
+                                    g, sp.start + u * kTile, sp.plane);
+                    else
+                        tma_load_4d(vb + c * C::kBox, &map_x, &bars.v_full[vs], c * C::A::kCols,
+                                    h, row0, sp.plane);
+                }
+                ++v_issued;
             }
-            for (int t = max(0, issued - ST); t < issued; ++t)
-                mbar_wait(&bars.st_full[t % ST], (t / ST) & 1, nullptr);
+            if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+            // drain: every copy issued by this CTA lands before it exits
+            for (int x = max(0, k_issued - KS); x < k_issued; ++x)
+                mbar_wait(&bars.st_full[x % KS], (x / KS) & 1, nullptr);
+            for (int x = max(0, v_issued - VS); x < v_issued; ++x)
+                mbar_wait(&bars.v_full[x % VS], (x / VS) & 1, nullptr);
             mbar_wait(&bars.x_full, 0, nullptr);
         }
     } else if (warp == kWarpMma) {
@@ -895,58 +924,60 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile, 0, 0);
             const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
             using A = typename C::A;
-            const uint64_t dKk0 = smem_desc(smem_u32(sStage), 16, A::kSBO, A::kMode);
-            const uint64_t dVk0 = smem_desc(smem_u32(sStage + C::kTileBytes), 16, A::kSBO, A::kMode);
-            const uint64_t dKm0 = smem_desc(smem_u32(sStage), C::kBox, A::kSBO, A::kMode);
-            constexpr uint64_t kStep = (uint64_t)C::kStageBytes >> 4;
-            // S = Qhat Khat^T and dP = dO V^T (A in TMEM), full 128-key tiles: the
-            // TS form at N = 128 runs at the full MMA rate (N = 64 does not)
-            auto issue_s = [&](int t) {
-                const uint64_t so = (uint64_t)(t % ST) * kStep;
+            const uint64_t dKk0 = smem_desc(smem_u32(sK), 16, A::kSBO, A::kMode);
+            const uint64_t dVk0 = smem_desc(smem_u32(sV), 16, A::kSBO, A::kMode);
+            const uint64_t dKm0 = smem_desc(smem_u32(sK), C::kBox, A::kSBO, A::kMode);
+            const uint64_t dDO = smem_desc(smem_u32(sDO), 16, A::kSBO, A::kMode);
+            constexpr uint64_t kStep = (uint64_t)C::kTileBytes >> 4;
+            // S = Qhat Khat^T (A in TMEM) and dP = dO V^T (both operands in shared
+            // memory), full 128-key tiles (N = 128 runs at the full MMA rate)
+            auto issue_sdp = [&](int t) {
+                const uint64_t ko = (uint64_t)(t % KS) * kStep, vo = (uint64_t)(t % VS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts_w(tmem, tmem + kTQ + kk * 8, dKk0 + so + kmajor_off<D>(kk), idesc_s, kk > 0);
-            };
-            auto issue_dp = [&](int t) {
-                const uint64_t so = (uint64_t)(t % ST) * kStep;
+                    mma_ts_w(tmem, tmem + kTQ + kk * 8, dKk0 + ko + kmajor_off<D>(kk), idesc_s, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    mma_ts_w(tmem + 128, tmem + kTDO + kk * 8, dVk0 + so + kmajor_off<D>(kk), idesc_s,
-                           kk > 0);
+                    mma_ss_w(tmem + 128, dDO + kmajor_off<D>(kk), dVk0 + vo + kmajor_off<D>(kk),
+                             idesc_s, kk > 0);
                 mma_commit_w(&bars.s_full[0]);         // S and dP of tile t are in TMEM
+                mma_commit_w(&bars.v_empty[t % VS]);   // V tile t is read
             };
             bool ok = !stall ||
                       __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
             ok = ok && mbar_wait_w(&bars.own_full, 0, abort_flag) &&
-                 mbar_wait_w(&bars.st_full[0], 0, abort_flag);
+                 mbar_wait_w(&bars.x_full, 0, abort_flag) &&
+                 mbar_wait_w(&bars.st_full[0], 0, abort_flag) &&
+                 mbar_wait_w(&bars.v_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
+                issue_sdp(0);
             }
-            // Per tile t: once the softmax warps hold S(t) and dP(t) in registers,
-            // S(t+1) is issued (it runs during the softmax of t); once dS(t) is
-            // packed over the dP columns, dQ(t) and then dP(t+1), which in issue
-            // order cannot overwrite dS(t) before dQ(t) has read it.
+            // Per tile t: once every softmax thread holds S(t) and dP(t) in registers,
+            // S(t+1) and dP(t+1) are issued (they run during the softmax of t); once
+            // dS(t) is packed in its own columns, dQ(t). The softmax of t+1 writes
+            // dS(t+1) only after dQ(t) has read dS(t) (ds_free).
             for (int t = 0; ok && t < T; ++t) {
-                const int st = t % ST;
-                const uint64_t so = (uint64_t)st * kStep;
+                const int ks = t % KS;
+                const uint64_t ko = (uint64_t)ks * kStep;
                 if (t + 1 < T) {
                     if (!(ok = mbar_wait_w(sdp_taken, t & 1, abort_flag) &&
-                               mbar_wait_w(&bars.st_full[(t + 1) % ST], ((t + 1) / ST) & 1,
-                                         abort_flag)))
+                               mbar_wait_w(&bars.st_full[(t + 1) % KS], ((t + 1) / KS) & 1,
+                                           abort_flag) &&
+                               mbar_wait_w(&bars.v_full[(t + 1) % VS], ((t + 1) / VS) & 1,
+                                           abort_flag)))
                         break;
                     tc_fence_after();
-                    issue_s(t + 1);
+                    issue_sdp(t + 1);
                 }
                 if (!(ok = mbar_wait_w(ds_ready, t & 1, abort_flag))) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts_w(tmem + 256, tmem + 128 + packed_col(kk), dKm0 + so + mnmajor_off<D>(kk),
-                           idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(&bars.st_empty[st]);
-                if (t + 1 < T) issue_dp(t + 1);
+                    mma_ts_w(tmem + 256, tmem + kTDS + kk * 8, dKm0 + ko + mnmajor_off<D>(kk),
+                             idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                mma_commit_w(&bars.st_empty[ks]);      // K tile t is read
+                mma_commit_w(ds_free);
             }
             if (ok) mma_commit_w(&bars.acc_done);
             else if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
@@ -962,21 +993,17 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         const float sl2 = kLog2e * rsqrtf((float)D);
         const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
         const float dl = tq < S ? dlt[qrow0 + tq] : 0.f;
-        if (wg < 2) {
-            // the owned Qhat (warpgroup 0) and dO (warpgroup 1) rows become TMEM-resident
-            // A operands (lane = row; a 32-bit column holds two consecutive bf16, the lower
-            // index in the low half)
+        if (wg == 0) {
+            // the owned Qhat rows become the TMEM-resident A operand of S (lane = row;
+            // a 32-bit column holds two consecutive bf16, the lower index in the low half)
             uint32_t xa[D / 2];
-            const uint4 *src = wg == 0
-                ? reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D)
-                : reinterpret_cast<const uint4 *>(
-                      dout + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D);
+            const uint4 *src = reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D);
 #pragma unroll
             for (int c = 0; c < D / 8; ++c) {
                 const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
                 xa[4 * c] = z.x; xa[4 * c + 1] = z.y; xa[4 * c + 2] = z.z; xa[4 * c + 3] = z.w;
             }
-            const uint32_t dst = tmem + (wg == 0 ? kTQ : kTDO) + lane_off;
+            const uint32_t dst = tmem + kTQ + lane_off;
             if constexpr (D == 128) tmem_st64_sync(dst, xa);
             else if constexpr (D == 64) tmem_st32_sync(dst, xa);
             else tmem_st16_sync(dst, xa);
@@ -1004,7 +1031,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 uint32_t sv[32], dpv[32];
                 tmem_ld32x2_sync(tS, sv, tP, dpv);
                 tc_fence_before();
-                mbar_arrive(sdp_taken);                 // S(t+1) may now be issued
+                mbar_arrive(sdp_taken);                 // S(t+1), dP(t+1) may now be issued
                 // only tiles that reach past the owned rows' diagonal take the select
                 // element pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
                 auto body = [&](auto masked) {
@@ -1028,18 +1055,28 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 if (interior) body(std::false_type{});
                 else body(std::true_type{});
             }
-            tmem_st16_sync(tP, dd);                     // packed dS over this warpgroup's dP columns
+            if (t > 0) {   // dQ(t-1) has read the dS columns
+                ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (t - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            tmem_st16_sync(tmem + lane_off + kTDS + 16 * wg, dd);   // packed dS, k-steps 2 wg, 2 wg + 1
             tc_fence_before();
             mbar_arrive(ds_ready);
         }
-        // ---- epilogue: dq and the CTA's dgamma_q partial from dQhat in TMEM; q rows
-        // (own region) and their (cos, sin) rows (the stage after the last K/V
-        // tile, box wg = pairs [16 wg, 16 wg + 16)) were loaded by the producer
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, 0, abort_flag) &&
-                                                 mbar_wait(&bars.x_full, 0, abort_flag) &&
-                                                 mbar_wait(&bars.st_full[T % ST], (T / ST) & 1,
-                                                           abort_flag));
-        const uint8_t *cs_row = sStage + (T % ST) * C::kStageBytes + wg * kTile * 128 + r * 128;
+        // ---- epilogue: dq and the CTA's dgamma_q partial from dQhat in TMEM; the
+        // producer loaded the q rows into the V slot after the last V tile and
+        // their (cos, sin) rows into the two K slots after the last K tile (row
+        // half r/64; piece wg = pairs [16 wg, 16 wg + 16))
+        if (ok) ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars.acc_done, 0, abort_flag) &&
+                                mbar_wait(&bars.v_full[T % VS], (T / VS) & 1, abort_flag) &&
+                                mbar_wait(&bars.st_full[T % KS], (T / KS) & 1, abort_flag) &&
+                                mbar_wait(&bars.st_full[(T + 1) % KS], ((T + 1) / KS) & 1,
+                                          abort_flag));
+        const uint8_t *sX = sV + (T % VS) * C::kTileBytes;
+        const uint8_t *cs_row = sK + ((T + (r >> 6)) % KS) * C::kTileBytes + wg * kCsPieceBytes +
+                                (r & 63) * 128;
         finish_rows_call<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
                             dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D, part);
         if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
@@ -1196,15 +1233,21 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     using C = BwdCfg<D>;
     const int n_qt = (p.max_len + kTile - 1) / kTile;
     const long blocks = (long)p.units * p.H * n_qt;
-    CUtensorMap mx, mcs;
-    cudaError_t e = make_epi_maps<D>(p, ep, p.H, kTile, mx, mcs);
+    CUtensorMap mx, mcs, mdo;
+    cudaError_t e = make_epi_maps<D>(p, ep, p.H, 64, mx, mcs);
+    if (e != cudaSuccess) return e;
+    // dO [B, S, H, D] with 128-row boxes (the owned rows, the dP MMA's A operand)
+    RowEpilogue eo = ep;
+    eo.x = dout;
+    CUtensorMap unused;
+    e = make_epi_maps<D>(p, eo, p.H, kTile, mdo, unused);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, (const bf16 *)qhat, (const bf16 *)dout, lse, dlt, ep.gamma,
-        ep.rstd, (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err,
+        m.k, m.v, mx, mcs, mdo, (const bf16 *)qhat, lse, dlt, ep.gamma, ep.rstd,
+        (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err,
         (test_stall_mask() & STALL_DQ_TC) != 0);
     return cudaGetLastError();
 }
