@@ -110,7 +110,8 @@ struct BwdBarriers {
     uint64_t s_full[2], p_full[2];   // per half of the streamed tile (columns [64h, 64h+64))
     uint64_t acc_done;
     uint64_t drain;
-    uint64_t x_full;                 // dQ kernel: the owned rows of q are in shared memory
+    uint64_t x_full;                 // dQ kernel: the owned rows of dO are in shared memory
+    uint64_t dp_full, dp_taken;      // dQ kernel: dP of a tile is in TMEM / in every softmax thread
     uint64_t stall;                  // never arrived on (xt_test_inject_stall)
     uint32_t tmem_base;
     int abort_flag;
@@ -142,6 +143,8 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     mbar_init(&bars.acc_done, 1);
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.x_full, 1);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_taken, 32 * 4 * kSoftmaxWGs);
     mbar_init(&bars.stall, 1);
     fence_barrier_init();
 }
@@ -839,11 +842,12 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;   // [.., H, S, ..] rows
     const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
-    // p_full[0]: packed dS of tile t in TMEM; p_full[1]: every softmax thread
-    // has S(t) and dP(t) in registers (their columns may be overwritten);
-    // s_full[1]: dQ(t) has read dS(t) (its columns may be overwritten)
+    // s_full[0] / dp_full: S(t) / dP(t) are in TMEM; p_full[1] / dp_taken: every
+    // softmax thread holds S(t) / dP(t) in registers (the columns may be
+    // overwritten); p_full[0]: packed dS(t) is in TMEM; s_full[1]: dQ(t) has read
+    // dS(t) (its columns may be overwritten)
     uint64_t *ds_ready = &bars.p_full[0];
-    uint64_t *sdp_taken = &bars.p_full[1];
+    uint64_t *s_taken = &bars.p_full[1];
     uint64_t *ds_free = &bars.s_full[1];
 
     if (threadIdx.x == 0) init_bwd_barriers(bars, 128, 1, KS > VS ? KS : VS, false);
@@ -931,16 +935,20 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             constexpr uint64_t kStep = (uint64_t)C::kTileBytes >> 4;
             // S = Qhat Khat^T (A in TMEM) and dP = dO V^T (both operands in shared
             // memory), full 128-key tiles (N = 128 runs at the full MMA rate)
-            auto issue_sdp = [&](int t) {
-                const uint64_t ko = (uint64_t)(t % KS) * kStep, vo = (uint64_t)(t % VS) * kStep;
+            auto issue_s = [&](int t) {
+                const uint64_t ko = (uint64_t)(t % KS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts_w(tmem, tmem + kTQ + kk * 8, dKk0 + ko + kmajor_off<D>(kk), idesc_s, kk > 0);
+                mma_commit_w(&bars.s_full[0]);         // S of tile t is in TMEM
+            };
+            auto issue_dp = [&](int t) {
+                const uint64_t vo = (uint64_t)(t % VS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss_w(tmem + 128, dDO + kmajor_off<D>(kk), dVk0 + vo + kmajor_off<D>(kk),
                              idesc_s, kk > 0);
-                mma_commit_w(&bars.s_full[0]);         // S and dP of tile t are in TMEM
+                mma_commit_w(&bars.dp_full);           // dP of tile t is in TMEM
                 mma_commit_w(&bars.v_empty[t % VS]);   // V tile t is read
             };
             bool ok = !stall ||
@@ -951,24 +959,30 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                  mbar_wait_w(&bars.v_full[0], 0, abort_flag);
             if (ok) {
                 tc_fence_after();
-                issue_sdp(0);
+                issue_s(0);
+                issue_dp(0);
             }
-            // Per tile t: once every softmax thread holds S(t) and dP(t) in registers,
-            // S(t+1) and dP(t+1) are issued (they run during the softmax of t); once
-            // dS(t) is packed in its own columns, dQ(t). The softmax of t+1 writes
-            // dS(t+1) only after dQ(t) has read dS(t) (ds_free).
+            // Per tile t: once every softmax thread holds S(t) in registers, S(t+1) is
+            // issued, and once they hold dP(t), dP(t+1) (both run during the softmax of
+            // t, and the dP loads overlap S(t+1)); once dS(t) is packed in its own
+            // columns, dQ(t). The softmax of t+1 writes dS(t+1) only after dQ(t) has
+            // read dS(t) (ds_free).
             for (int t = 0; ok && t < T; ++t) {
                 const int ks = t % KS;
                 const uint64_t ko = (uint64_t)ks * kStep;
                 if (t + 1 < T) {
-                    if (!(ok = mbar_wait_w(sdp_taken, t & 1, abort_flag) &&
+                    if (!(ok = mbar_wait_w(s_taken, t & 1, abort_flag) &&
                                mbar_wait_w(&bars.st_full[(t + 1) % KS], ((t + 1) / KS) & 1,
-                                           abort_flag) &&
+                                           abort_flag)))
+                        break;
+                    tc_fence_after();
+                    issue_s(t + 1);
+                    if (!(ok = mbar_wait_w(&bars.dp_taken, t & 1, abort_flag) &&
                                mbar_wait_w(&bars.v_full[(t + 1) % VS], ((t + 1) / VS) & 1,
                                            abort_flag)))
                         break;
                     tc_fence_after();
-                    issue_sdp(t + 1);
+                    issue_dp(t + 1);
                 }
                 if (!(ok = mbar_wait_w(ds_ready, t & 1, abort_flag))) break;
                 tc_fence_after();
@@ -1029,9 +1043,17 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             uint32_t dd[kWgCols / 2];
             {
                 uint32_t sv[32], dpv[32];
-                tmem_ld32x2_sync(tS, sv, tP, dpv);
+                tmem_ld32_sync(tS, sv);
                 tc_fence_before();
-                mbar_arrive(sdp_taken);                 // S(t+1), dP(t+1) may now be issued
+                mbar_arrive(s_taken);                   // S(t+1) may now be issued
+                if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                tmem_ld32_sync(tP, dpv);
+                tc_fence_before();
+                mbar_arrive(&bars.dp_taken);            // dP(t+1) may now be issued
                 // only tiles that reach past the owned rows' diagonal take the select
                 // element pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
                 auto body = [&](auto masked) {
