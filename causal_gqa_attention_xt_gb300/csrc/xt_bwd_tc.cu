@@ -521,13 +521,16 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
             const size_t row0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
+                // column kq of the half: lse at 4 (kq / 2) + kq % 2, Dlt two words on
+                // (one 16-byte word per column pair, the softmax's load unit)
                 const int kq = lane + 32 * e, q = q0 + kq;
+                const int o = 4 * (kq >> 1) + (kq & 1);
                 if (q < S) {
-                    cp_async4(sl + kq, lse + row0 + q);
-                    cp_async4(sl + 64 + kq, dlt + row0 + q);
+                    cp_async4(sl + o, lse + row0 + q);
+                    cp_async4(sl + o + 2, dlt + row0 + q);
                 } else {
-                    sl[kq] = 0.f;
-                    sl[64 + kq] = 0.f;
+                    sl[o] = 0.f;
+                    sl[o + 2] = 0.f;
                 }
             }
             // each lane's copies become one pending arrival of the stage barrier
@@ -661,26 +664,33 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
         const int hf = wg >> 1;                         // this warpgroup's half of the tile
         for (int t = 0; t < T; ++t) {
             const int x = 2 * t + hf, hs = x % HS;
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[hf], t & 1, abort_flag) &&
-                                             mbar_wait(&bars.st_full[hs], (x / HS) & 1, abort_flag));
+            // the half stage first: its row statistics are loaded into registers while
+            // S^T/dP^T are still being computed (their shared-memory loads would
+            // otherwise queue behind the tensor core's operand reads)
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[hs], (x / HS) & 1, abort_flag));
+            if (!ok) break;
+            float4 st4[4];
+            {
+                // (lse, lse, Dlt, Dlt) of the column pairs 8 k + 2 (lane % 4) of this
+                // warpgroup's 32 columns
+                const float4 *sl4 = reinterpret_cast<const float4 *>(
+                    sStage + hs * C::kHStageBytes + 2 * C::kHalfBytes);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) st4[k] = sl4[16 * (wg & 1) + 4 * k + (lane & 3)];
+            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[hf], t & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int u = j + ((t0 + t) % nU);
             const int c0 = wg * kWgCols;                // this warpgroup's columns
             const int q0 = u * kTile + c0;
-            // statistics of the half: lse at [0,64), Dlt at [64,128), this warpgroup's
-            // 32 columns from 32 (wg & 1)
-            const float *sl = reinterpret_cast<const float *>(sStage + hs * C::kHStageBytes +
-                                                              2 * C::kHalfBytes) +
-                              32 * (wg & 1);
             const uint32_t tS = tmem + lane_off + c0;         // S^T columns
             const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
             // no masking when every query of these columns is at/after every owned key and < S
             const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + kWgCols <= S);
             // 16-lane TMEM shapes (xt_tc.cuh): this thread holds rows
             // 16 L + lane/4 + 8 jh of its warp's 32 and the column pairs 8 k + 2 (lane % 4)
-            // of the warpgroup's 32, so it needs the statistics of 8 columns only: one
-            // 8-byte load per pair, 4 distinct conflict-free addresses per warp.
+            // of the warpgroup's 32, so it needs the statistics of 8 columns only (st4).
             uint32_t pp[kWgCols / 2], dd[kWgCols / 2];
             {
                 uint32_t sv[32], dpv[32];
@@ -691,10 +701,9 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                 auto body = [&](auto masked) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const float2 nl = fmul2(*reinterpret_cast<const float2 *>(sl + 8 * k + cp),
+                        const float2 nl = fmul2(make_float2(st4[k].x, st4[k].y),
                                                 make_float2(-kLog2e, -kLog2e));
-                        const float2 ndl = fmul2(*reinterpret_cast<const float2 *>(sl + 64 + 8 * k + cp),
-                                                 make_float2(-1.f, -1.f));
+                        const float2 ndl = make_float2(-st4[k].z, -st4[k].w);
 #pragma unroll
                         for (int L = 0; L < 2; ++L) {
 #pragma unroll

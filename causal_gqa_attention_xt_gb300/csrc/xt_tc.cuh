@@ -49,20 +49,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// parked by the hardware until the phase completes or about `hint_ns` pass, so
+// a waiting warp takes no issue slots from the warps that share its SM
+// sub-partition (in the tensor-core kernels a spinning MMA or softmax warp
+// measurably slowed the softmax warps beside it).
+__device__ __forceinline__ bool mbar_try_wait_park(uint64_t *bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+
 // Waits until the phase with parity `parity` has completed. Gives up after
-// ~kWaitLimitNs (or as soon as *abort is set) and returns false.
+// ~kWaitLimitNs (or soon after *abort is set) and returns false.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kParkHintNs = 20000;           // 20 us between abort / limit checks
 
 __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
                                               volatile int *abort_flag, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255u) == 0) {
-            if (abort_flag && *abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait_park(bar, parity, kParkHintNs)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
