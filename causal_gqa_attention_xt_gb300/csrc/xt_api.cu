@@ -216,9 +216,10 @@ int run_fwd(const Problem &p, const void *q, const void *k, const void *v, const
     });
 }
 
-// The backward pipeline: RoPE table, Dlt, dK/dV (+ chunk reduce for split key
-// tiles), dQ, the row epilogue where the attention kernels do not finish the
-// rows themselves (fp32 problems; k rows of split bf16 problems), dgamma reduce.
+// The backward pipeline: RoPE table; bf16: dQ (which also writes Dlt), dK/dV
+// (+ chunk reduce for split key tiles); fp32: Dlt, dK/dV, dQ; then the row
+// epilogue where the attention kernels do not finish the rows themselves (fp32
+// problems; k rows of split bf16 problems) and the dgamma reduce.
 int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const float *gamma_q,
             const float *gamma_k, const void *out, const float *lse, const void *q_hat,
             const void *k_hat, const float *rstd_q, const float *rstd_k, const void *dout,
@@ -244,13 +245,21 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
 
     int st = timed_launch(KID_ROPE_TABLE, s, [&] { return launch_rope_table(p, tab, err, s); });
     if (st != XT_OK) return st;
-    st = timed_launch(KID_BWD_PRE, s, [&] {
-        return launch_bwd_pre(p, out, dout, dlt, err, s);
-    });
-    if (st != XT_OK) return st;
     const bool tc = p.dtype == XT_BF16;
     const bool fuse_k = tc && dkdv_part_bytes(p) == 0;   // the dK/dV kernel finishes dk
+    if (!tc) {
+        st = timed_launch(KID_BWD_PRE, s, [&] {
+            return launch_bwd_pre(p, out, dout, dlt, err, s);
+        });
+        if (st != XT_OK) return st;
+    }
     if (tc) {
+        // dQ first: it also writes Dlt, which the dK/dV kernel reads
+        const RowEpilogue ep = {q, gamma_q, rstd_q, tab, dq, part_q};
+        st = timed_launch(KID_BWD_DQ_TC, s, [&] {
+            return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, out, lse, dlt, ep, err, s);
+        });
+        if (st != XT_OK) return st;
         float *part_dkdv = (float *)(ws + w.off_dkdv);
         const RowEpilogue ek = {k, gamma_k, rstd_k, tab, dk, part_k};
         st = timed_launch(KID_BWD_DKDV_TC, s, [&] {
@@ -264,11 +273,6 @@ int run_bwd(const Problem &p, const void *q, const void *k, const void *v, const
             });
             if (st != XT_OK) return st;
         }
-        const RowEpilogue ep = {q, gamma_q, rstd_q, tab, dq, part_q};
-        st = timed_launch(KID_BWD_DQ_TC, s, [&] {
-            return launch_bwd_dq_tc(p, q_hat, k_hat, v, dout, lse, dlt, ep, err, s);
-        });
-        if (st != XT_OK) return st;
     } else {
         st = timed_launch(KID_BWD_DKDV_SIMT, s, [&] {
             return launch_bwd_dkdv_simt(p, q_hat, k_hat, v, dout, lse, dlt, dkhat, dv, s);

@@ -817,7 +817,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
             const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
             const __grid_constant__ CUtensorMap map_do, const bf16 *__restrict__ qhat,
-            const float *__restrict__ lse, const float *__restrict__ dlt,
+            const bf16 *__restrict__ out, const float *__restrict__ lse, float *__restrict__ dlt,
             const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
             bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
             int n_qt, unsigned int *err, int stall) {
@@ -1015,7 +1015,6 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
-        const float dl = tq < S ? dlt[qrow0 + tq] : 0.f;
         if (wg == 0) {
             // the owned Qhat rows become the TMEM-resident A operand of S (lane = row;
             // a 32-bit column holds two consecutive bf16, the lower index in the low half)
@@ -1038,8 +1037,40 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             escr.rstd[r] = tq < S ? rstd_q[((size_t)sp.plane * sr.S + sp.start + tq) * H + h] : 0.f;
             if (r < D) escr.gamma[r] = gamma_q[r];
         }
-        bool ok = true;
-        for (int t = 0; t < T; ++t) {
+        // Dlt = rowsum(dO o O) of the owned rows (the softmax backward's row term;
+        // the dK/dV kernel, launched after this one, reads it): warpgroup wg sums the
+        // columns [wg D/4, (wg + 1) D/4) of its thread's row, dO from the TMA'd tile,
+        // O from global memory; the four parts are added in warpgroup order. It
+        // overlaps the first S and dP MMAs.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.x_full, 0, abort_flag));
+        {
+            using A = Atoms<D>;
+            float part0 = 0.f, part1 = 0.f;
+            if (ok && tq < S) {
+                const uint4 *orow = reinterpret_cast<const uint4 *>(
+                    out + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D + wg * (D / 4));
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    const int col = wg * (D / 4) + 8 * c;
+                    const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                                    r * A::kRowBytes + (col % A::kCols) * 2);
+                    const uint4 g = *reinterpret_cast<const uint4 *>(sDO + swizzled<A::kRowBytes>(off));
+                    const uint4 o = orow[c];
+                    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        part0 = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), part0);
+                        part1 = fmaf(__uint_as_float(gw[e] & 0xffff0000u),
+                                     __uint_as_float(ow[e] & 0xffff0000u), part1);
+                    }
+                }
+            }
+            escr.dot[wg][r] = part0 + part1;
+        }
+        softmax_bar_sync();   // every softmax thread reaches this (no wait above is unbounded)
+        const float dl = ((escr.dot[0][r] + escr.dot[1][r]) + escr.dot[2][r]) + escr.dot[3][r];
+        if (ok && wg == 0 && tq < S) dlt[qrow0 + tq] = dl;
+        for (int t = 0; ok && t < T; ++t) {
             ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], t & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -1259,7 +1290,7 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
 
 template <int D>
 cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, const void *dout,
-                        const float *lse, const float *dlt, const RowEpilogue &ep,
+                        const void *out, const float *lse, float *dlt, const RowEpilogue &ep,
                         unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
     const int n_qt = (p.max_len + kTile - 1) / kTile;
@@ -1277,7 +1308,7 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
                              C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, mdo, (const bf16 *)qhat, lse, dlt, ep.gamma, ep.rstd,
+        m.k, m.v, mx, mcs, mdo, (const bf16 *)qhat, (const bf16 *)out, lse, dlt, ep.gamma, ep.rstd,
         (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err,
         (test_stall_mask() & STALL_DQ_TC) != 0);
     return cudaGetLastError();
@@ -1295,12 +1326,12 @@ cudaError_t run_dkdv(const Problem &p, const void *qhat, const void *khat, const
 
 template <int D>
 cudaError_t run_dq(const Problem &p, const void *qhat, const void *khat, const void *v,
-                   const void *dout, const float *lse, const float *dlt, const RowEpilogue &ep,
-                   unsigned int *err, cudaStream_t st) {
+                   const void *dout, const void *out, const float *lse, float *dlt,
+                   const RowEpilogue &ep, unsigned int *err, cudaStream_t st) {
     BwdMaps m;
     cudaError_t e = make_maps<D>(p, qhat, khat, v, dout, m);
     if (e != cudaSuccess) return e;
-    return launch_dq_d<D>(p, m, qhat, dout, lse, dlt, ep, err, st);
+    return launch_dq_d<D>(p, m, qhat, dout, out, lse, dlt, ep, err, st);
 }
 
 }  // namespace
@@ -1337,11 +1368,11 @@ size_t dq_part_count(const Problem &p) {
 }
 
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
-                             const void *dout, const float *lse, const float *dlt,
+                             const void *dout, const void *out, const float *lse, float *dlt,
                              const RowEpilogue &ep, unsigned int *err, cudaStream_t st) {
-    if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
-    if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
-    if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, lse, dlt, ep, err, st);
+    if (p.D == 128) return run_dq<128>(p, qhat, khat, v, dout, out, lse, dlt, ep, err, st);
+    if (p.D == 64) return run_dq<64>(p, qhat, khat, v, dout, out, lse, dlt, ep, err, st);
+    if (p.D == 32) return run_dq<32>(p, qhat, khat, v, dout, out, lse, dlt, ep, err, st);
     return cudaErrorInvalidValue;
 }
 

@@ -142,8 +142,10 @@ cudaError_t launch_bwd_dkdv_tc(const Problem &p, const void *qhat, const void *k
                                const RowEpilogue &ek, unsigned int *err, cudaStream_t st);
 cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat, void *dv,
                                cudaStream_t st);
+// The bf16 dQ kernel also computes Dlt = rowsum(dO o O) of its rows and writes
+// it to dlt, for the dK/dV kernel launched after it.
 cudaError_t launch_bwd_dq_tc(const Problem &p, const void *qhat, const void *khat, const void *v,
-                             const void *dout, const float *lse, const float *dlt,
+                             const void *dout, const void *out, const float *lse, float *dlt,
                              const RowEpilogue &ep, unsigned int *err, cudaStream_t st);
 
 // ---- fp32 CUDA-core flash kernels (xt_simt.cu) ----
