@@ -22,28 +22,31 @@
 //
 // TMEM: S (or S^T) in columns [0,128), dP (or dP^T) in [128,256), the
 // accumulators from 256. Four softmax warpgroups split the streamed tile's 128
-// columns (warpgroup w takes [32w, 32w+32)), form P and dS, and write them back
-// as packed bf16 over the first 16 of the columns they themselves read, so no
-// two warpgroups race. The accumulating MMAs (TS form, A from TMEM) read those
-// packed columns k-step by k-step; the causal-mask select runs only on tiles
-// that cross the diagonal or the end of the sequence.
+// columns (warpgroup w takes [32w, 32w+32)) and form P and dS; the
+// accumulating MMAs (TS form, A from TMEM) read them packed as bf16 k-step by
+// k-step; the causal-mask select runs only on tiles that cross the diagonal or
+// the end of the sequence.
 //
 // dK/dV pipeline: S^T and dP^T are issued per half of the streamed tile
 // (queries [64h, 64h+64), N = 64), each half with its own "S ready" and "P
-// ready" mbarriers, warpgroups 2h and 2h+1 being that half's. Once half h's P/dS
-// are in TMEM, the MMA thread issues that half's 4 k-steps of dV and dKhat and
-// then S^T/dP^T of the same half of the next tile: the tensor core works on one
-// half while the other half's softmax runs. One thread's tcgen05.mma
-// operations execute in issue order, so the next tile's S/dP cannot overwrite
-// P/dS before they are read.
+// ready" mbarriers, warpgroups 2h and 2h+1 being that half's, which write
+// packed P^T/dS^T over the first 16 of the columns they read. Once half h's
+// P/dS are in TMEM, the MMA warp issues that half's 4 k-steps of dV and dKhat
+// and then S^T/dP^T of the same half of the next tile: the tensor core works on
+// one half while the other half's softmax runs. tcgen05.mma operations issued
+// by one thread execute in issue order, so the next tile's S/dP cannot
+// overwrite P/dS before they are read. The softmax threads hold their columns
+// as 16-lane TMEM fragments, so each needs the (lse, Dlt) of 8 columns only,
+// loaded from the half stage as soon as it lands.
 //
-// dQ pipeline: the S/dP MMAs are TS-form (Qhat and dO of the owned rows are
-// TMEM-resident A operands), which at N = 64 runs well below the full rate, so
-// the tiles stay whole. Each warpgroup writes its packed dS over its own dP
-// columns; as soon as every softmax thread holds S(t) and dP(t) in registers,
-// the MMA thread issues S(t+1) (it runs during the softmax of t), and once
-// dS(t) is in TMEM, dQ(t) followed by dP(t+1), which in issue order cannot
-// overwrite dS(t) before dQ(t) has read it.
+// dQ pipeline: S = Qhat Khat^T is TS-form (the owned Qhat rows are a
+// TMEM-resident A operand), dP = dO V^T SS-form (the owned dO rows in shared
+// memory); packed dS has its own 64 columns. As soon as every softmax thread
+// holds S(t) in registers, S(t+1) is issued, and dP(t+1) once they hold dP(t),
+// so both run during the softmax of t; dQ(t) follows once dS(t) is in TMEM.
+// K and V tiles come through separate rings (a V tile is released after its dP
+// MMA, a K tile after its dQ MMA). The kernel also computes Dlt = rowsum(dO o
+// O) of its rows and writes it for the dK/dV kernel, which is launched after it.
 //
 // An mbarrier poll right after tcgen05.commit stalls the issuing thread until
 // earlier MMAs drain, so the TMA-arrival check for the next tile is done by the

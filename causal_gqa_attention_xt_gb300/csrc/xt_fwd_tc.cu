@@ -8,13 +8,17 @@
 // accumulation and softmax). Keys j > t are skipped; the pages' additive
 // -1e9 mask makes their probabilities exactly 0 in fp32 anyway.
 //
-// One CTA computes two consecutive 128-row query tiles (2p, 2p+1) of one
-// (batch, head), ping-ponging them so that the tensor core works on one tile
-// while the softmax warps work on the other:
+// A work item is two consecutive 128-row query tiles (2p, 2p+1) of one
+// (batch, head); a persistent grid of one CTA per SM walks the items (longest
+// first), ping-ponging the item's two tiles so that the tensor core works on
+// one while the softmax warps work on the other:
 //   warps 0-3  softmax + epilogue of query tile 0 (thread = one query row)
 //   warps 4-7  softmax + epilogue of query tile 1
-//   warp  8    TMA producer: each item's Q tiles, then K and V tiles into two rings
-//   warp  9    TMEM allocator and MMA issuer (one thread)
+//   warp  8    TMA producer: each item's Q tiles, then its K and V tiles into
+//              two rings (a K tile is released after its last S MMA, an
+//              iteration before its V tile)
+//   warp  9    TMEM allocator and MMA issuer (the whole warp runs the issue
+//              loop; one elected lane issues each MMA)
 // TMEM (512 columns): S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
 // S_i = Q_i K^T is an SS MMA (both operands K-major, 128B swizzle); the
 // softmax warps overwrite the first 64 columns of S_i with P_i as packed
