@@ -115,6 +115,7 @@ struct BwdBarriers {
     uint64_t drain;
     uint64_t x_full;                 // dQ kernel: the owned rows of dO are in shared memory
     uint64_t dp_full, dp_taken;      // dQ kernel: dP of a tile is in TMEM / in every softmax thread
+    uint64_t do_free;                // dQ kernel: the item's dP MMAs and its Dlt have read the dO rows
     uint64_t stall;                  // never arrived on (xt_test_inject_stall)
     uint32_t tmem_base;
     int abort_flag;
@@ -148,6 +149,7 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     mbar_init(&bars.x_full, 1);
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_taken, 32 * 4 * kSoftmaxWGs);
+    mbar_init(&bars.do_free, 2);   // the last dP MMA's commit + the softmax threads after Dlt
     mbar_init(&bars.stall, 1);
     fence_barrier_init();
 }
@@ -196,6 +198,39 @@ __device__ __forceinline__ void softmax_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(32 * 4 * kSoftmaxWGs) : "memory");
 }
 
+// Named barrier 1 for the 512 softmax threads with an OR over their flags: every
+// thread gets the same answer (the persistent dQ kernel's softmax threads
+// decide together whether to stop, so that no named barrier is left waiting).
+__device__ __forceinline__ bool softmax_bar_any(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n"
+        " bar.red.or.pred p, 1, %2, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r) : "r"((uint32_t)v), "n"(32 * 4 * kSoftmaxWGs) : "memory");
+    return r != 0;
+}
+
+// Work item w of the dQ kernel: query tile i of (unit, head) bh, longest first
+// (i descending, heads and units fastest). T: key tiles at or before the rows
+// (0 for a packed sample shorter than this tile).
+struct DqItem {
+    int i, bh, h, g, T;
+    SeqSpan sp;
+};
+
+__device__ __forceinline__ DqItem dq_item(int w, int BH, int n_qt, int H, int G,
+                                          const SeqRows &sr) {
+    DqItem it;
+    it.i = n_qt - 1 - w / BH;
+    it.bh = w - (w / BH) * BH;
+    const int unit = it.bh / H;
+    it.h = it.bh - unit * H;
+    it.g = it.h / (H / G);
+    it.sp = seq_span(sr, unit);
+    it.T = it.i * kTile < it.sp.len ? it.i + 1 : 0;
+    return it;
+}
+
 // Element e of 32 bf16 packed two per word (the lower index in the low half).
 __device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[16], int e) {
     const uint32_t v = w[e >> 1];
@@ -241,7 +276,8 @@ template <int D>
 __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int lane,
                                             uint32_t tacc, const uint8_t *sX,
                                             const uint8_t *cs_row, bool row_ok,
-                                            EpiScratch &escr, bf16 *dst_row, float *part) {
+                                            EpiScratch &escr, bf16 *dst_row, float *part,
+                                            uint8_t *stage) {
     using A = Atoms<D>;
     constexpr int kHalf = D / 2, kEpiWGs = D / 32;
     const bool in_epi = wg < kEpiWGs;
@@ -314,7 +350,18 @@ __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int la
             ow[e / 2] = pack_bf16x2(ol[0], ol[1]);
             ow[8 + e / 2] = pack_bf16x2(oh[0], oh[1]);
         }
-        if (row_ok) {
+        if (stage != nullptr) {
+            // in place of the x chunks this thread read (the caller stores the tile by TMA)
+#pragma unroll
+            for (int part8 = 0; part8 < 4; ++part8) {
+                const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
+                const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                                r * A::kRowBytes + (col % A::kCols) * 2);
+                *reinterpret_cast<uint4 *>(stage + swizzled<A::kRowBytes>(off)) =
+                    make_uint4(ow[4 * part8], ow[4 * part8 + 1], ow[4 * part8 + 2], ow[4 * part8 + 3]);
+            }
+            fence_proxy_async_smem();
+        } else if (row_ok) {
             uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
             dst[i0 / 8] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
             dst[i0 / 8 + 1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
@@ -346,8 +393,9 @@ template <int D>
 __device__ __noinline__ void finish_rows_call(bool ok, int wg, int quarter, int lane,
                                               uint32_t tacc, const uint8_t *sX,
                                               const uint8_t *cs_row, bool row_ok,
-                                              EpiScratch &escr, bf16 *dst_row, float *part) {
-    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part);
+                                              EpiScratch &escr, bf16 *dst_row, float *part,
+                                              uint8_t *stage) {
+    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part, stage);
 }
 
 // The dK/dV kernel's accumulator stores (a separate function, so that its
@@ -409,7 +457,7 @@ __device__ __noinline__ void finish_rows_dk(bool ok, int wg, int quarter, int la
                                             uint32_t tacc, const uint8_t *sX,
                                             const uint8_t *cs_row, bool row_ok,
                                             EpiScratch &escr, bf16 *dst_row, float *part) {
-    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part);
+    finish_rows<D>(ok, wg, quarter, lane, tacc, sX, cs_row, row_ok, escr, dst_row, part, nullptr);
 }
 
 // kSplit: the chunked work split is on (a separate instantiation keeps the
@@ -819,11 +867,12 @@ template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
             const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
-            const __grid_constant__ CUtensorMap map_do, const bf16 *__restrict__ qhat,
+            const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_o,
+            const __grid_constant__ CUtensorMap map_dq, const bf16 *__restrict__ qhat,
             const bf16 *__restrict__ out, const float *__restrict__ lse, float *__restrict__ dlt,
             const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
             bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
-            int n_qt, unsigned int *err, int stall) {
+            int BH, int n_qt, int n_items, unsigned int *err, int stall) {
     using C = BwdCfg<D>;
     constexpr int KS = C::kKStages, VS = C::kVStages;
     // TMEM: S [0,128), dP [128,256), dQhat accumulator [256, 256+D), the resident
@@ -840,24 +889,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     uint8_t *sDO = sV + VS * C::kTileBytes;            // owned rows of dO (the dP MMA's A)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int BH = gridDim.x / n_qt;
-    const int i = n_qt - 1 - (int)(blockIdx.x / BH);   // query tile, longest first
-    const int bh = blockIdx.x % BH;
-    const int unit = bh / H, h = bh - unit * H, g = h / (H / G);
-    const SeqSpan sp = seq_span(sr, unit);
-    const int S = sp.len;                              // rows of this unit
-    float *part = part_q + ((size_t)bh * n_qt + i) * D;   // this CTA's dgamma_q partial
-    if (i * kTile >= S) {                              // a packed sample shorter than this tile
-        for (int d = threadIdx.x; d < D; d += blockDim.x) part[d] = 0.f;
-        return;
-    }
-    const size_t qrow0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;   // [.., H, S, ..] rows
-    const int T = i + 1;                               // key tiles at or before the rows
     volatile int *abort_flag = &bars.abort_flag;
-    // s_full[0] / dp_full: S(t) / dP(t) are in TMEM; p_full[1] / dp_taken: every
-    // softmax thread holds S(t) / dP(t) in registers (the columns may be
-    // overwritten); p_full[0]: packed dS(t) is in TMEM; s_full[1]: dQ(t) has read
-    // dS(t) (its columns may be overwritten)
+    // s_full[0] / dp_full: S / dP of a key tile are in TMEM; p_full[1] / dp_taken:
+    // every softmax thread holds them in registers (the columns may be
+    // overwritten); p_full[0]: packed dS is in TMEM; s_full[1]: dQ has read dS
+    // (its columns may be overwritten). Their phases count key tiles across items.
     uint64_t *ds_ready = &bars.p_full[0];
     uint64_t *s_taken = &bars.p_full[1];
     uint64_t *ds_free = &bars.s_full[1];
@@ -871,6 +907,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
+    // Every role walks the same items (w = blockIdx.x, + gridDim.x, ...) and skips
+    // the same empty ones. Ring uses per item: K ring, its T key tiles and then
+    // the two (cos, sin) halves of its rows; V ring, its T value tiles and then its
+    // q rows (the epilogue's inputs, released by the softmax threads after it).
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -879,59 +919,78 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_x);
             tma_prefetch_desc(&map_cs);
             tma_prefetch_desc(&map_do);
-            const int row0 = sp.start + i * kTile;
-            // the owned rows of dO (the first dP needs them)
-            mbar_expect_tx(&bars.x_full, C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_4d(sDO + c * C::kBox, &map_do, &bars.x_full, c * C::A::kCols, h, row0,
-                            sp.plane);
-            // K ring uses: K tiles 0..T-1, then the two (cos, sin) halves; V ring uses:
-            // V tiles 0..T-1, then the owned q rows
-            int k_issued = 0, v_issued = 0;
+            tma_prefetch_desc(&map_o);
+            tma_prefetch_desc(&map_dq);
+            int items = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
-            for (int u = 0; ok && u < T + 2; ++u) {
-                const int ks = u % KS;
-                if (u >= KS &&
-                    !(ok = mbar_wait(&bars.st_empty[ks], ((u / KS) - 1) & 1, abort_flag)))
-                    break;
-                uint8_t *kb = sK + ks * C::kTileBytes;
-                if (u < T) {
-                    mbar_expect_tx(&bars.st_full[ks], C::kTileBytes);
+            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+                const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
+                if (it.T == 0) continue;
+                const int T = it.T, row0 = it.sp.start + it.i * kTile;
+                {
+                    // L2 prefetch of the rows the softmax threads read with plain loads when
+                    // the item starts (after the previous item's epilogue): Qhat and O
+                    const int rows = min(kTile, it.sp.len - it.i * kTile);
+                    l2_prefetch_bulk(qhat + (((size_t)it.sp.plane * H + it.h) * sr.S + row0) * D,
+                                     (uint32_t)(rows * D * 2));
                     for (int c = 0; c < C::kChunks; ++c)
-                        tma_load_3d(kb + c * C::kBox, &map_k, &bars.st_full[ks], c * C::A::kCols,
-                                    sp.start + u * kTile, sp.plane * G + g);
-                } else {
-                    // (cos, sin) rows [64 e, 64 e + 64) of the owned rows: D/32 pieces
-                    mbar_expect_tx(&bars.st_full[ks], (D / 32) * kCsPieceBytes);
-                    for (int c = 0; c < D / 32; ++c)
-                        tma_load_2d(kb + c * kCsPieceBytes, &map_cs, &bars.st_full[ks], 32 * c,
-                                    row0 + 64 * (u - T));
+                        l2_prefetch_4d(&map_o, c * C::A::kCols, it.h, row0, it.sp.plane);
                 }
-                ++k_issued;
-                if (u > T) continue;
-                const int vs = u % VS;
-                if (u >= VS &&
-                    !(ok = mbar_wait(&bars.v_empty[vs], ((u / VS) - 1) & 1, abort_flag)))
+                // the item's dO rows, once the previous item's dP MMAs and Dlt have read sDO
+                if (items > 0 && !(ok = mbar_wait(&bars.do_free, (items - 1) & 1, abort_flag)))
                     break;
-                uint8_t *vb = sV + vs * C::kTileBytes;
-                mbar_expect_tx(&bars.v_full[vs], C::kTileBytes);
-                for (int c = 0; c < C::kChunks; ++c) {
-                    if (u < T)
-                        tma_load_4d(vb + c * C::kBox, &map_v, &bars.v_full[vs], c * C::A::kCols,
-                                    g, sp.start + u * kTile, sp.plane);
-                    else
-                        tma_load_4d(vb + c * C::kBox, &map_x, &bars.v_full[vs], c * C::A::kCols,
-                                    h, row0, sp.plane);
+                mbar_expect_tx(&bars.x_full, C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_load_4d(sDO + c * C::kBox, &map_do, &bars.x_full, c * C::A::kCols, it.h,
+                                row0, it.sp.plane);
+                ++items;
+                for (int u = 0; ok && u < T + 2; ++u) {
+                    const int ks = k_issued % KS;
+                    if (k_issued >= KS &&
+                        !(ok = mbar_wait(&bars.st_empty[ks], ((k_issued / KS) - 1) & 1, abort_flag)))
+                        break;
+                    uint8_t *kb = sK + ks * C::kTileBytes;
+                    if (u < T) {
+                        mbar_expect_tx(&bars.st_full[ks], C::kTileBytes);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_3d(kb + c * C::kBox, &map_k, &bars.st_full[ks],
+                                        c * C::A::kCols, it.sp.start + u * kTile,
+                                        it.sp.plane * G + it.g);
+                    } else {
+                        // (cos, sin) rows [64 e, 64 e + 64) of the owned rows: D/32 pieces
+                        mbar_expect_tx(&bars.st_full[ks], (D / 32) * kCsPieceBytes);
+                        for (int c = 0; c < D / 32; ++c)
+                            tma_load_2d(kb + c * kCsPieceBytes, &map_cs, &bars.st_full[ks],
+                                        32 * c, row0 + 64 * (u - T));
+                    }
+                    ++k_issued;
+                    if (u > T) continue;
+                    const int vs = v_issued % VS;
+                    if (v_issued >= VS &&
+                        !(ok = mbar_wait(&bars.v_empty[vs], ((v_issued / VS) - 1) & 1, abort_flag)))
+                        break;
+                    uint8_t *vb = sV + vs * C::kTileBytes;
+                    mbar_expect_tx(&bars.v_full[vs], C::kTileBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        if (u < T)
+                            tma_load_4d(vb + c * C::kBox, &map_v, &bars.v_full[vs],
+                                        c * C::A::kCols, it.g, it.sp.start + u * kTile,
+                                        it.sp.plane);
+                        else
+                            tma_load_4d(vb + c * C::kBox, &map_x, &bars.v_full[vs],
+                                        c * C::A::kCols, it.h, row0, it.sp.plane);
+                    }
+                    ++v_issued;
                 }
-                ++v_issued;
             }
             if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
-            // drain: every copy issued by this CTA lands before it exits
+            // drain: every copy issued by this CTA lands before it exits (at most the
+            // last dO load, the last KS K-ring and the last VS V-ring loads in flight)
+            if (items > 0) mbar_wait(&bars.x_full, (items - 1) & 1, nullptr);
             for (int x = max(0, k_issued - KS); x < k_issued; ++x)
                 mbar_wait(&bars.st_full[x % KS], (x / KS) & 1, nullptr);
             for (int x = max(0, v_issued - VS); x < v_issued; ++x)
                 mbar_wait(&bars.v_full[x % VS], (x / VS) & 1, nullptr);
-            mbar_wait(&bars.x_full, 0, nullptr);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issuer
@@ -946,67 +1005,83 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const uint64_t dDO = smem_desc(smem_u32(sDO), 16, A::kSBO, A::kMode);
             constexpr uint64_t kStep = (uint64_t)C::kTileBytes >> 4;
             // S = Qhat Khat^T (A in TMEM) and dP = dO V^T (both operands in shared
-            // memory), full 128-key tiles (N = 128 runs at the full MMA rate)
-            auto issue_s = [&](int t) {
-                const uint64_t ko = (uint64_t)(t % KS) * kStep;
+            // memory), full 128-key tiles (N = 128 runs at the full MMA rate); kx / vx
+            // are the tiles' K-ring / V-ring use indices
+            auto issue_s = [&](int kx) {
+                const uint64_t ko = (uint64_t)(kx % KS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ts_w(tmem, tmem + kTQ + kk * 8, dKk0 + ko + kmajor_off<D>(kk), idesc_s, kk > 0);
-                mma_commit_w(&bars.s_full[0]);         // S of tile t is in TMEM
+                mma_commit_w(&bars.s_full[0]);         // S of the tile is in TMEM
             };
-            auto issue_dp = [&](int t) {
-                const uint64_t vo = (uint64_t)(t % VS) * kStep;
+            auto issue_dp = [&](int vx) {
+                const uint64_t vo = (uint64_t)(vx % VS) * kStep;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     mma_ss_w(tmem + 128, dDO + kmajor_off<D>(kk), dVk0 + vo + kmajor_off<D>(kk),
                              idesc_s, kk > 0);
-                mma_commit_w(&bars.dp_full);           // dP of tile t is in TMEM
-                mma_commit_w(&bars.v_empty[t % VS]);   // V tile t is read
+                mma_commit_w(&bars.dp_full);           // dP of the tile is in TMEM
+                mma_commit_w(&bars.v_empty[vx % VS]);  // its V tile is read
             };
             bool ok = !stall ||
                       __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
-            ok = ok && mbar_wait_w(&bars.own_full, 0, abort_flag) &&
-                 mbar_wait_w(&bars.x_full, 0, abort_flag) &&
-                 mbar_wait_w(&bars.st_full[0], 0, abort_flag) &&
-                 mbar_wait_w(&bars.v_full[0], 0, abort_flag);
-            if (ok) {
+            int items = 0, kt = 0, vt = 0, tg = 0;   // ring uses and key tiles before this item
+            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+                const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
+                if (it.T == 0) continue;
+                const int T = it.T;
+                // the item's Qhat rows in TMEM and dO rows in shared memory (the softmax
+                // threads store Qhat only after the previous item's epilogue, when every
+                // MMA of that item has completed), and its first K and V tiles
+                ok = mbar_wait_w(&bars.own_full, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.x_full, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.st_full[kt % KS], (kt / KS) & 1, abort_flag) &&
+                     mbar_wait_w(&bars.v_full[vt % VS], (vt / VS) & 1, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
-                issue_s(0);
-                issue_dp(0);
-            }
-            // Per tile t: once every softmax thread holds S(t) in registers, S(t+1) is
-            // issued, and once they hold dP(t), dP(t+1) (both run during the softmax of
-            // t, and the dP loads overlap S(t+1)); once dS(t) is packed in its own
-            // columns, dQ(t). The softmax of t+1 writes dS(t+1) only after dQ(t) has
-            // read dS(t) (ds_free).
-            for (int t = 0; ok && t < T; ++t) {
-                const int ks = t % KS;
-                const uint64_t ko = (uint64_t)ks * kStep;
-                if (t + 1 < T) {
-                    if (!(ok = mbar_wait_w(s_taken, t & 1, abort_flag) &&
-                               mbar_wait_w(&bars.st_full[(t + 1) % KS], ((t + 1) / KS) & 1,
-                                           abort_flag)))
-                        break;
+                issue_s(kt);
+                issue_dp(vt);
+                if (T == 1) mma_commit_w(&bars.do_free);
+                // Per tile t: once every softmax thread holds S(t) in registers, S(t+1)
+                // is issued, and once they hold dP(t), dP(t+1) (both run during the
+                // softmax of t, and the dP loads overlap S(t+1)); once dS(t) is packed
+                // in its own columns, dQ(t). The softmax of t+1 writes dS(t+1) only
+                // after dQ(t) has read dS(t) (ds_free).
+                for (int t = 0; ok && t < T; ++t) {
+                    const int x = tg + t;
+                    if (t + 1 < T) {
+                        if (!(ok = mbar_wait_w(s_taken, x & 1, abort_flag) &&
+                                   mbar_wait_w(&bars.st_full[(kt + t + 1) % KS],
+                                               ((kt + t + 1) / KS) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_s(kt + t + 1);
+                        if (!(ok = mbar_wait_w(&bars.dp_taken, x & 1, abort_flag) &&
+                                   mbar_wait_w(&bars.v_full[(vt + t + 1) % VS],
+                                               ((vt + t + 1) / VS) & 1, abort_flag)))
+                            break;
+                        tc_fence_after();
+                        issue_dp(vt + t + 1);
+                        if (t + 2 == T) mma_commit_w(&bars.do_free);   // the item's last dP
+                    }
+                    if (!(ok = mbar_wait_w(ds_ready, x & 1, abort_flag))) break;
                     tc_fence_after();
-                    issue_s(t + 1);
-                    if (!(ok = mbar_wait_w(&bars.dp_taken, t & 1, abort_flag) &&
-                               mbar_wait_w(&bars.v_full[(t + 1) % VS], ((t + 1) / VS) & 1,
-                                           abort_flag)))
-                        break;
-                    tc_fence_after();
-                    issue_dp(t + 1);
-                }
-                if (!(ok = mbar_wait_w(ds_ready, t & 1, abort_flag))) break;
-                tc_fence_after();
+                    const uint64_t ko = (uint64_t)((kt + t) % KS) * kStep;
 #pragma unroll
-                for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
-                    mma_ts_w(tmem + 256, tmem + kTDS + kk * 8, dKm0 + ko + mnmajor_off<D>(kk),
-                             idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_w(&bars.st_empty[ks]);      // K tile t is read
-                mma_commit_w(ds_free);
+                    for (int kk = 0; kk < kTile / 16; ++kk)   // dQhat += dS Khat
+                        mma_ts_w(tmem + 256, tmem + kTDS + kk * 8, dKm0 + ko + mnmajor_off<D>(kk),
+                                 idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_w(&bars.st_empty[(kt + t) % KS]);   // K tile t is read
+                    mma_commit_w(ds_free);
+                }
+                if (!ok) break;
+                mma_commit_w(&bars.acc_done);
+                kt += T + 2;
+                vt += T + 1;
+                tg += T;
+                ++items;
             }
-            if (ok) mma_commit_w(&bars.acc_done);
-            else if (lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+            if (!ok && lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
             mma_commit_w(&bars.drain);
             mbar_wait_w(&bars.drain, 0, nullptr);
         }
@@ -1014,137 +1089,183 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         // ------------------------------------------------------------ softmax + epilogue
         const int wg = warp >> 2, quarter = warp & 3;
         const int r = quarter * 32 + lane;             // owned query row = TMEM lane
-        const int tq = i * kTile + r;                  // query position
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
-        const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
-        if (wg == 0) {
-            // the owned Qhat rows become the TMEM-resident A operand of S (lane = row;
-            // a 32-bit column holds two consecutive bf16, the lower index in the low half)
-            uint32_t xa[D / 2];
-            const uint4 *src = reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
-                xa[4 * c] = z.x; xa[4 * c + 1] = z.y; xa[4 * c + 2] = z.z; xa[4 * c + 3] = z.w;
+        int items = 0, kt = 0, vt = 0, tg = 0;
+        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+            const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
+            float *part = part_q + ((size_t)it.bh * n_qt + it.i) * D;   // the item's dgamma_q partial
+            if (it.T == 0) {                       // a packed sample shorter than this tile
+                if (threadIdx.x < D) part[threadIdx.x] = 0.f;
+                continue;
             }
-            const uint32_t dst = tmem + kTQ + lane_off;
-            if constexpr (D == 128) tmem_st64_sync(dst, xa);
-            else if constexpr (D == 64) tmem_st32_sync(dst, xa);
-            else tmem_st16_sync(dst, xa);
-            tc_fence_before();
-            mbar_arrive(&bars.own_full);
-        } else if (wg == kSoftmaxWGs - 1) {
-            // for the dq epilogue (read after its first named barrier; the writes
-            // and reads are ordered by that barrier)
-            escr.rstd[r] = tq < S ? rstd_q[((size_t)sp.plane * sr.S + sp.start + tq) * H + h] : 0.f;
-            if (r < D) escr.gamma[r] = gamma_q[r];
-        }
-        // Dlt = rowsum(dO o O) of the owned rows (the softmax backward's row term;
-        // the dK/dV kernel, launched after this one, reads it): warpgroup wg sums the
-        // columns [wg D/4, (wg + 1) D/4) of its thread's row, dO from the TMA'd tile,
-        // O from global memory; the four parts are added in warpgroup order. It
-        // overlaps the first S and dP MMAs.
-        bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.x_full, 0, abort_flag));
-        {
-            using A = Atoms<D>;
-            float part0 = 0.f, part1 = 0.f;
-            if (ok && tq < S) {
-                const uint4 *orow = reinterpret_cast<const uint4 *>(
-                    out + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D + wg * (D / 4));
+            const int T = it.T, S = it.sp.len, h = it.h;
+            const int tq = it.i * kTile + r;           // query position
+            const size_t qrow0 = ((size_t)it.sp.plane * H + h) * sr.S + it.sp.start;
+            const size_t xrow = ((size_t)it.sp.plane * sr.S + it.sp.start + tq) * H + h;   // [.., S, H, ..]
+            const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
+            if (wg == 0) {
+                // the owned Qhat rows become the TMEM-resident A operand of S (lane = row;
+                // a 32-bit column holds two consecutive bf16, the lower index in the low
+                // half); the previous item's MMAs have all completed (its epilogue waited)
+                uint32_t xa[D / 2];
+                const uint4 *src = reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D);
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    const int col = wg * (D / 4) + 8 * c;
-                    const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
-                                                    r * A::kRowBytes + (col % A::kCols) * 2);
-                    const uint4 g = *reinterpret_cast<const uint4 *>(sDO + swizzled<A::kRowBytes>(off));
-                    const uint4 o = orow[c];
-                    const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, ow[4] = {o.x, o.y, o.z, o.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        part0 = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), part0);
-                        part1 = fmaf(__uint_as_float(gw[e] & 0xffff0000u),
-                                     __uint_as_float(ow[e] & 0xffff0000u), part1);
-                    }
+                for (int c = 0; c < D / 8; ++c) {
+                    const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
+                    xa[4 * c] = z.x; xa[4 * c + 1] = z.y; xa[4 * c + 2] = z.z; xa[4 * c + 3] = z.w;
                 }
+                const uint32_t dst = tmem + kTQ + lane_off;
+                if constexpr (D == 128) tmem_st64_sync(dst, xa);
+                else if constexpr (D == 64) tmem_st32_sync(dst, xa);
+                else tmem_st16_sync(dst, xa);
+                tc_fence_before();
+                mbar_arrive(&bars.own_full);
+            } else if (wg == kSoftmaxWGs - 1) {
+                // for the dq epilogue (read after its first named barrier; the previous
+                // item's epilogue finished reading these before the stop barrier below)
+                escr.rstd[r] = tq < S ? rstd_q[xrow] : 0.f;
+                if (r < D) escr.gamma[r] = gamma_q[r];
             }
-            escr.dot[wg][r] = part0 + part1;
-        }
-        softmax_bar_sync();   // every softmax thread reaches this (no wait above is unbounded)
-        const float dl = ((escr.dot[0][r] + escr.dot[1][r]) + escr.dot[2][r]) + escr.dot[3][r];
-        if (ok && wg == 0 && tq < S) dlt[qrow0 + tq] = dl;
-        for (int t = 0; ok && t < T; ++t) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], t & 1, abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            const int c0 = wg * kWgCols;
-            const int k0 = t * kTile + c0;
-            const uint32_t tS = tmem + lane_off + c0;
-            const uint32_t tP = tmem + lane_off + 128 + c0;
-            // no masking when every key of these columns is at/before every owned query
-            const bool interior = (k0 + kWgCols - 1 <= i * kTile);
-            uint32_t dd[kWgCols / 2];
+            // Dlt = rowsum(dO o O) of the owned rows (the softmax backward's row term;
+            // the dK/dV kernel, launched after this one, reads it): warpgroup wg sums the
+            // columns [wg D/4, (wg + 1) D/4) of its thread's row, O from global memory
+            // (loaded before the wait for the dO tile, so the two latencies overlap), dO
+            // from the TMA'd tile; the four parts are added in warpgroup order.
+            uint4 orow[D / 32];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c)
+                orow[c] = tq < S ? reinterpret_cast<const uint4 *>(out + xrow * D + wg * (D / 4))[c]
+                                 : make_uint4(0, 0, 0, 0);
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.x_full, items & 1, abort_flag));
             {
-                uint32_t sv[32], dpv[32];
-                tmem_ld32_sync(tS, sv);
-                tc_fence_before();
-                mbar_arrive(s_taken);                   // S(t+1) may now be issued
-                if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, t & 1, abort_flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                tmem_ld32_sync(tP, dpv);
-                tc_fence_before();
-                mbar_arrive(&bars.dp_taken);            // dP(t+1) may now be issued
-                // only tiles that reach past the owned rows' diagonal take the select
-                // element pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
-                auto body = [&](auto masked) {
-                    const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2);
-                    const float2 ndl = make_float2(-dl, -dl);
+                using A = Atoms<D>;
+                float part0 = 0.f, part1 = 0.f;
+                if (ok && tq < S) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const float2 a = ffma2(make_float2(__uint_as_float(sv[e]),
-                                                           __uint_as_float(sv[e + 1])), sl2v, nl);
-                        float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
-                        if constexpr (decltype(masked)::value) {
-                            if (k0 + e > tq) p.x = 0.f;
-                            if (k0 + e + 1 > tq) p.y = 0.f;
+                    for (int c = 0; c < D / 32; ++c) {
+                        const int col = wg * (D / 4) + 8 * c;
+                        const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                                        r * A::kRowBytes + (col % A::kCols) * 2);
+                        const uint4 gv = *reinterpret_cast<const uint4 *>(sDO + swizzled<A::kRowBytes>(off));
+                        const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                        const uint32_t ow[4] = {orow[c].x, orow[c].y, orow[c].z, orow[c].w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            part0 = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), part0);
+                            part1 = fmaf(__uint_as_float(gw[e] & 0xffff0000u),
+                                         __uint_as_float(ow[e] & 0xffff0000u), part1);
                         }
-                        const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e]),
-                                                                     __uint_as_float(dpv[e + 1])),
-                                                         ndl));
-                        dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
                     }
-                };
-                if (interior) body(std::false_type{});
-                else body(std::true_type{});
+                }
+                escr.dot[wg][r] = part0 + part1;
             }
-            if (t > 0) {   // dQ(t-1) has read the dS columns
-                ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (t - 1) & 1, abort_flag));
+            softmax_bar_sync();   // every softmax thread reaches this (no wait above is unbounded)
+            if (threadIdx.x == 0) mbar_arrive(&bars.do_free);   // no softmax thread reads sDO any more
+            const float dl = ((escr.dot[0][r] + escr.dot[1][r]) + escr.dot[2][r]) + escr.dot[3][r];
+            if (ok && wg == 0 && tq < S) dlt[qrow0 + tq] = dl;
+            for (int t = 0; ok && t < T; ++t) {
+                const int x = tg + t;                   // key tiles before this one
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[0], x & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
+                const int c0 = wg * kWgCols;
+                const int k0 = t * kTile + c0;
+                const uint32_t tS = tmem + lane_off + c0;
+                const uint32_t tP = tmem + lane_off + 128 + c0;
+                // no masking when every key of these columns is at/before every owned query
+                const bool interior = (k0 + kWgCols - 1 <= it.i * kTile);
+                uint32_t dd[kWgCols / 2];
+                {
+                    uint32_t sv[32], dpv[32];
+                    tmem_ld32_sync(tS, sv);
+                    tc_fence_before();
+                    mbar_arrive(s_taken);                   // S of the next tile may be issued
+                    if (!__all_sync(0xffffffffu, mbar_wait(&bars.dp_full, x & 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    tmem_ld32_sync(tP, dpv);
+                    tc_fence_before();
+                    mbar_arrive(&bars.dp_taken);            // dP of the next tile may be issued
+                    // only tiles that reach past the owned rows' diagonal take the select
+                    // element pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
+                    auto body = [&](auto masked) {
+                        const float2 sl2v = make_float2(sl2, sl2), nl = make_float2(-lse2, -lse2);
+                        const float2 ndl = make_float2(-dl, -dl);
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 a = ffma2(make_float2(__uint_as_float(sv[e]),
+                                                               __uint_as_float(sv[e + 1])), sl2v, nl);
+                            float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                            if constexpr (decltype(masked)::value) {
+                                if (k0 + e > tq) p.x = 0.f;
+                                if (k0 + e + 1 > tq) p.y = 0.f;
+                            }
+                            const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e]),
+                                                                         __uint_as_float(dpv[e + 1])),
+                                                             ndl));
+                            dd[e >> 1] = pack_bf16x2(ds.x, ds.y);
+                        }
+                    };
+                    if (interior) body(std::false_type{});
+                    else body(std::true_type{});
+                }
+                if (x > 0) {   // the previous dQ MMA has read the dS columns
+                    ok = __all_sync(0xffffffffu, mbar_wait(ds_free, (x - 1) & 1, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                tmem_st16_sync(tmem + lane_off + kTDS + 16 * wg, dd);   // packed dS, k-steps 2 wg, 2 wg + 1
+                tc_fence_before();
+                mbar_arrive(ds_ready);
             }
-            tmem_st16_sync(tmem + lane_off + kTDS + 16 * wg, dd);   // packed dS, k-steps 2 wg, 2 wg + 1
-            tc_fence_before();
-            mbar_arrive(ds_ready);
+            // ---- epilogue: dq and the item's dgamma_q partial from dQhat in TMEM; the
+            // producer loaded the q rows into the V slot after the item's last V tile
+            // and their (cos, sin) rows into the two K slots after its last K tile (row
+            // half r/64; piece wg = pairs [16 wg, 16 wg + 16))
+            const int xq = vt + T, xc = kt + T;         // their ring use indices
+            if (ok) ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&bars.acc_done, items & 1, abort_flag) &&
+                                    mbar_wait(&bars.v_full[xq % VS], (xq / VS) & 1, abort_flag) &&
+                                    mbar_wait(&bars.st_full[xc % KS], (xc / KS) & 1, abort_flag) &&
+                                    mbar_wait(&bars.st_full[(xc + 1) % KS], ((xc + 1) / KS) & 1,
+                                              abort_flag));
+            if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+            const uint8_t *sX = sV + (xq % VS) * C::kTileBytes;
+            const uint8_t *cs_row = sK + ((xc + (r >> 6)) % KS) * C::kTileBytes + wg * kCsPieceBytes +
+                                    (r & 63) * 128;
+            // dq rows: written over the q rows in shared memory and stored by one TMA
+            // store, unless the tile reaches past a packed sample (its last rows would
+            // land on the next sample's; those tiles store row by row)
+            const bool tma_out = sr.cu == nullptr || it.i * kTile + kTile <= S;
+            finish_rows_call<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
+                                dq + xrow * D, part,
+                                tma_out ? const_cast<uint8_t *>(sX) : nullptr);
+            // every softmax thread is done with the item (finish_rows ends on a named
+            // barrier): its epilogue inputs' ring slots may be refilled (the staged dq
+            // tile once the TMA store has read it)
+            if (threadIdx.x == 0) {
+                if (tma_out && ok) {
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_store_4d(&map_dq, sX + c * C::kBox, c * C::A::kCols, h,
+                                     it.sp.start + it.i * kTile, it.sp.plane);
+                    bulk_commit();
+                    bulk_wait_read0();
+                }
+                mbar_arrive(&bars.v_empty[xq % VS]);
+                mbar_arrive(&bars.st_empty[xc % KS]);
+                mbar_arrive(&bars.st_empty[(xc + 1) % KS]);
+            }
+            // stop together: a failed wait here, or one raised by another warp
+            if (softmax_bar_any(!ok || *abort_flag)) break;
+            kt += T + 2;
+            vt += T + 1;
+            tg += T;
+            ++items;
         }
-        // ---- epilogue: dq and the CTA's dgamma_q partial from dQhat in TMEM; the
-        // producer loaded the q rows into the V slot after the last V tile and
-        // their (cos, sin) rows into the two K slots after the last K tile (row
-        // half r/64; piece wg = pairs [16 wg, 16 wg + 16))
-        if (ok) ok = __all_sync(0xffffffffu,
-                                mbar_wait(&bars.acc_done, 0, abort_flag) &&
-                                mbar_wait(&bars.v_full[T % VS], (T / VS) & 1, abort_flag) &&
-                                mbar_wait(&bars.st_full[T % KS], (T / KS) & 1, abort_flag) &&
-                                mbar_wait(&bars.st_full[(T + 1) % KS], ((T + 1) / KS) & 1,
-                                          abort_flag));
-        const uint8_t *sX = sV + (T % VS) * C::kTileBytes;
-        const uint8_t *cs_row = sK + ((T + (r >> 6)) % KS) * C::kTileBytes + wg * kCsPieceBytes +
-                                (r & 63) * 128;
-        finish_rows_call<D>(ok, wg, quarter, lane, tmem + 256 + lane_off, sX, cs_row, tq < S, escr,
-                            dq + (((size_t)sp.plane * sr.S + sp.start + tq) * H + h) * D, part);
-        if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+        if (threadIdx.x == 0) bulk_wait0();   // the dq stores have completed
     }
     tc_fence_before();
     __syncthreads();
@@ -1297,7 +1418,11 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
                         unsigned int *err, cudaStream_t st) {
     using C = BwdCfg<D>;
     const int n_qt = (p.max_len + kTile - 1) / kTile;
-    const long blocks = (long)p.units * p.H * n_qt;
+    const long BH = (long)p.units * p.H;
+    const long n_items = BH * n_qt;
+    if (n_items >= (1L << 31)) return cudaErrorInvalidValue;
+    // persistent grid: one CTA per SM walks the items (one CTA fits an SM: 512 TMEM columns)
+    const long blocks = std::min<long>(n_items, sm_count());
     CUtensorMap mx, mcs, mdo;
     cudaError_t e = make_epi_maps<D>(p, ep, p.H, 64, mx, mcs);
     if (e != cudaSuccess) return e;
@@ -1307,13 +1432,20 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     CUtensorMap unused;
     e = make_epi_maps<D>(p, eo, p.H, kTile, mdo, unused);
     if (e != cudaSuccess) return e;
+    // the forward output O (L2 prefetch of the rows Dlt reads) and dq (TMA store of the rows)
+    CUtensorMap mo, mdq;
+    eo.x = out;
+    if ((e = make_epi_maps<D>(p, eo, p.H, kTile, mo, unused)) != cudaSuccess) return e;
+    eo.x = ep.out;
+    if ((e = make_epi_maps<D>(p, eo, p.H, kTile, mdq, unused)) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, mdo, (const bf16 *)qhat, (const bf16 *)out, lse, dlt, ep.gamma, ep.rstd,
-        (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, n_qt, err,
-        (test_stall_mask() & STALL_DQ_TC) != 0);
+        m.k, m.v, mx, mcs, mdo, mo, mdq, (const bf16 *)qhat, (const bf16 *)out, lse, dlt, ep.gamma,
+        ep.rstd,
+        (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_qt,
+        (int)n_items, err, (test_stall_mask() & STALL_DQ_TC) != 0);
     return cudaGetLastError();
 }
 

@@ -154,6 +154,51 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         : "memory");
 }
 
+// L2 prefetch hints (no shared memory, no completion): `bytes` (a multiple of
+// 16) from a 16-byte aligned global address, or one box of a tensor map.
+__device__ __forceinline__ void l2_prefetch_bulk(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void l2_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2,
+                                               int c3) {
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+                 : "memory");
+}
+
+// TMA store of one box from shared memory (bulk-group completion): the writing
+// threads make their shared-memory stores visible to the async proxy first
+// (fence_proxy_async_smem, then a barrier); bulk_wait_read0 waits until every
+// committed store has finished reading shared memory.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int c0,
+                                             int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_read0() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until every committed bulk store of this thread has completed (its
+// writes are performed).
+__device__ __forceinline__ void bulk_wait0() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Non-tensor bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global to shared memory, completion counted on `bar`.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,
