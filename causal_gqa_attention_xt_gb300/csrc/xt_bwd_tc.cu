@@ -907,7 +907,8 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    // Every role walks the same items (w = blockIdx.x, + gridDim.x, ...) and skips
+    // Every role walks the same items (snake_item: rounds of gridDim.x items,
+    // walked forwards and backwards in turn) and skips
     // the same empty ones. Ring uses per item: K ring, its T key tiles and then
     // the two (cos, sin) halves of its rows; V ring, its T value tiles and then its
     // q rows (the epilogue's inputs, released by the softmax threads after it).
@@ -923,7 +924,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_dq);
             int items = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
-            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
                 if (it.T == 0) continue;
                 const int T = it.T, row0 = it.sp.start + it.i * kTile;
@@ -1026,7 +1027,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             bool ok = !stall ||
                       __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
             int items = 0, kt = 0, vt = 0, tg = 0;   // ring uses and key tiles before this item
-            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
                 if (it.T == 0) continue;
                 const int T = it.T;
@@ -1092,7 +1093,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const float sl2 = kLog2e * rsqrtf((float)D);
         int items = 0, kt = 0, vt = 0, tg = 0;
-        for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+        for (int rnd = 0, w = snake_item(0); w < n_items; w = snake_item(++rnd)) {
             const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
             float *part = part_q + ((size_t)it.bh * n_qt + it.i) * D;   // the item's dgamma_q partial
             if (it.T == 0) {                       // a packed sample shorter than this tile

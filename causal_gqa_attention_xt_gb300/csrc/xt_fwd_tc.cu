@@ -174,7 +174,8 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    // Every role walks the same items (w = blockIdx.x, + gridDim.x, ...) and
+    // Every role walks the same items (snake_item: rounds of gridDim.x items,
+    // walked forwards and backwards in turn) and
     // skips the same empty ones; barrier phases are counted across items.
     if (warp == 8) {
         // ------------------------------------------------------------ producer
@@ -184,7 +185,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             tma_prefetch_desc(&map_v);
             int q_issued = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
-            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
                 if (it.n_kv[0] == 0) continue;   // a packed sample shorter than this pair's rows
                 const int n_iter = max(it.n_kv[0], it.n_kv[1]);
@@ -265,7 +266,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
             bool ok = !stall ||
                       __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
             int items = 0, kv_used = 0, p_cnt[2] = {0, 0};
-            for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+            for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
                 if (it.n_kv[0] == 0) continue;
                 const int n_iter = max(it.n_kv[0], it.n_kv[1]);
@@ -330,7 +331,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
         const float sl2 = kLog2e * rsqrtf((float)D);
         bool ok = true;
         int s_cnt = 0;   // S_i tiles (and PV_i MMAs) of the previous items
-        for (int w = blockIdx.x; ok && w < n_items; w += gridDim.x) {
+        for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
             const FwdItem it = fwd_item(w, BH, n_pairs, H, G, sr);
             const int n = it.n_kv[i];
             if (n == 0) continue;                // no query tile i in this item
