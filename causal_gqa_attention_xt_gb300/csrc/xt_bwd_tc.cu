@@ -116,6 +116,7 @@ struct BwdBarriers {
     uint64_t x_full;                 // dQ kernel: the owned rows of dO are in shared memory
     uint64_t dp_full, dp_taken;      // dQ kernel: dP of a tile is in TMEM / in every softmax thread
     uint64_t do_free;                // dQ kernel: the item's dP MMAs and its Dlt have read the dO rows
+    uint64_t q_read;                 // dQ kernel: the Qhat rows are copied from the dO slot into TMEM
     uint64_t stall;                  // never arrived on (xt_test_inject_stall)
     uint32_t tmem_base;
     int abort_flag;
@@ -150,6 +151,7 @@ __device__ __forceinline__ void init_bwd_barriers(BwdBarriers &bars, uint32_t ow
     mbar_init(&bars.dp_full, 1);
     mbar_init(&bars.dp_taken, 32 * 4 * kSoftmaxWGs);
     mbar_init(&bars.do_free, 2);   // the last dP MMA's commit + the softmax threads after Dlt
+    mbar_init(&bars.q_read, 1);
     mbar_init(&bars.stall, 1);
     fence_barrier_init();
 }
@@ -868,7 +870,7 @@ __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
             const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
             const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_o,
-            const __grid_constant__ CUtensorMap map_dq, const bf16 *__restrict__ qhat,
+            const __grid_constant__ CUtensorMap map_dq, const __grid_constant__ CUtensorMap map_qh,
             const bf16 *__restrict__ out, const float *__restrict__ lse, float *__restrict__ dlt,
             const float *__restrict__ gamma_q, const float *__restrict__ rstd_q,
             bf16 *__restrict__ dq, float *__restrict__ part_q, const SeqRows sr, int H, int G,
@@ -886,7 +888,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t *sK = smem;                                // KS K tiles
     uint8_t *sV = sK + KS * C::kTileBytes;             // VS V tiles
-    uint8_t *sDO = sV + VS * C::kTileBytes;            // owned rows of dO (the dP MMA's A)
+    // the owned rows: first Qhat (copied into TMEM as the S MMA's A), then dO (the
+    // dP MMA's A, and Dlt's)
+    uint8_t *sDO = sV + VS * C::kTileBytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &bars.abort_flag;
@@ -898,7 +902,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     uint64_t *s_taken = &bars.p_full[1];
     uint64_t *ds_free = &bars.s_full[1];
 
-    if (threadIdx.x == 0) init_bwd_barriers(bars, 128, 1, KS > VS ? KS : VS, false);
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 1, KS > VS ? KS : VS, false);
     if (warp == kWarpMma) {
         tmem_alloc(&bars.tmem_base, 512);
         tmem_relinquish();
@@ -912,6 +916,11 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     // the same empty ones. Ring uses per item: K ring, its T key tiles and then
     // the two (cos, sin) halves of its rows; V ring, its T value tiles and then its
     // q rows (the epilogue's inputs, released by the softmax threads after it).
+    // The owned-row slot takes the item's Qhat rows (own_full), which the MMA warp
+    // copies into TMEM once the previous item's last S MMA has run (q_read), then
+    // its dO rows (x_full), held until its dP MMAs and Dlt are done (do_free): the
+    // next item's Qhat copy, first S and first dP run during the current item's
+    // epilogue.
     if (warp == kWarpTma) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
@@ -922,28 +931,24 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_do);
             tma_prefetch_desc(&map_o);
             tma_prefetch_desc(&map_dq);
-            int items = 0, k_issued = 0, v_issued = 0;
+            int items = 0, x_issued = 0, k_issued = 0, v_issued = 0;
             bool ok = true;
             for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
                 if (it.T == 0) continue;
                 const int T = it.T, row0 = it.sp.start + it.i * kTile;
-                {
-                    // L2 prefetch of the rows the softmax threads read with plain loads when
-                    // the item starts (after the previous item's epilogue): Qhat and O
-                    const int rows = min(kTile, it.sp.len - it.i * kTile);
-                    l2_prefetch_bulk(qhat + (((size_t)it.sp.plane * H + it.h) * sr.S + row0) * D,
-                                     (uint32_t)(rows * D * 2));
-                    for (int c = 0; c < C::kChunks; ++c)
-                        l2_prefetch_4d(&map_o, c * C::A::kCols, it.h, row0, it.sp.plane);
-                }
-                // the item's dO rows, once the previous item's dP MMAs and Dlt have read sDO
+                // L2 prefetch of the O rows the softmax threads read with plain loads when
+                // the item starts (after the previous item's epilogue)
+                for (int c = 0; c < C::kChunks; ++c)
+                    l2_prefetch_4d(&map_o, c * C::A::kCols, it.h, row0, it.sp.plane);
+                // the item's Qhat rows, once the previous item's dP MMAs and Dlt have read
+                // its dO rows
                 if (items > 0 && !(ok = mbar_wait(&bars.do_free, (items - 1) & 1, abort_flag)))
                     break;
-                mbar_expect_tx(&bars.x_full, C::kTileBytes);
+                mbar_expect_tx(&bars.own_full, C::kTileBytes);
                 for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_4d(sDO + c * C::kBox, &map_do, &bars.x_full, c * C::A::kCols, it.h,
-                                row0, it.sp.plane);
+                    tma_load_3d(sDO + c * C::kBox, &map_qh, &bars.own_full, c * C::A::kCols, row0,
+                                it.sp.plane * H + it.h);
                 ++items;
                 for (int u = 0; ok && u < T + 2; ++u) {
                     const int ks = k_issued % KS;
@@ -982,12 +987,24 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                                         c * C::A::kCols, it.h, row0, it.sp.plane);
                     }
                     ++v_issued;
+                    if (u == 0) {
+                        // the item's dO rows, once its Qhat rows are in TMEM (behind its
+                        // first K and V tiles, whose slots free up earlier)
+                        if (!(ok = mbar_wait(&bars.q_read, (items - 1) & 1, abort_flag))) break;
+                        mbar_expect_tx(&bars.x_full, C::kTileBytes);
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_4d(sDO + c * C::kBox, &map_do, &bars.x_full, c * C::A::kCols,
+                                        it.h, row0, it.sp.plane);
+                        ++x_issued;
+                    }
                 }
             }
             if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
             // drain: every copy issued by this CTA lands before it exits (at most the
-            // last dO load, the last KS K-ring and the last VS V-ring loads in flight)
-            if (items > 0) mbar_wait(&bars.x_full, (items - 1) & 1, nullptr);
+            // last Qhat and dO loads, the last KS K-ring and the last VS V-ring loads
+            // in flight)
+            if (items > 0) mbar_wait(&bars.own_full, (items - 1) & 1, nullptr);
+            if (x_issued > 0) mbar_wait(&bars.x_full, (x_issued - 1) & 1, nullptr);
             for (int x = max(0, k_issued - KS); x < k_issued; ++x)
                 mbar_wait(&bars.st_full[x % KS], (x / KS) & 1, nullptr);
             for (int x = max(0, v_issued - VS); x < v_issued; ++x)
@@ -1031,16 +1048,27 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                 const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
                 if (it.T == 0) continue;
                 const int T = it.T;
-                // the item's Qhat rows in TMEM and dO rows in shared memory (the softmax
-                // threads store Qhat only after the previous item's epilogue, when every
-                // MMA of that item has completed), and its first K and V tiles
-                ok = mbar_wait_w(&bars.own_full, items & 1, abort_flag) &&
-                     mbar_wait_w(&bars.x_full, items & 1, abort_flag) &&
-                     mbar_wait_w(&bars.st_full[kt % KS], (kt / KS) & 1, abort_flag) &&
-                     mbar_wait_w(&bars.v_full[vt % VS], (vt / VS) & 1, abort_flag);
+                // the item's Qhat rows from the owned-row slot into TMEM. The previous
+                // item's last S MMA, which read the old ones, has completed: its dS
+                // was signalled (after the softmax threads had waited for that S)
+                // before the previous dQ MMA was issued. The copy's commit releases the
+                // slot for the dO rows and orders the copy before the S MMAs.
+                if (!(ok = mbar_wait_w(&bars.own_full, items & 1, abort_flag))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    tmem_cp128x256b_w(tmem + kTQ + kk * 8, dDO + kmajor_off<D>(kk));
+                mma_commit_w(&bars.q_read);
+                ok = mbar_wait_w(&bars.q_read, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.st_full[kt % KS], (kt / KS) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
                 issue_s(kt);
+                // the first dP once the dO rows and the first V tile have landed
+                ok = mbar_wait_w(&bars.x_full, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.v_full[vt % VS], (vt / VS) & 1, abort_flag);
+                if (!ok) break;
+                tc_fence_after();
                 issue_dp(vt);
                 if (T == 1) mma_commit_w(&bars.do_free);
                 // Per tile t: once every softmax thread holds S(t) in registers, S(t+1)
@@ -1104,25 +1132,12 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             const int tq = it.i * kTile + r;           // query position
             const size_t qrow0 = ((size_t)it.sp.plane * H + h) * sr.S + it.sp.start;
             const size_t xrow = ((size_t)it.sp.plane * sr.S + it.sp.start + tq) * H + h;   // [.., S, H, ..]
-            const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : 0.f;
-            if (wg == 0) {
-                // the owned Qhat rows become the TMEM-resident A operand of S (lane = row;
-                // a 32-bit column holds two consecutive bf16, the lower index in the low
-                // half); the previous item's MMAs have all completed (its epilogue waited)
-                uint32_t xa[D / 2];
-                const uint4 *src = reinterpret_cast<const uint4 *>(qhat + (qrow0 + tq) * D);
-#pragma unroll
-                for (int c = 0; c < D / 8; ++c) {
-                    const uint4 z = tq < S ? src[c] : make_uint4(0, 0, 0, 0);
-                    xa[4 * c] = z.x; xa[4 * c + 1] = z.y; xa[4 * c + 2] = z.z; xa[4 * c + 3] = z.w;
-                }
-                const uint32_t dst = tmem + kTQ + lane_off;
-                if constexpr (D == 128) tmem_st64_sync(dst, xa);
-                else if constexpr (D == 64) tmem_st32_sync(dst, xa);
-                else tmem_st16_sync(dst, xa);
-                tc_fence_before();
-                mbar_arrive(&bars.own_full);
-            } else if (wg == kSoftmaxWGs - 1) {
+            // Rows past the sample's end hold whatever the Qhat tile's TMA load brought
+            // (zeros past the tensor, the next sample's rows in a packed batch): an
+            // infinite lse gives them P = 0 exactly, so dS = 0 and their dQhat rows
+            // stay finite (they are never stored, and their dgamma terms are zero).
+            const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : INFINITY;
+            if (wg == kSoftmaxWGs - 1) {
                 // for the dq epilogue (read after its first named barrier; the previous
                 // item's epilogue finished reading these before the stop barrier below)
                 escr.rstd[r] = tq < S ? rstd_q[xrow] : 0.f;
@@ -1439,11 +1454,22 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     if ((e = make_epi_maps<D>(p, eo, p.H, kTile, mo, unused)) != cudaSuccess) return e;
     eo.x = ep.out;
     if ((e = make_epi_maps<D>(p, eo, p.H, kTile, mdq, unused)) != cudaSuccess) return e;
+    // Qhat [B, H, S, D] with 128-row boxes (the owned rows, copied into TMEM)
+    CUtensorMap mqh;
+    {
+        using A = Atoms<D>;
+        const uint64_t dims[3] = {D, (uint64_t)p.S, (uint64_t)p.B * p.H};
+        const uint64_t strides[2] = {D * 2, (uint64_t)p.S * D * 2};
+        const uint32_t box[3] = {(uint32_t)A::kCols, (uint32_t)kTile, 1};
+        if ((e = encode_tmap_bf16(&mqh, qhat, 3, dims, strides, box, A::kSwizzleBytes)) !=
+            cudaSuccess)
+            return e;
+    }
     e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemB);
     if (e != cudaSuccess) return e;
     k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, mdo, mo, mdq, (const bf16 *)qhat, (const bf16 *)out, lse, dlt, ep.gamma,
+        m.k, m.v, mx, mcs, mdo, mo, mdq, mqh, (const bf16 *)out, lse, dlt, ep.gamma,
         ep.rstd,
         (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_qt,
         (int)n_items, err, (test_stall_mask() & STALL_DQ_TC) != 0);

@@ -293,6 +293,19 @@ __device__ __forceinline__ void mma_commit_w(uint64_t *bar) {
         ::"r"(smem_u32(bar)) : "memory");
 }
 
+// Shared memory -> TMEM copy of a 128-row x 256-bit matrix (one k-step of 16 bf16
+// of a K-major operand, described by the same descriptor as the MMA operand):
+// row i goes to lane i, its 32 bytes to 8 consecutive 32-bit columns in address
+// order, i.e. the layout of an A operand read from TMEM. Asynchronous, issued by
+// one elected lane of a converged warp; a later tcgen05.commit tracks it like an
+// MMA.
+__device__ __forceinline__ void tmem_cp128x256b_w(uint32_t taddr, uint64_t s_desc) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.cp.cta_group::1.128x256b [%0], %1;\n}\n"
+        ::"r"(taddr), "l"(s_desc) : "memory");
+}
+
 // Bounded wait for a whole warp: every lane polls, the warp agrees on the result.
 __device__ __forceinline__ bool mbar_wait_w(uint64_t *bar, uint32_t parity, volatile int *abort_flag) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
