@@ -865,6 +865,13 @@ k_dkdv_reduce(const float *__restrict__ part, float *__restrict__ dkhat, bf16 *_
 // ---------------------------------------------------------------------------
 // dQhat and the dq epilogue
 // ---------------------------------------------------------------------------
+// L2 prefetch of [p, p + bytes), widened to 16-byte boundaries.
+__device__ __forceinline__ void l2_prefetch_span(const void *p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p) & ~(uintptr_t)15;
+    const uintptr_t e = (reinterpret_cast<uintptr_t>(p) + bytes + 15) & ~(uintptr_t)15;
+    l2_prefetch_bulk(reinterpret_cast<const void *>(a), (uint32_t)(e - a));
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreadsBwd, 1)
 k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
@@ -915,7 +922,9 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     // walked forwards and backwards in turn) and skips
     // the same empty ones. Ring uses per item: K ring, its T key tiles and then
     // the two (cos, sin) halves of its rows; V ring, its T value tiles and then its
-    // q rows (the epilogue's inputs, released by the softmax threads after it).
+    // q rows (the epilogue's inputs, released by the softmax threads after it; the
+    // epilogue writes the dq rows over them, and the producer stores that tile by
+    // TMA before it reloads the slot, so the softmax threads never wait for it).
     // The owned-row slot takes the item's Qhat rows (own_full), which the MMA warp
     // copies into TMEM once the previous item's last S MMA has run (q_read), then
     // its dO rows (x_full), held until its dP MMAs and Dlt are done (do_free): the
@@ -932,15 +941,35 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tma_prefetch_desc(&map_o);
             tma_prefetch_desc(&map_dq);
             int items = 0, x_issued = 0, k_issued = 0, v_issued = 0;
+            // a V slot holding an item's staged dq rows, to be stored by TMA once the
+            // softmax threads release the slot: (head, first row, plane), or h < 0
+            int pend_h[VS], pend_row[VS], pend_plane[VS];
+#pragma unroll
+            for (int v = 0; v < VS; ++v) pend_h[v] = -1;
+            auto store_dq = [&](int vs) {
+                for (int c = 0; c < C::kChunks; ++c)
+                    tma_store_4d(&map_dq, sV + vs * C::kTileBytes + c * C::kBox, c * C::A::kCols,
+                                 pend_h[vs], pend_row[vs], pend_plane[vs]);
+                bulk_commit();
+                pend_h[vs] = -1;
+            };
             bool ok = true;
             for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
                 const DqItem it = dq_item(w, BH, n_qt, H, G, sr);
                 if (it.T == 0) continue;
                 const int T = it.T, row0 = it.sp.start + it.i * kTile;
-                // L2 prefetch of the O rows the softmax threads read with plain loads when
-                // the item starts (after the previous item's epilogue)
-                for (int c = 0; c < C::kChunks; ++c)
-                    l2_prefetch_4d(&map_o, c * C::A::kCols, it.h, row0, it.sp.plane);
+                {
+                    // L2 prefetch of what the softmax threads read with plain loads when
+                    // the item starts (after the previous item's epilogue): the O rows,
+                    // the rows' lse and the rstd_q block of the rows (all heads)
+                    const int rows = min(kTile, it.sp.len - it.i * kTile);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        l2_prefetch_4d(&map_o, c * C::A::kCols, it.h, row0, it.sp.plane);
+                    l2_prefetch_span(lse + ((size_t)it.sp.plane * H + it.h) * sr.S + row0,
+                                     (size_t)rows * 4);
+                    l2_prefetch_span(rstd_q + ((size_t)it.sp.plane * sr.S + row0) * H,
+                                     (size_t)rows * H * 4);
+                }
                 // the item's Qhat rows, once the previous item's dP MMAs and Dlt have read
                 // its dO rows
                 if (items > 0 && !(ok = mbar_wait(&bars.do_free, (items - 1) & 1, abort_flag)))
@@ -975,6 +1004,12 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                     if (v_issued >= VS &&
                         !(ok = mbar_wait(&bars.v_empty[vs], ((v_issued / VS) - 1) & 1, abort_flag)))
                         break;
+                    if (pend_h[vs] >= 0) {
+                        // the dq rows an earlier epilogue staged here: stored before the
+                        // slot is reloaded
+                        store_dq(vs);
+                        bulk_wait_read0();
+                    }
                     uint8_t *vb = sV + vs * C::kTileBytes;
                     mbar_expect_tx(&bars.v_full[vs], C::kTileBytes);
                     for (int c = 0; c < C::kChunks; ++c) {
@@ -985,6 +1020,13 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                         else
                             tma_load_4d(vb + c * C::kBox, &map_x, &bars.v_full[vs],
                                         c * C::A::kCols, it.h, row0, it.sp.plane);
+                    }
+                    // the epilogue stages dq over the q rows unless the tile reaches past
+                    // a packed sample (those rows are stored one by one)
+                    if (u == T && (sr.cu == nullptr || it.i * kTile + kTile <= it.sp.len)) {
+                        pend_h[vs] = it.h;
+                        pend_row[vs] = row0;
+                        pend_plane[vs] = it.sp.plane;
                     }
                     ++v_issued;
                     if (u == 0) {
@@ -999,7 +1041,14 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                     }
                 }
             }
+            // the last items' staged dq rows, in ring order, once their epilogues are done
+            for (int x = max(0, v_issued - VS); ok && x < v_issued; ++x) {
+                const int vs = x % VS;
+                if (pend_h[vs] < 0) continue;
+                if ((ok = mbar_wait(&bars.v_empty[vs], (x / VS) & 1, abort_flag))) store_dq(vs);
+            }
             if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+            bulk_wait0();   // every dq store has completed
             // drain: every copy issued by this CTA lands before it exits (at most the
             // last Qhat and dO loads, the last KS K-ring and the last VS V-ring loads
             // in flight)
@@ -1260,16 +1309,10 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                                 dq + xrow * D, part,
                                 tma_out ? const_cast<uint8_t *>(sX) : nullptr);
             // every softmax thread is done with the item (finish_rows ends on a named
-            // barrier): its epilogue inputs' ring slots may be refilled (the staged dq
-            // tile once the TMA store has read it)
+            // barrier, after each thread's fence for its staged dq rows): its epilogue
+            // inputs' ring slots may be refilled (the producer first stores the staged
+            // dq tile)
             if (threadIdx.x == 0) {
-                if (tma_out && ok) {
-                    for (int c = 0; c < C::kChunks; ++c)
-                        tma_store_4d(&map_dq, sX + c * C::kBox, c * C::A::kCols, h,
-                                     it.sp.start + it.i * kTile, it.sp.plane);
-                    bulk_commit();
-                    bulk_wait_read0();
-                }
                 mbar_arrive(&bars.v_empty[xq % VS]);
                 mbar_arrive(&bars.st_empty[xc % KS]);
                 mbar_arrive(&bars.st_empty[(xc + 1) % KS]);
@@ -1281,7 +1324,6 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             tg += T;
             ++items;
         }
-        if (threadIdx.x == 0) bulk_wait0();   // the dq stores have completed
     }
     tc_fence_before();
     __syncthreads();
