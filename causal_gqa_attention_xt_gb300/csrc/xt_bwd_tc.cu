@@ -1186,35 +1186,44 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
             // infinite lse gives them P = 0 exactly, so dS = 0 and their dQhat rows
             // stay finite (they are never stored, and their dgamma terms are zero).
             const float lse2 = tq < S ? lse[qrow0 + tq] * kLog2e : INFINITY;
-            if (wg == kSoftmaxWGs - 1) {
-                // for the dq epilogue (read after its first named barrier; the previous
-                // item's epilogue finished reading these before the stop barrier below)
-                escr.rstd[r] = tq < S ? rstd_q[xrow] : 0.f;
-                if (r < D) escr.gamma[r] = gamma_q[r];
-            }
+            // rstd_q of the row for the dq epilogue (stashed below, read after the
+            // epilogue's first named barrier)
+            const float rstd_v = (wg == kSoftmaxWGs - 1 && tq < S) ? rstd_q[xrow] : 0.f;
             // Dlt = rowsum(dO o O) of the owned rows (the softmax backward's row term;
-            // the dK/dV kernel, launched after this one, reads it): warpgroup wg sums the
-            // columns [wg D/4, (wg + 1) D/4) of its thread's row, O from global memory
-            // (loaded before the wait for the dO tile, so the two latencies overlap), dO
-            // from the TMA'd tile; the four parts are added in warpgroup order.
-            uint4 orow[D / 32];
+            // the dK/dV kernel, launched after this one, reads it). Row-contiguous
+            // mapping: warp w takes rows [8w, 8w + 8) with D/8 lanes per row, a lane one
+            // 16-byte chunk (8 columns), so each load instruction reads whole O rows.
+            // O comes from global memory (loaded before the wait for the dO tile, so the
+            // two latencies overlap), dO from the TMA'd tile; the lanes of a row are
+            // summed by a fixed butterfly and the sum reaches the row's owner through
+            // shared memory.
+            constexpr int kLpr = D / 8;              // lanes per row
+            constexpr int kRpi = 32 / kLpr;          // rows per load instruction
+            constexpr int kNi = 8 / kRpi;            // load instructions per warp
+            const int dch = lane % kLpr;
+            uint4 orow[kNi];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c)
-                orow[c] = tq < S ? reinterpret_cast<const uint4 *>(out + xrow * D + wg * (D / 4))[c]
-                                 : make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < kNi; ++k) {
+                const int q = it.i * kTile + 8 * warp + k * kRpi + lane / kLpr;
+                orow[k] = q < S ? *reinterpret_cast<const uint4 *>(
+                                      out + (((size_t)it.sp.plane * sr.S + it.sp.start + q) * H + h) * D +
+                                      8 * dch)
+                                : make_uint4(0, 0, 0, 0);
+            }
             bool ok = __all_sync(0xffffffffu, mbar_wait(&bars.x_full, items & 1, abort_flag));
             {
                 using A = Atoms<D>;
-                float part0 = 0.f, part1 = 0.f;
-                if (ok && tq < S) {
+                const int col = 8 * dch;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        const int col = wg * (D / 4) + 8 * c;
+                for (int k = 0; k < kNi; ++k) {
+                    const int rr = 8 * warp + k * kRpi + lane / kLpr;
+                    float part0 = 0.f, part1 = 0.f;
+                    if (ok) {
                         const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
-                                                        r * A::kRowBytes + (col % A::kCols) * 2);
+                                                        rr * A::kRowBytes + (col % A::kCols) * 2);
                         const uint4 gv = *reinterpret_cast<const uint4 *>(sDO + swizzled<A::kRowBytes>(off));
                         const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-                        const uint32_t ow[4] = {orow[c].x, orow[c].y, orow[c].z, orow[c].w};
+                        const uint32_t ow[4] = {orow[k].x, orow[k].y, orow[k].z, orow[k].w};
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
                             part0 = fmaf(__uint_as_float(gw[e] << 16), __uint_as_float(ow[e] << 16), part0);
@@ -1222,12 +1231,21 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                                          __uint_as_float(ow[e] & 0xffff0000u), part1);
                         }
                     }
+                    float sum = part0 + part1;
+#pragma unroll
+                    for (int o = kLpr / 2; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                    if (dch == 0) escr.dot[0][rr] = sum;
                 }
-                escr.dot[wg][r] = part0 + part1;
             }
             softmax_bar_sync();   // every softmax thread reaches this (no wait above is unbounded)
             if (threadIdx.x == 0) mbar_arrive(&bars.do_free);   // no softmax thread reads sDO any more
-            const float dl = ((escr.dot[0][r] + escr.dot[1][r]) + escr.dot[2][r]) + escr.dot[3][r];
+            if (wg == kSoftmaxWGs - 1) {
+                // for the dq epilogue (the previous item's epilogue finished reading these
+                // before the stop barrier below)
+                escr.rstd[r] = rstd_v;
+                if (r < D) escr.gamma[r] = gamma_q[r];
+            }
+            const float dl = escr.dot[0][r];
             if (ok && wg == 0 && tq < S) dlt[qrow0 + tq] = dl;
             for (int t = 0; ok && t < T; ++t) {
                 const int x = tg + t;                   // key tiles before this one
