@@ -233,19 +233,23 @@ __device__ __forceinline__ DqItem dq_item(int w, int BH, int n_qt, int H, int G,
     return it;
 }
 
-// Element e of 32 bf16 packed two per word (the lower index in the low half).
-__device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[16], int e) {
+// Element e of bf16 values packed two per word (the lower index in the low half).
+template <int N>
+__device__ __forceinline__ float bf16_lo_or_hi(const uint32_t (&w)[N], int e) {
     const uint32_t v = w[e >> 1];
     return __uint_as_float((e & 1) ? (v & 0xffff0000u) : (v << 16));
 }
 
-// Transposing butterfly: every lane holds 32 values v[c] (c = column); after
-// five exchange steps lane l holds the sum over the 32 lanes of column l (each
-// step a lane keeps half of its columns, sends the other half to the partner
-// lane and adds the partner's copy of the kept half). Fixed association.
-__device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
+// Transposing butterfly: every lane holds V values v[c] (c = column, V = 8, 16
+// or 32); after log2 V exchange steps lane l holds the sum over its group of V
+// lanes of column l % V (each step a lane keeps half of its columns, sends the
+// other half to the partner lane and adds the partner's copy of the kept half),
+// and the 32 / V groups are then added by xor shuffles: every lane l ends with
+// the sum over the warp of column l % V. Fixed association.
+template <int V>
+__device__ __forceinline__ float transpose_sum(float (&v)[V], int lane) {
 #pragma unroll
-    for (int n = 16; n >= 1; n >>= 1) {
+    for (int n = V / 2; n >= 1; n >>= 1) {
         const bool up = (lane & n) != 0;
 #pragma unroll
         for (int e = 0; e < n; ++e) {
@@ -254,9 +258,41 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
             v[e] = keep + __shfl_xor_sync(0xffffffffu, send, n);
         }
     }
-    return v[0];
+    float s = v[0];
+#pragma unroll
+    for (int m = V; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+    return s;
 }
 
+// N consecutive TMEM columns (N = 4, 8 or 16) from each of two addresses, then
+// one wait (32x32b shape: thread i of the warp reads lane base + i).
+template <int N>
+__device__ __forceinline__ void tmem_ld_pair_n(uint32_t ta, uint32_t (&a)[N], uint32_t tb,
+                                               uint32_t (&b)[N]) {
+    if constexpr (N == 16) {
+        tmem_ld16_pair_sync(ta, a, tb, b);
+    } else if constexpr (N == 8) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%16];\n"
+            "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%17];\n"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]),
+              "=r"(a[7]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]),
+              "=r"(b[6]), "=r"(b[7])
+            : "r"(ta), "r"(tb)
+            : "memory");
+    } else {
+        static_assert(N == 4, "4, 8 or 16 columns");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%8];\n"
+            "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%4, %5, %6, %7}, [%9];\n"
+            "tcgen05.wait::ld.sync.aligned;"
+            : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(b[0]), "=r"(b[1]), "=r"(b[2]),
+              "=r"(b[3])
+            : "r"(ta), "r"(tb)
+            : "memory");
+    }
+}
 
 // The epilogue that turns the gradient of 128 normed-and-rotated rows into the
 // gradient of the raw rows (Mint project report 5.4.4: RoPE backward, the
@@ -265,15 +301,16 @@ __device__ __forceinline__ float transpose_sum32(float (&v)[32], int lane) {
 // row r = TMEM lane). Inputs: the accumulator in TMEM columns [0, D) at `tacc`
 // (this warp's lanes; the gradient times sqrt(D)), the raw rows in shared
 // memory as D / kCols TMA boxes of 128 rows (tc::Atoms<D> layout), this
-// thread's (cos, sin) row of pairs [16 wg, 16 wg + 16) at `cs_row` (a 128-byte
-// row of a 128-byte-swizzled fp32 box, unswizzled start), and rstd and gamma
-// in escr (written before the call by other threads: the first named barrier
-// orders them). Warpgroup wg < D/32 takes the 16 pairs [16 wg, 16 wg + 16)
-// (columns 16 wg.. and D/2 + 16 wg..) of its row; the row's dot product is
-// summed over those warpgroups in order. The dgamma terms are summed over the
-// warp's rows by a transposing butterfly, then over the four row quarters in
-// order, into part[0, D). Every softmax thread must call this (it holds three
-// named barriers); with ok false it only writes a zero partial.
+// thread's row of the (cos, sin) pieces at `cs_row` (piece c holds pairs
+// [16 c, 16 c + 16): a 128-byte row of a 128-byte-swizzled fp32 box at
+// cs_row + c * kCsPieceBytes, unswizzled start), and rstd and gamma in escr
+// (written before the call by other threads: the first named barrier orders
+// them). Warpgroup wg takes the P = D/8 pairs [P wg, P wg + P) (columns P wg..
+// and D/2 + P wg..) of its row; the row's dot product is summed over the four
+// warpgroups in order. The dgamma terms are summed over the warp's rows by a
+// transposing butterfly, then over the four row quarters in order, into
+// part[0, D). Every softmax thread must call this (it holds three named
+// barriers); with ok false it only writes a zero partial.
 template <int D>
 __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int lane,
                                             uint32_t tacc, const uint8_t *sX,
@@ -281,37 +318,54 @@ __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int la
                                             EpiScratch &escr, bf16 *dst_row, float *part,
                                             uint8_t *stage) {
     using A = Atoms<D>;
-    constexpr int kHalf = D / 2, kEpiWGs = D / 32;
-    const bool in_epi = wg < kEpiWGs;
-    const int i0 = wg * 16;
+    constexpr int kHalf = D / 2;
+    constexpr int kP = D / 8;             // pairs per warpgroup (all four take part)
+    constexpr int kXW = kP / 2;           // 32-bit words of x (and of dq) per row half
+    const int i0 = wg * kP;
     const int r = quarter * 32 + lane;
+    // the swizzled place of column `col` of this thread's row in a tile
+    auto xoff = [&](int col) -> uint32_t {
+        return swizzled<A::kRowBytes>((uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
+                                                 r * A::kRowBytes + (col % A::kCols) * 2));
+    };
     softmax_bar_sync();   // the stashed gamma and rstd are visible from here on
-    uint32_t xw[16];      // the row's x: 8 words of the low pairs' columns, then 8 of the high
-    float dy[32];         // dy[e] (e < 16): column i0 + e; dy[16 + e]: column D/2 + i0 + e
+    uint32_t xw[2 * kXW]; // the row's x: kXW words of the low pairs' columns, then kXW of the high
+    float dy[2 * kP];     // dy[e] (e < kP): column i0 + e; dy[kP + e]: column D/2 + i0 + e
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dy[e] = 0.f;
+    for (int e = 0; e < 2 * kP; ++e) dy[e] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 16; ++e) xw[e] = 0u;
-    if (ok && in_epi) {
+    for (int e = 0; e < 2 * kXW; ++e) xw[e] = 0u;
+    if (ok) {
         tc_fence_after();
+        // x: kP columns of each half, in 16-byte chunks of 8 (8 bytes when kP = 4)
 #pragma unroll
-        for (int part8 = 0; part8 < 4; ++part8) {
-            // 8-column chunks: i0, i0+8 (low), D/2+i0, D/2+i0+8 (high)
-            const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
-            const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
-                                            r * A::kRowBytes + (col % A::kCols) * 2);
-            const uint4 v = *reinterpret_cast<const uint4 *>(sX + swizzled<A::kRowBytes>(off));
-            xw[4 * part8] = v.x; xw[4 * part8 + 1] = v.y;
-            xw[4 * part8 + 2] = v.z; xw[4 * part8 + 3] = v.w;
+        for (int hh = 0; hh < 2; ++hh) {
+            const int cb = hh * kHalf + i0;
+            if constexpr (kP >= 8) {
+#pragma unroll
+                for (int c8 = 0; c8 < kP / 8; ++c8) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(sX + xoff(cb + 8 * c8));
+                    xw[hh * kXW + 4 * c8] = v.x; xw[hh * kXW + 4 * c8 + 1] = v.y;
+                    xw[hh * kXW + 4 * c8 + 2] = v.z; xw[hh * kXW + 4 * c8 + 3] = v.w;
+                }
+            } else {
+                const uint2 v = *reinterpret_cast<const uint2 *>(sX + xoff(cb));
+                xw[hh * kXW] = v.x; xw[hh * kXW + 1] = v.y;
+            }
         }
-        uint32_t a[16], b[16];
-        tmem_ld16_pair_sync(tacc + i0, a, tacc + kHalf + i0, b);
+        uint32_t a[kP], b[kP];
+        tmem_ld_pair_n<kP>(tacc + i0, a, tacc + kHalf + i0, b);
         const float scale = rsqrtf((float)D);
+        // this warpgroup's pairs lie in piece i0 / 16 (kP divides 16), from pair i0 % 16
+        const uint8_t *cs_p = cs_row + (i0 >> 4) * kCsPieceBytes;
+        const int j0 = kP == 16 ? 0 : (i0 & 15);
         float dotp = 0.f;
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-            // (cos, sin) of pairs e, e+1: the 16-byte chunk e/2 of the swizzled row
-            const float4 c2 = *reinterpret_cast<const float4 *>(cs_row + (((e >> 1) ^ (r & 7)) << 4));
+        for (int e = 0; e < kP; e += 2) {
+            // (cos, sin) of pairs i0 + e, i0 + e + 1: 16-byte chunk (j0 + e) / 2 of the
+            // swizzled row
+            const float4 c2 = *reinterpret_cast<const float4 *>(
+                cs_p + ((((j0 + e) >> 1) ^ (r & 7)) << 4));
             const float cv[2] = {c2.x, c2.z}, sv[2] = {c2.y, c2.w};
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
@@ -321,64 +375,79 @@ __device__ __forceinline__ void finish_rows(bool ok, int wg, int quarter, int la
                 const float dyl = gl * cv[x] + gh * sv[x];
                 const float dyh = gh * cv[x] - gl * sv[x];
                 dy[e + x] = dyl;
-                dy[16 + e + x] = dyh;
+                dy[kP + e + x] = dyh;
                 dotp = fmaf(escr.gamma[i0 + e + x] * dyl, bf16_lo_or_hi(xw, e + x), dotp);
-                dotp = fmaf(escr.gamma[kHalf + i0 + e + x] * dyh, bf16_lo_or_hi(xw, 16 + e + x),
-                            dotp);
+                dotp = fmaf(escr.gamma[kHalf + i0 + e + x] * dyh,
+                            bf16_lo_or_hi(xw, 2 * kXW + e + x), dotp);
             }
         }
         escr.dot[wg][r] = dotp;
     }
     softmax_bar_sync();
-    if (ok && in_epi) {
-        float dot = 0.f;
-#pragma unroll
-        for (int w = 0; w < kEpiWGs; ++w) dot += escr.dot[w][r];
+    if (ok) {
+        const float dot = ((escr.dot[0][r] + escr.dot[1][r]) + escr.dot[2][r]) + escr.dot[3][r];
         const float rr = escr.rstd[r];
         const float corr = dot * rr * rr * rr * (1.0f / (float)D);
-        uint32_t ow[16];
+        uint32_t ow[2 * kXW];
 #pragma unroll
-        for (int e = 0; e < 16; e += 2) {
+        for (int e = 0; e < kP; e += 2) {
             float ol[2], oh[2];
 #pragma unroll
             for (int x = 0; x < 2; ++x) {
-                const float xl = bf16_lo_or_hi(xw, e + x), xh = bf16_lo_or_hi(xw, 16 + e + x);
+                const float xl = bf16_lo_or_hi(xw, e + x);
+                const float xh = bf16_lo_or_hi(xw, 2 * kXW + e + x);
                 ol[x] = escr.gamma[i0 + e + x] * dy[e + x] * rr - xl * corr;
-                oh[x] = escr.gamma[kHalf + i0 + e + x] * dy[16 + e + x] * rr - xh * corr;
+                oh[x] = escr.gamma[kHalf + i0 + e + x] * dy[kP + e + x] * rr - xh * corr;
                 // the dgamma terms replace dy
                 dy[e + x] = dy[e + x] * xl * rr;
-                dy[16 + e + x] = dy[16 + e + x] * xh * rr;
+                dy[kP + e + x] = dy[kP + e + x] * xh * rr;
             }
             ow[e / 2] = pack_bf16x2(ol[0], ol[1]);
-            ow[8 + e / 2] = pack_bf16x2(oh[0], oh[1]);
+            ow[kXW + e / 2] = pack_bf16x2(oh[0], oh[1]);
         }
         if (stage != nullptr) {
-            // in place of the x chunks this thread read (the caller stores the tile by TMA)
+            // in place of the x pieces this thread read (the caller stores the tile by TMA)
 #pragma unroll
-            for (int part8 = 0; part8 < 4; ++part8) {
-                const int col = (part8 < 2 ? 0 : kHalf) + i0 + 8 * (part8 & 1);
-                const uint32_t off = (uint32_t)((col / A::kCols) * A::box_bytes(kTile) +
-                                                r * A::kRowBytes + (col % A::kCols) * 2);
-                *reinterpret_cast<uint4 *>(stage + swizzled<A::kRowBytes>(off)) =
-                    make_uint4(ow[4 * part8], ow[4 * part8 + 1], ow[4 * part8 + 2], ow[4 * part8 + 3]);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int cb = hh * kHalf + i0;
+                if constexpr (kP >= 8) {
+#pragma unroll
+                    for (int c8 = 0; c8 < kP / 8; ++c8)
+                        *reinterpret_cast<uint4 *>(stage + xoff(cb + 8 * c8)) =
+                            make_uint4(ow[hh * kXW + 4 * c8], ow[hh * kXW + 4 * c8 + 1],
+                                       ow[hh * kXW + 4 * c8 + 2], ow[hh * kXW + 4 * c8 + 3]);
+                } else {
+                    *reinterpret_cast<uint2 *>(stage + xoff(cb)) =
+                        make_uint2(ow[hh * kXW], ow[hh * kXW + 1]);
+                }
             }
             fence_proxy_async_smem();
         } else if (row_ok) {
-            uint4 *dst = reinterpret_cast<uint4 *>(dst_row);
-            dst[i0 / 8] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-            dst[i0 / 8 + 1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-            dst[(kHalf + i0) / 8] = make_uint4(ow[8], ow[9], ow[10], ow[11]);
-            dst[(kHalf + i0) / 8 + 1] = make_uint4(ow[12], ow[13], ow[14], ow[15]);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                bf16 *dst = dst_row + hh * kHalf + i0;
+                if constexpr (kP >= 8) {
+#pragma unroll
+                    for (int c8 = 0; c8 < kP / 8; ++c8)
+                        reinterpret_cast<uint4 *>(dst)[c8] =
+                            make_uint4(ow[hh * kXW + 4 * c8], ow[hh * kXW + 4 * c8 + 1],
+                                       ow[hh * kXW + 4 * c8 + 2], ow[hh * kXW + 4 * c8 + 3]);
+                } else {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(ow[hh * kXW], ow[hh * kXW + 1]);
+                }
+            }
         }
-        // column sums over the warp's 32 rows: lane l ends with column l of dy
-        escr.g[wg][quarter][lane] = transpose_sum32(dy, lane);
+        // column sums over the warp's 32 rows: lane l ends with column l % 2P of dy
+        const float g = transpose_sum<2 * kP>(dy, lane);
+        if (lane < 2 * kP) escr.g[wg][quarter][lane] = g;
     }
     softmax_bar_sync();
     if (threadIdx.x < D) {
         // column d of the partial: the four row quarters of its warpgroup, in order
         const int d = threadIdx.x;
-        const int w = (d < kHalf ? d : d - kHalf) / 16;
-        const int l = (d < kHalf ? 0 : 16) + (d & 15);
+        const int pd = d < kHalf ? d : d - kHalf;
+        const int w = pd / kP;
+        const int l = (d < kHalf ? 0 : kP) + pd % kP;
         float sum = 0.f;
         if (ok) {
 #pragma unroll
@@ -819,7 +888,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
                                               abort_flag));
             const uint8_t *sX = sStage + (x0 % HS) * C::kHStageBytes;
             const uint8_t *cs_row = sStage + ((x0 + 1 + (r >> 6)) % HS) * C::kHStageBytes +
-                                    wg * kCsPieceBytes + (r & 63) * 128;
+                                    (r & 63) * 128;
             finish_rows_dk<D>(ok, wg, quarter, lane, tmem + 384 + lane_off, sX, cs_row, kp < S,
                               escr, dk + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D,
                               pk);
@@ -1317,8 +1386,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
                                               abort_flag));
             if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
             const uint8_t *sX = sV + (xq % VS) * C::kTileBytes;
-            const uint8_t *cs_row = sK + ((xc + (r >> 6)) % KS) * C::kTileBytes + wg * kCsPieceBytes +
-                                    (r & 63) * 128;
+            const uint8_t *cs_row = sK + ((xc + (r >> 6)) % KS) * C::kTileBytes + (r & 63) * 128;
             // dq rows: written over the q rows in shared memory and stored by one TMA
             // store, unless the tile reaches past a packed sample (its last rows would
             // land on the next sample's; those tiles store row by row)
