@@ -594,6 +594,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     }
     __syncthreads();
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem = bars.tmem_base;
 
     if (warp == kWarpTma) {
@@ -908,6 +909,7 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
 __global__ void __launch_bounds__(256)
 k_dkdv_reduce(const float *__restrict__ part, float *__restrict__ dkhat, bf16 *__restrict__ dv,
               const SeqRows sr, int H, int G, int D, int n_kvt, int chunk, int nw) {
+    pdl_enter();
     const int j = blockIdx.x, bg = blockIdx.y;
     const int unit = bg / G, g = bg - unit * G, group = H / G;
     int w0 = 0;
@@ -985,6 +987,7 @@ k_bwd_dq_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ C
     }
     __syncthreads();
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem = bars.tmem_base;
 
     // Every role walks the same items (snake_item: rounds of gridDim.x items,
@@ -1549,11 +1552,11 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
     auto kern = split ? k_bwd_dkdv_tc<D, true> : k_bwd_dkdv_tc<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
     if (e != cudaSuccess) return e;
-    kern<<<(unsigned)blocks, kThreadsBwd, C::kSmemA, st>>>(
-        m.k, m.v, m.q, m.dout, mx, mcs, lse, dlt, dkhat, (bf16 *)dv, part, ek.gamma, ek.rstd,
-        (bf16 *)ek.out, ek.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, pl.n_kvt, pl.chunk,
-        pl.nw, err, (test_stall_mask() & STALL_DKDV_TC) != 0);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)blocks), dim3(kThreadsBwd), C::kSmemA, st, m.k,
+                            m.v, m.q, m.dout, mx, mcs, lse, dlt, dkhat, (bf16 *)dv, part, ek.gamma,
+                            ek.rstd, (bf16 *)ek.out, ek.part, SeqRows{p.cu, p.S, p.max_len}, p.H,
+                            p.G, pl.n_kvt, pl.chunk, pl.nw, err,
+                            (int)((test_stall_mask() & STALL_DKDV_TC) != 0));
 }
 
 template <int D>
@@ -1596,12 +1599,11 @@ cudaError_t launch_dq_d(const Problem &p, const BwdMaps &m, const void *qhat, co
     e = cudaFuncSetAttribute(k_bwd_dq_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemB);
     if (e != cudaSuccess) return e;
-    k_bwd_dq_tc<D><<<(unsigned)blocks, kThreadsBwd, C::kSmemB, st>>>(
-        m.k, m.v, mx, mcs, mdo, mo, mdq, mqh, (const bf16 *)out, lse, dlt, ep.gamma,
-        ep.rstd,
-        (bf16 *)ep.out, ep.part, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_qt,
-        (int)n_items, err, (test_stall_mask() & STALL_DQ_TC) != 0);
-    return cudaGetLastError();
+    return launch_dependent(k_bwd_dq_tc<D>, dim3((unsigned)blocks), dim3(kThreadsBwd), C::kSmemB,
+                            st, m.k, m.v, mx, mcs, mdo, mo, mdq, mqh, (const bf16 *)out, lse, dlt,
+                            ep.gamma, ep.rstd, (bf16 *)ep.out, ep.part,
+                            SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_qt, (int)n_items,
+                            err, (int)((test_stall_mask() & STALL_DQ_TC) != 0));
 }
 
 template <int D>
@@ -1648,9 +1650,9 @@ cudaError_t launch_dkdv_reduce(const Problem &p, const float *part, float *dkhat
     const DkdvPlan pl = dkdv_plan(p);
     if (pl.n_split == 0) return cudaSuccess;
     dim3 grid((unsigned)pl.n_split, (unsigned)((long)p.units * p.G));
-    k_dkdv_reduce<<<grid, 256, 0, st>>>(part, dkhat, (bf16 *)dv, SeqRows{p.cu, p.S, p.max_len},
-                                         p.H, p.G, p.D, pl.n_kvt, pl.chunk, pl.nw);
-    return cudaGetLastError();
+    return launch_dependent(k_dkdv_reduce, grid, dim3(256), 0, st, part, dkhat, (bf16 *)dv,
+                            SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, p.D, pl.n_kvt, pl.chunk,
+                            pl.nw);
 }
 
 size_t dq_part_count(const Problem &p) {

@@ -111,4 +111,15 @@ __device__ __forceinline__ SeqSpan seq_span(const SeqRows &sr, int u) {
     return SeqSpan{0, s0, s1 - s0};
 }
 
+// Programmatic dependent launch (kernels launched with launch_dependent): lets
+// the next kernel on the stream be scheduled (its CTAs take SMs as they free up
+// and run their set-up), then waits until the earlier grids on the stream have
+// completed and their writes are visible. Every thread calls it before its
+// first global-memory access; in a kernel launched the ordinary way it returns
+// at once.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 }  // namespace xt

@@ -482,24 +482,6 @@ cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Launches `kernel` as a programmatic dependent of the previous launch on the
-// stream: it may start before that grid ends and waits for it (griddepcontrol)
-// before touching its results.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t st, Args... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
 
 }  // namespace
 
@@ -551,7 +533,7 @@ cudaError_t launch_decode_rows(const Problem &p, const int *pos, const void *q, 
                                const void *v, const float *gq, const float *gk, float *qhat,
                                void *kc, void *vc, unsigned int *err, cudaStream_t st) {
     dim3 grid((p.H + 2 * p.G + 7) / 8, p.B);
-    const RopeConsts rc = make_rope_consts(p.theta, p.D);
+    const RopeConsts &rc = rope_consts(p.theta, p.D);
     if (p.dtype == 1)
         k_decode_rows<bf16><<<grid, 256, 0, st>>>(pos, (const bf16 *)q, (const bf16 *)k,
                                                   (const bf16 *)v, gq, gk, qhat, (bf16 *)kc,

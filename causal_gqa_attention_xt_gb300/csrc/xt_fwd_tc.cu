@@ -172,6 +172,7 @@ k_fwd_tc(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUte
     }
     __syncthreads();
     tc_fence_after();
+    pdl_enter();
     const uint32_t tmem = bars.tmem_base;
 
     // Every role walks the same items (snake_item: rounds of gridDim.x items,
@@ -458,10 +459,10 @@ cudaError_t launch_fwd_tc_d(const Problem &p, const void *qhat, const void *khat
     cudaError_t e = cudaFuncSetAttribute(k_fwd_tc<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    k_fwd_tc<D><<<(unsigned)blocks, kThreadsFwd, C::kSmemBytes, st>>>(
-        mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, (int)BH, n_pairs,
-        (int)n_items, err, (test_stall_mask() & STALL_FWD_TC) != 0);
-    return cudaGetLastError();
+    return launch_dependent(k_fwd_tc<D>, dim3((unsigned)blocks), dim3(kThreadsFwd), C::kSmemBytes,
+                            st, mq, mk, mv, (bf16 *)out, lse, SeqRows{p.cu, p.S, p.max_len}, p.H,
+                            p.G, (int)BH, n_pairs, (int)n_items, err,
+                            (int)((test_stall_mask() & STALL_FWD_TC) != 0));
 }
 
 }  // namespace

@@ -104,6 +104,25 @@ cudaError_t launch_decode_combine(const Problem &p, const DecodePlan &d, const f
 // ---- TMA tensor maps and the SM count (xt_tmap.cu) ----
 // Multiprocessors of the current device (queried once per device).
 int sm_count();
+
+// Launches `kernel` as a programmatic dependent of the previous launch on the
+// stream: it may be scheduled before that grid ends; the kernel waits for it
+// (pdl_enter, griddepcontrol) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 // swizzle_bytes: 128 or 64 (the smem row width of the box, see tc::Atoms).
 cudaError_t encode_tmap_bf16(CUtensorMap *map, const void *base, int rank, const uint64_t *dims,
                              const uint64_t *strides_bytes, const uint32_t *box,

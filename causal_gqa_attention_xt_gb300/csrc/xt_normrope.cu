@@ -90,6 +90,7 @@ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv &f) {
 __global__ void __launch_bounds__(256)
 k_rope_table(float2 *__restrict__ tab, int S, int half, const int *__restrict__ cu, int units,
              int max_len, unsigned int *err, const __grid_constant__ RopeConsts rc) {
+    pdl_enter();
     __shared__ float fhi[kRopeMaxHalf], flo[kRopeMaxHalf];
     __shared__ double fd[kRopeMaxHalf];
     for (int i = threadIdx.x; i < half; i += blockDim.x) {
@@ -258,6 +259,7 @@ k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__rest
            const float *__restrict__ gk, const float2 *__restrict__ tab, T *__restrict__ qhat,
            T *__restrict__ khat, float *__restrict__ rstd_q, float *__restrict__ rstd_k, int S,
            int H, int G, int D, float eps, const UnitGeo geo, unsigned int *err) {
+    pdl_enter();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int NS = kStagesPro;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -403,6 +405,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
            T *__restrict__ dq, T *__restrict__ dk, float *__restrict__ part_q,
            float *__restrict__ part_k, int S, int H, int G, int D, const UnitGeo geo,
            unsigned int *err) {
+    pdl_enter();
     constexpr int VEC = 16 / sizeof(T);
     constexpr int NS = kStagesEpi;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -542,6 +545,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
 __global__ void __launch_bounds__(1024)
 k_dgamma_reduce(const float *__restrict__ part_q, const float *__restrict__ part_k,
                 int nparts_q, int nparts_k, int D, float *__restrict__ dgq, float *__restrict__ dgk) {
+    pdl_enter();
     constexpr int kCols = 8, kSlices = 128;
     __shared__ float red[kSlices][kCols + 1];
     const float *part = blockIdx.y == 0 ? part_q : part_k;
@@ -635,10 +639,8 @@ cudaError_t launch_rope_table(const Problem &p, void *tab, unsigned int *err, cu
     const long n = (long)p.S * (p.D / 2);
     long blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    k_rope_table<<<(unsigned)blocks, 256, 0, st>>>((float2 *)tab, p.S, p.D / 2, p.cu, p.units,
-                                                   p.max_len, err,
-                                                   make_rope_consts(p.theta, p.D));
-    return cudaGetLastError();
+    return launch_dependent(k_rope_table, dim3((unsigned)blocks), dim3(256), 0, st, (float2 *)tab,
+                            p.S, p.D / 2, p.cu, p.units, p.max_len, err, rope_consts(p.theta, p.D));
 }
 
 cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, const float *gq,
@@ -652,16 +654,16 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = set_smem(k_prologue<bf16>, smem)) != cudaSuccess) return e;
-        k_prologue<bf16><<<grid, kThreads, smem, st>>>(
-            (const bf16 *)q, (const bf16 *)k, gq, gk, (const float2 *)tab, (bf16 *)qhat,
-            (bf16 *)khat, rstd_q, rstd_k, p.S, p.H, p.G, p.D, p.eps, geo, err);
-    } else {
-        if ((e = set_smem(k_prologue<float>, smem)) != cudaSuccess) return e;
-        k_prologue<float><<<grid, kThreads, smem, st>>>(
-            (const float *)q, (const float *)k, gq, gk, (const float2 *)tab, (float *)qhat,
-            (float *)khat, rstd_q, rstd_k, p.S, p.H, p.G, p.D, p.eps, geo, err);
+        return launch_dependent(k_prologue<bf16>, dim3(grid), dim3(kThreads), smem, st,
+                                (const bf16 *)q, (const bf16 *)k, gq, gk, (const float2 *)tab,
+                                (bf16 *)qhat, (bf16 *)khat, rstd_q, rstd_k, p.S, p.H, p.G, p.D,
+                                p.eps, geo, err);
     }
-    return cudaGetLastError();
+    if ((e = set_smem(k_prologue<float>, smem)) != cudaSuccess) return e;
+    return launch_dependent(k_prologue<float>, dim3(grid), dim3(kThreads), smem, st,
+                            (const float *)q, (const float *)k, gq, gk, (const float2 *)tab,
+                            (float *)qhat, (float *)khat, rstd_q, rstd_k, p.S, p.H, p.G, p.D, p.eps,
+                            geo, err);
 }
 
 cudaError_t launch_bwd_pre(const Problem &p, const void *out, const void *dout, float *dlt,
@@ -703,16 +705,18 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
     cudaError_t e;
     if (p.dtype == 1) {
         if ((e = set_smem(k_epilogue<bf16>, smem)) != cudaSuccess) return e;
-        k_epilogue<bf16><<<grid, kThreads, smem, st>>>(
-            dqhat, dkhat, (const bf16 *)q, (const bf16 *)k, gq, gk, rstd_q, rstd_k,
-            (const float2 *)tab, (bf16 *)dq, (bf16 *)dk, part_q, part_k, p.S, p.H, p.G, p.D, geo,
-            err);
+        e = launch_dependent(k_epilogue<bf16>, dim3(grid), dim3(kThreads), smem, st, dqhat, dkhat,
+                             (const bf16 *)q, (const bf16 *)k, gq, gk, rstd_q, rstd_k,
+                             (const float2 *)tab, (bf16 *)dq, (bf16 *)dk, part_q, part_k, p.S, p.H,
+                             p.G, p.D, geo, err);
+        if (e != cudaSuccess) return e;
     } else {
         if ((e = set_smem(k_epilogue<float>, smem)) != cudaSuccess) return e;
-        k_epilogue<float><<<grid, kThreads, smem, st>>>(
-            dqhat, dkhat, (const float *)q, (const float *)k, gq, gk, rstd_q, rstd_k,
-            (const float2 *)tab, (float *)dq, (float *)dk, part_q, part_k, p.S, p.H, p.G, p.D,
-            geo, err);
+        e = launch_dependent(k_epilogue<float>, dim3(grid), dim3(kThreads), smem, st, dqhat,
+                             dkhat, (const float *)q, (const float *)k, gq, gk, rstd_q, rstd_k,
+                             (const float2 *)tab, (float *)dq, (float *)dk, part_q, part_k, p.S,
+                             p.H, p.G, p.D, geo, err);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -720,9 +724,8 @@ cudaError_t launch_epilogue(const Problem &p, const float *dqhat, const float *d
 cudaError_t launch_dgamma_reduce(const Problem &p, const float *part_q, const float *part_k,
                                  int nparts_q, int nparts_k, float *dgq, float *dgk,
                                  cudaStream_t st) {
-    k_dgamma_reduce<<<dim3((p.D + 7) / 8, 2), 1024, 0, st>>>(part_q, part_k, nparts_q, nparts_k,
-                                                             p.D, dgq, dgk);
-    return cudaGetLastError();
+    return launch_dependent(k_dgamma_reduce, dim3((p.D + 7) / 8, 2), dim3(1024), 0, st, part_q,
+                            part_k, nparts_q, nparts_k, p.D, dgq, dgk);
 }
 
 }  // namespace xt

@@ -44,6 +44,21 @@ inline RopeConsts make_rope_consts(double theta, int D) {
     return f;
 }
 
+// The frequencies of the last (theta, D) this host thread asked for: calls
+// with the same model shape skip the D/2 pow() evaluations, which otherwise
+// delay the first launch of each call.
+inline const RopeConsts &rope_consts(double theta, int D) {
+    thread_local double c_theta = -1.0;
+    thread_local int c_D = -1;
+    thread_local RopeConsts c;
+    if (theta != c_theta || D != c_D) {
+        c = make_rope_consts(theta, D);
+        c_theta = theta;
+        c_D = D;
+    }
+    return c;
+}
+
 // (cos, sin) of s * f for f = hi + lo (fd the same frequency in double).
 __device__ __forceinline__ float2 rope_cos_sin(int s, float hi, float lo, double fd) {
     float red;
