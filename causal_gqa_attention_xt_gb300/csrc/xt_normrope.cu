@@ -33,6 +33,7 @@
 //
 // RoPE angles: xt_rope.cuh (one table per call, read by the prologue and the
 // epilogue).
+#include <algorithm>
 #include "xt_common.cuh"
 #include "xt_internal.h"
 #include "xt_rope.cuh"
@@ -125,13 +126,16 @@ k_rope_table(float2 *__restrict__ tab, int S, int half, const int *__restrict__ 
 }
 
 // ---------------------------------------------------------------- units
-// Units: u = (b * S + s) * (nqc + nkc) + chunk; chunk < nqc are q-head chunks
-// of HC heads, the rest k-head chunks.
+// Units: u = (b * SG + sg) * (nqc + nkc) + chunk; chunk < nqc are q-head chunks
+// of HC heads, the rest k-head chunks; position group sg holds positions
+// [P sg, P sg + P) (P = 1 unless one chunk covers all heads of each tensor, when a
+// unit may take several positions: their rows are contiguous then).
 struct UnitGeo {
     int HC;           // heads per unit
     int nqc, nkc;     // chunks over the q heads and over the k heads
-    int units;        // B * S * (nqc + nkc)
-    FastDiv fd_chunks, fd_S;
+    int P;            // positions per unit
+    int units;        // B * SG * (nqc + nkc), SG = ceil(S / P)
+    FastDiv fd_chunks, fd_S;   // fd_S divides by SG
     int y_off;        // stage offset of the second input's rows
     int r_off;        // stage offset of the rstd words
     int t_off;        // stage offset of the cos/sin row
@@ -139,17 +143,20 @@ struct UnitGeo {
 };
 
 struct Unit {
-    int b, s;         // batch element, position
+    int b, s;         // batch element, first position
+    int np;           // positions [s, s + np)
     int h0, nh;       // heads [h0, h0 + nh) of q (isq) or of k
     bool isq;
 };
 
-__device__ __forceinline__ Unit decode_unit(uint32_t u, const UnitGeo &g, int H, int G) {
+__device__ __forceinline__ Unit decode_unit(uint32_t u, const UnitGeo &g, int H, int G, int S) {
     Unit t;
     const uint32_t bs = fdiv(u, g.fd_chunks);
     const int ch = (int)(u - bs * (uint32_t)(g.nqc + g.nkc));
     t.b = (int)fdiv(bs, g.fd_S);
-    t.s = (int)(bs - (uint32_t)t.b * g.fd_S.d);
+    const int sg = (int)(bs - (uint32_t)t.b * g.fd_S.d);
+    t.s = sg * g.P;
+    t.np = g.P == 1 ? 1 : min(g.P, S - t.s);
     t.isq = ch < g.nqc;
     t.h0 = (t.isq ? ch : ch - g.nqc) * g.HC;
     t.nh = min(g.HC, (t.isq ? H : G) - t.h0);
@@ -277,31 +284,38 @@ k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__rest
     const int cc = lane_has ? c : 0;              // clamped column group for the loads
     const float inv_d = 1.0f / (float)D;
 
+    // a unit's rows (np positions x nh heads, contiguous in q / k: with np > 1 the
+    // chunk holds all heads) and its np table rows
     auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
-        const Unit t = decode_unit(u, geo, H, G);
-        const uint32_t xb = (uint32_t)t.nh * xrow;
+        const Unit t = decode_unit(u, geo, H, G, S);
+        const uint32_t xb = (uint32_t)(t.np * t.nh) * xrow;
         if (lane == 0) {
-            mbar_expect_tx(bar, xb + trow);
+            mbar_expect_tx(bar, xb + (uint32_t)t.np * trow);
             const T *x = t.isq ? q + (((size_t)t.b * S + t.s) * H + t.h0) * D
                                : k + (((size_t)t.b * S + t.s) * G + t.h0) * D;
             bulk_load(buf, x, xb, bar);
-            bulk_load(buf + geo.t_off, tab + (size_t)t.s * half, trow, bar);
+            bulk_load(buf + geo.t_off, tab + (size_t)t.s * half, (uint32_t)t.np * trow, bar);
         }
     };
     auto process = [&](uint32_t u, const unsigned char *buf) {
-        const Unit t = decode_unit(u, geo, H, G);
+        const Unit t = decode_unit(u, geo, H, G, S);
         const int NH = t.isq ? H : G;
         float glo[VEC], ghi[VEC], cv[VEC], sv[VEC];
         const float *gamma = t.isq ? gq : gk;
         ldg_f32<VEC>(gamma + cc * VEC, glo);
         ldg_f32<VEC>(gamma + half + cc * VEC, ghi);
-        load_cs<VEC>(reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC, cv, sv);
+        const float2 *tb = reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC;
+        if (geo.P == 1) load_cs<VEC>(tb, cv, sv);
         T *obase = (t.isq ? qhat : khat) + (((size_t)t.b * NH + t.h0) * S + t.s) * D;
         float *rbase = (t.isq ? rstd_q : rstd_k) + ((size_t)t.b * S + t.s) * NH + t.h0;
-        for (int lh0 = 0; lh0 < t.nh; lh0 += rpi) {
-            const int lh = lh0 + sub;
-            const bool ok = lh < t.nh && lane_has;
-            const T *x = reinterpret_cast<const T *>(buf + (size_t)min(lh, t.nh - 1) * xrow);
+        const int nrow = t.np * t.nh;   // row l: position l / nh of the unit, head l % nh
+        for (int l0 = 0; l0 < nrow; l0 += rpi) {
+            const int l = l0 + sub;
+            const bool ok = l < nrow && lane_has;
+            const int lc = min(l, nrow - 1);
+            const int pp = geo.P == 1 ? 0 : lc / t.nh, lh = lc - pp * t.nh;
+            if (geo.P != 1) load_cs<VEC>(tb + (size_t)pp * half, cv, sv);
+            const T *x = reinterpret_cast<const T *>(buf + (size_t)lc * xrow);
             float lo[VEC], hi[VEC];
             load16<T>(x + cc * VEC, lo);
             load16<T>(x + half + cc * VEC, hi);
@@ -322,16 +336,21 @@ k_prologue(const T *__restrict__ q, const T *__restrict__ k, const float *__rest
                 ohi[e] = ylo * sv[e] + yhi * cv[e];
             }
             if (ok) {
-                T *y = obase + (size_t)lh * S * D;
+                T *y = obase + ((size_t)lh * S + pp) * D;
                 store16<T>(y + c * VEC, olo);
                 store16<T>(y + half + c * VEC, ohi);
-                if (c == 0) rbase[lh] = r;
+                if (c == 0) rbase[(size_t)pp * NH + lh] = r;
             }
         }
     };
+    // Warp w takes units w, w + stride, ... With q and k chunks alternating in the
+    // unit order, an even stride would give each warp one kind only, and the warps
+    // with the (smaller) k units would finish early and leave fewer copies in flight
+    // for the rest of the kernel; an odd stride gives every warp both kinds in turn.
     const uint32_t gw = blockIdx.x * kWarps + warp, nw = gridDim.x * kWarps;
-    warp_pipeline<NS>(full, ring, geo.stage_bytes, gw, nw, (uint32_t)geo.units, err, issue,
-                      process);
+    const uint32_t stride = ((geo.nqc + geo.nkc) % 2 == 0 && nw % 2 == 0 && nw > 1) ? nw - 1 : nw;
+    warp_pipeline<NS>(full, ring, geo.stage_bytes, gw < stride ? gw : 0xffffffffu, stride,
+                      (uint32_t)geo.units, err, issue, process);
 }
 
 // ---------------------------------------------------------------- bwd_pre
@@ -357,7 +376,7 @@ k_bwd_pre(const T *__restrict__ out, const T *__restrict__ dout, float *__restri
     const int cc = lane_has ? c : 0;
 
     auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
-        const Unit t = decode_unit(u, geo, H, 0);
+        const Unit t = decode_unit(u, geo, H, 0, S);
         const uint32_t nb = (uint32_t)t.nh * xrow;
         const size_t off = (((size_t)t.b * S + t.s) * H + t.h0) * D;
         if (lane == 0) {
@@ -367,7 +386,7 @@ k_bwd_pre(const T *__restrict__ out, const T *__restrict__ dout, float *__restri
         }
     };
     auto process = [&](uint32_t u, const unsigned char *buf) {
-        const Unit t = decode_unit(u, geo, H, 0);
+        const Unit t = decode_unit(u, geo, H, 0, S);
         float *dbase = dlt + ((size_t)t.b * H + t.h0) * S + t.s;
         for (int lh0 = 0; lh0 < t.nh; lh0 += rpi) {
             const int lh = lh0 + sub;
@@ -440,7 +459,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
     // Stage: x rows [lh], dyhat rows [lh] (one copy per head: dqhat/dkhat are
     // [B, heads, S, D]), rstd [lh], the position's cos/sin row.
     auto issue = [&](uint32_t u, unsigned char *buf, uint64_t *bar) {
-        const Unit t = decode_unit(u, geo, H, G);
+        const Unit t = decode_unit(u, geo, H, G, S);
         const int NH = t.isq ? H : G;
         const size_t bs = (size_t)t.b * S + t.s;
         if (lane < t.nh)
@@ -460,7 +479,7 @@ k_epilogue(const float *__restrict__ dqhat, const float *__restrict__ dkhat,
             bulk_load(buf + geo.y_off + (size_t)lane * yrow, dy + (size_t)lane * S * D, yrow, bar);
     };
     auto process = [&](uint32_t u, const unsigned char *buf) {
-        const Unit t = decode_unit(u, geo, H, G);
+        const Unit t = decode_unit(u, geo, H, G, S);
         const int NH = t.isq ? H : G;
         float cv[VEC], sv[VEC];
         load_cs<VEC>(reinterpret_cast<const float2 *>(buf + geo.t_off) + cc * VEC, cv, sv);
@@ -583,7 +602,7 @@ k_dgamma_reduce(const float *__restrict__ part_q, const float *__restrict__ part
 // whose rows fit `row_budget` bytes, at most max(H, G) rounded up to rpi, and
 // at most 32 (one copy per lane).
 UnitGeo make_geo(const Problem &p, int H, int G, size_t x_row, size_t y_row, size_t r_row,
-                 bool table, int rpi, size_t row_budget) {
+                 bool table, int rpi, size_t row_budget, bool group_positions = false) {
     UnitGeo g = {};
     const size_t row = x_row + y_row + r_row;
     const int hmax = H > G ? H : G;
@@ -595,13 +614,22 @@ UnitGeo make_geo(const Problem &p, int H, int G, size_t x_row, size_t y_row, siz
     g.HC = hc;
     g.nqc = (H + hc - 1) / hc;
     g.nkc = G > 0 ? (G + hc - 1) / hc : 0;
-    g.units = p.B * p.S * (g.nqc + g.nkc);
+    // several positions per unit when one chunk holds all heads of each tensor and
+    // a position's rows are small (the unit's copies stay near the row budget)
+    g.P = 1;
+    if (group_positions && g.nqc <= 1 && g.nkc <= 1) {
+        const size_t pos_bytes = (size_t)hc * (x_row + y_row + r_row);   // as the stage is laid out
+        g.P = (int)std::max<size_t>(1, std::min<size_t>(8, row_budget / pos_bytes));
+    }
+    const int SG = (p.S + g.P - 1) / g.P;
+    g.units = p.B * SG * (g.nqc + g.nkc);
     g.fd_chunks = make_fastdiv((uint32_t)(g.nqc + g.nkc));
-    g.fd_S = make_fastdiv((uint32_t)p.S);
-    g.y_off = (int)align16((size_t)hc * x_row);
-    g.r_off = (int)align16(g.y_off + (size_t)hc * y_row);
-    g.t_off = (int)align16(g.r_off + (size_t)hc * r_row);
-    g.stage_bytes = (int)align128(g.t_off + (table ? (size_t)(p.D / 2) * sizeof(float2) : 0));
+    g.fd_S = make_fastdiv((uint32_t)SG);
+    g.y_off = (int)align16((size_t)hc * x_row * g.P);
+    g.r_off = (int)align16(g.y_off + (size_t)hc * y_row * g.P);
+    g.t_off = (int)align16(g.r_off + (size_t)hc * r_row * g.P);
+    g.stage_bytes =
+        (int)align128(g.t_off + (table ? (size_t)g.P * (p.D / 2) * sizeof(float2) : 0));
     return g;
 }
 
@@ -648,7 +676,7 @@ cudaError_t launch_prologue(const Problem &p, const void *q, const void *k, cons
                             float *rstd_q, float *rstd_k, unsigned int *err, cudaStream_t st) {
     const size_t es = p.dtype == 1 ? 2 : 4;
     const UnitGeo geo = make_geo(p, p.H, p.G, (size_t)p.D * es, 0, 0, true,
-                                 rows_per_iter(p.D, p.dtype, true), 4096);
+                                 rows_per_iter(p.D, p.dtype, true), 4096, true);
     const size_t smem = ring_offset<kStagesPro>() + (size_t)kWarps * kStagesPro * geo.stage_bytes;
     const int grid = persistent_grid(geo);
     cudaError_t e;
