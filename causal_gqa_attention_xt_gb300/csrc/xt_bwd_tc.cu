@@ -904,6 +904,448 @@ k_bwd_dkdv_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__
     }
 }
 
+// Work item w of the dK/dV kernel: 128 key rows (key tile j) of (unit, kv head)
+// bg, or with the chunked split one chunk cidx of that tile's iterations; items
+// run longest first (key tile ascending, units and kv heads fastest). T: the
+// item's (head, query tile) iterations starting at t0 (0: nothing to do, a
+// packed sample shorter than the tile). witem: the item's index within its bg.
+struct DkdvItem {
+    int witem, bg, g, j, T, t0, nU;
+    bool split;   // a chunk of a split tile (its partials go to the chunk reduce)
+    SeqSpan sp;
+};
+
+template <bool kSplit>
+__device__ __forceinline__ DkdvItem dkdv_item(int w, int BG, int H, int G, int n_kvt, int chunk,
+                                              const SeqRows &sr) {
+    DkdvItem it;
+    it.witem = w / BG;
+    it.bg = w - it.witem * BG;
+    const int unit = it.bg / G, group = H / G;
+    it.g = it.bg - unit * G;
+    int j = it.witem, cidx = 0, nc = 1;
+    if constexpr (kSplit) {
+        j = 0;
+        cidx = it.witem;
+        for (;;) {
+            nc = dkdv_chunks(group * (n_kvt - j), chunk);
+            if (cidx < nc || j + 1 >= n_kvt) break;
+            cidx -= nc;
+            ++j;
+        }
+    }
+    it.j = j;
+    it.sp = seq_span(sr, unit);
+    const int n_q = (it.sp.len + kTile - 1) / kTile;
+    it.split = kSplit && nc > 1;
+    if (j >= n_q || cidx >= nc) {
+        it.T = 0; it.t0 = 0; it.nU = 0;
+        return it;
+    }
+    it.nU = n_q - j;                                // query tiles at/after the keys, per head
+    it.t0 = it.split ? cidx * chunk : 0;            // this item's iterations [t0, t0 + T)
+    it.T = it.split ? min(chunk, group * it.nU - it.t0) : group * it.nU;
+    return it;
+}
+
+// The persistent form of k_bwd_dkdv_tc (used at D <= 64, where items are short
+// and a CTA's set-up, pipeline fill and epilogue are a large share of each): a
+// grid of one CTA per SM walks the items in snake order (snake_item), barrier
+// phases and half-stage uses counted across items, the next item's own K/V
+// tiles loaded once the last S^T/dP^T MMA of the current one has read the old
+// ones. Same arguments as k_bwd_dkdv_tc plus the item count.
+template <int D, bool kSplit>
+__global__ void __launch_bounds__(kThreadsBwd, 1)
+k_bwd_dkdv_tc_p(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+              const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_do,
+              const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_cs,
+              const float *__restrict__ lse, const float *__restrict__ dlt,
+              float *__restrict__ dkhat, bf16 *__restrict__ dv, float *__restrict__ part,
+              const float *__restrict__ gamma_k, const float *__restrict__ rstd_k,
+              bf16 *__restrict__ dk, float *__restrict__ part_k, const SeqRows sr, int H, int G,
+              int n_kvt, int chunk, int nw, int BG, int n_items, unsigned int *err, int stall) {
+    using C = BwdCfg<D>;
+    constexpr int HS = C::kHStages;
+    constexpr bool kFuse = !kSplit;
+    constexpr int kEpiStages = kFuse ? 3 : 0;       // k rows + two (cos, sin) halves per item
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ BwdBarriers bars;
+    __shared__ EpiScratch escr;
+    uint8_t *smem = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t *sK = smem;
+    uint8_t *sV = smem + C::kTileBytes;
+    uint8_t *sStage = smem + 2 * C::kTileBytes;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int group = H / G;
+    volatile int *abort_flag = &bars.abort_flag;
+
+    if (threadIdx.x == 0) init_bwd_barriers(bars, 1, 2, HS, true);
+    if (warp == kWarpMma) {
+        tmem_alloc(&bars.tmem_base, 512);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    pdl_enter();
+    const uint32_t tmem = bars.tmem_base;
+
+    // Every role walks the same items (snake_item) and skips
+    // the same empty ones. Half stages are used in one sequence across items: an
+    // item's 2T streamed half tiles (x = 2 t + hf: rows [64 hf, 64 hf + 64) of
+    // streamed tile t), then (kFuse) its three epilogue-input stages, which the
+    // softmax threads release after the epilogue. Barrier phases count items
+    // (own_full, acc_done) or streamed tiles (s_full, p_full) across items.
+    if (warp == kWarpTma) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            tma_prefetch_desc(&map_k);
+            tma_prefetch_desc(&map_v);
+            tma_prefetch_desc(&map_q);
+            tma_prefetch_desc(&map_do);
+        }
+        int items = 0, issued = 0;   // items whose own tiles were loaded; half stages used
+        bool ok = true;
+        for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
+            const DkdvItem it = dkdv_item<kSplit>(w, BG, H, G, n_kvt, chunk, sr);
+            if (it.T == 0) continue;
+            const SeqSpan sp = it.sp;
+            const int S = sp.len, T = it.T, g = it.g, j = it.j;
+            // the item's own K and V tiles, once the previous item's S^T/dP^T MMAs
+            // have read the old ones
+            if (lane == 0 && items > 0)
+                ok = mbar_wait(&bars.acc_done, (items - 1) & 1, abort_flag);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (lane == 0) {
+                mbar_expect_tx(&bars.own_full, 2 * C::kTileBytes);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    tma_load_3d(sK + c * C::kBox, &map_k, &bars.own_full, c * C::A::kCols,
+                                sp.start + j * kTile, sp.plane * G + g);
+                    tma_load_4d(sV + c * C::kBox, &map_v, &bars.own_full, c * C::A::kCols, g,
+                                sp.start + j * kTile, sp.plane);
+                }
+            }
+            ++items;
+            for (int x = 0; x < 2 * T + kEpiStages; ++x) {
+                const int xs = issued, hs = xs % HS;
+                if (lane == 0 && xs >= HS)
+                    ok = mbar_wait(&bars.st_empty[hs], ((xs / HS) - 1) & 1, abort_flag);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                uint8_t *base = sStage + hs * C::kHStageBytes;
+                if (x >= 2 * T) {
+                    // the dk epilogue's inputs: the owned k rows (one 128-row tile),
+                    // then their (cos, sin) rows in two 64-row halves (D/32 boxes of 64
+                    // rows x 16 pairs each)
+                    const int e = x - 2 * T;
+                    if (lane == 0) {
+                        if (e == 0) {
+                            mbar_expect_tx(&bars.st_full[hs], C::kTileBytes);
+                            for (int c = 0; c < C::kChunks; ++c)
+                                tma_load_4d(base + c * C::kBox, &map_x, &bars.st_full[hs],
+                                            c * C::A::kCols, g, sp.start + j * kTile, sp.plane);
+                        } else {
+                            mbar_expect_tx(&bars.st_full[hs], (D / 32) * kCsPieceBytes);
+                            for (int c = 0; c < D / 32; ++c)
+                                tma_load_2d(base + c * kCsPieceBytes, &map_cs, &bars.st_full[hs],
+                                            32 * c, sp.start + j * kTile + 64 * (e - 1));
+                        }
+                        mbar_arrive(&bars.st_full[hs]);
+                    }
+                    ++issued;
+                    continue;
+                }
+                const int t = it.t0 + (x >> 1), hf = x & 1;
+                const int rr = t / it.nU, u = j + (t - rr * it.nU);
+                const int h = g * group + rr;
+                const int q0 = u * kTile + 64 * hf;
+                if (lane == 0) {
+                    mbar_expect_tx(&bars.st_full[hs], 2 * C::kHalfBytes);
+                    for (int c = 0; c < C::kChunks; ++c) {
+                        tma_load_3d(base + c * C::kHalfBox, &map_q, &bars.st_full[hs],
+                                    c * C::A::kCols, sp.start + q0, sp.plane * H + h);
+                        tma_load_4d(base + C::kHalfBytes + c * C::kHalfBox, &map_do,
+                                    &bars.st_full[hs], c * C::A::kCols, h, sp.start + q0, sp.plane);
+                    }
+                }
+                // the half's row statistics by 4-byte asynchronous copies that the stage's
+                // barrier waits for (so the producer never stalls on a global load):
+                // column kq at 4 (kq / 2) + kq % 2 (lse) and two words on (Dlt), one
+                // 16-byte word per column pair; rows past the end read as 0
+                float *sl = reinterpret_cast<float *>(base + 2 * C::kHalfBytes);
+                const size_t row0 = ((size_t)sp.plane * H + h) * sr.S + sp.start;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int kq = lane + 32 * e, q = q0 + kq;
+                    const int o = 4 * (kq >> 1) + (kq & 1);
+                    if (q < S) {
+                        cp_async4(sl + o, lse + row0 + q);
+                        cp_async4(sl + o + 2, dlt + row0 + q);
+                    } else {
+                        sl[o] = 0.f;
+                        sl[o + 2] = 0.f;
+                    }
+                }
+                // each lane's copies become one pending arrival of the stage barrier
+                // (registered before lane 0's arrival below, hence the __syncwarp)
+                cp_async_mbar_arrive(&bars.st_full[hs]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars.st_full[hs]);
+                ++issued;
+            }
+        }
+        if (!ok && lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+        if (lane == 0) {
+            // drain: every copy issued by this CTA lands before it exits
+            if (items > 0) mbar_wait(&bars.own_full, (items - 1) & 1, nullptr);
+            for (int x = max(0, issued - HS); x < issued; ++x)
+                mbar_wait(&bars.st_full[x % HS], (x / HS) & 1, nullptr);
+        }
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issuer
+        {
+            // the whole warp runs this loop; one elected lane issues each MMA / commit
+            const uint32_t idesc_s = idesc_bf16_f32(kTile, kTile / 2, 0, 0);
+            const uint32_t idesc_acc = idesc_bf16_f32(kTile, D, 0, 1);
+            using A = typename C::A;
+            const uint64_t dK = smem_desc(smem_u32(sK), 16, A::kSBO, A::kMode);
+            const uint64_t dV = smem_desc(smem_u32(sV), 16, A::kSBO, A::kMode);
+            const uint64_t dQk0 = smem_desc(smem_u32(sStage), 16, A::kSBO, A::kMode);
+            const uint64_t dDOk0 = smem_desc(smem_u32(sStage + C::kHalfBytes), 16, A::kSBO, A::kMode);
+            const uint64_t dQm0 = smem_desc(smem_u32(sStage), C::kHalfBox, A::kSBO, A::kMode);
+            const uint64_t dDOm0 = smem_desc(smem_u32(sStage + C::kHalfBytes), C::kHalfBox, A::kSBO,
+                                             A::kMode);
+            constexpr uint64_t kStep = (uint64_t)C::kHStageBytes >> 4;
+            // S^T = Khat Qhat^T and dP^T = V dO^T for the queries [64h, 64h+64) of a
+            // streamed tile, from half stage xs (its use index) % HS
+            auto issue_sp = [&](int xs, int h) {
+                const uint64_t so = (uint64_t)(xs % HS) * kStep;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss_w(tmem + 64 * h, dK + kmajor_off<D>(kk), dQk0 + so + kmajor_off_half<D>(kk),
+                             idesc_s, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    mma_ss_w(tmem + 128 + 64 * h, dV + kmajor_off<D>(kk),
+                             dDOk0 + so + kmajor_off_half<D>(kk), idesc_s, kk > 0);
+                mma_commit_w(&bars.s_full[h]);
+            };
+            bool ok = !stall ||
+                      __all_sync(0xffffffffu, mbar_wait_for(&bars.stall, 0, abort_flag, kStallLimitNs));
+            int items = 0, xb = 0, tg = 0;   // items, half stages and streamed tiles before this item
+            for (int rnd = 0, w = snake_item(0); ok && w < n_items; w = snake_item(++rnd)) {
+                const DkdvItem it = dkdv_item<kSplit>(w, BG, H, G, n_kvt, chunk, sr);
+                if (it.T == 0) continue;
+                const int T = it.T;
+                ok = mbar_wait_w(&bars.own_full, items & 1, abort_flag) &&
+                     mbar_wait_w(&bars.st_full[xb % HS], (xb / HS) & 1, abort_flag) &&
+                     mbar_wait_w(&bars.st_full[(xb + 1) % HS], ((xb + 1) / HS) & 1,
+                                 abort_flag);   // both halves of tile 0
+                if (!ok) break;
+                tc_fence_after();
+                issue_sp(xb, 0);
+                issue_sp(xb + 1, 1);
+                // Per half h: once its P/dS are in TMEM, accumulate its 4 k-steps of
+                // dV += P^T dO and dKhat += dS^T Qhat, then start S/dP of the same half
+                // of the next tile (in-order execution keeps them behind those reads).
+                // The first accumulating MMA of an item overwrites the accumulators: the
+                // softmax threads read the previous item's out (epilogue) before they
+                // signal this item's first P.
+                for (int t = 0; ok && t < T; ++t) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int xs = xb + 2 * t + h;
+                        const uint64_t so = (uint64_t)(xs % HS) * kStep;
+                        if (!(ok = mbar_wait_w(&bars.p_full[h], (tg + t) & 1, abort_flag))) break;
+                        tc_fence_after();
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {   // dV += P^T dO
+                            const int kk = 4 * h + k4;
+                            mma_ts_w(tmem + 256, tmem + packed_col(kk), dDOm0 + so + mnmajor_off<D>(k4),
+                                     idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4) {   // dKhat += dS^T Qhat
+                            const int kk = 4 * h + k4;
+                            mma_ts_w(tmem + 384, tmem + 128 + packed_col(kk), dQm0 + so + mnmajor_off<D>(k4),
+                                     idesc_acc, (t > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit_w(&bars.st_empty[xs % HS]);   // this half stage may be reloaded
+                        if (t + 1 < T) issue_sp(xs + 2, h);      // operands checked by the softmax warps
+                    }
+                }
+                if (!ok) break;
+                mma_commit_w(&bars.acc_done);   // also frees the own K/V tiles
+                xb += 2 * T + kEpiStages;
+                tg += T;
+                ++items;
+            }
+            if (!ok && lane == 0 && !*abort_flag) raise_error_b(err, abort_flag);
+            mma_commit_w(&bars.drain);
+            mbar_wait_w(&bars.drain, 0, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int wg = warp >> 2, quarter = warp & 3;
+        const int r = quarter * 32 + lane;              // owned key row = TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+        const float sl2 = kLog2e * rsqrtf((float)D);
+        const int hf = wg >> 1;                         // this warpgroup's half of the tile
+        int items = 0, xb = 0, tg = 0;
+        for (int rnd = 0, w = snake_item(0); w < n_items; w = snake_item(++rnd)) {
+            const DkdvItem it = dkdv_item<kSplit>(w, BG, H, G, n_kvt, chunk, sr);
+            float *pk = kFuse ? part_k + ((size_t)it.bg * nw + it.witem) * D : nullptr;   // dgamma_k partial
+            if (it.T == 0) {                            // a packed sample shorter than this tile
+                if constexpr (kFuse)
+                    if (threadIdx.x < D) pk[threadIdx.x] = 0.f;
+                continue;
+            }
+            const SeqSpan sp = it.sp;
+            const int S = sp.len, T = it.T, g = it.g, j = it.j;
+            const int kp = j * kTile + r;               // key position
+            if (kFuse && wg == kSoftmaxWGs - 1) {
+                // for the dk epilogue (read after its first named barrier; the previous
+                // item's epilogue finished reading these before the stop barrier below)
+                escr.rstd[r] = kp < S ? rstd_k[((size_t)sp.plane * sr.S + sp.start + kp) * G + g] : 0.f;
+                if (r < D) escr.gamma[r] = gamma_k[r];
+            }
+            bool ok = true;
+            for (int t = 0; t < T; ++t) {
+                const int x = xb + 2 * t + hf, hs = x % HS;
+                // the half stage first: its row statistics are loaded into registers while
+                // S^T/dP^T are still being computed (their shared-memory loads would
+                // otherwise queue behind the tensor core's operand reads)
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[hs], (x / HS) & 1, abort_flag));
+                if (!ok) break;
+                float4 st4[4];
+                {
+                    // (lse, lse, Dlt, Dlt) of the column pairs 8 k + 2 (lane % 4) of this
+                    // warpgroup's 32 columns
+                    const float4 *sl4 = reinterpret_cast<const float4 *>(
+                        sStage + hs * C::kHStageBytes + 2 * C::kHalfBytes);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) st4[k] = sl4[16 * (wg & 1) + 4 * k + (lane & 3)];
+                }
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.s_full[hf], (tg + t) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                const int u = j + ((it.t0 + t) % it.nU);
+                const int c0 = wg * kWgCols;                // this warpgroup's columns
+                const int q0 = u * kTile + c0;
+                const uint32_t tS = tmem + lane_off + c0;         // S^T columns
+                const uint32_t tP = tmem + lane_off + 128 + c0;   // dP^T columns
+                // no masking when every query of these columns is at/after every owned key and < S
+                const bool interior = (q0 >= j * kTile + kTile - 1) && (q0 + kWgCols <= S);
+                // 16-lane TMEM shapes (xt_tc.cuh): this thread holds rows
+                // 16 L + lane/4 + 8 jh of its warp's 32 and the column pairs 8 k + 2 (lane % 4)
+                // of the warpgroup's 32, so it needs the statistics of 8 columns only (st4).
+                uint32_t pp[kWgCols / 2], dd[kWgCols / 2];
+                {
+                    uint32_t sv[32], dpv[32];
+                    tmem_ld16x256b_x4_rows32_pair_sync(tS, sv, tP, dpv);
+                    const int cp = 2 * (lane & 3);
+                    // masked columns (the diagonal tile, the ragged end) take the select;
+                    // interior tiles (all but about one in n_q) run without it
+                    auto body = [&](auto masked) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 nl = fmul2(make_float2(st4[k].x, st4[k].y),
+                                                    make_float2(-kLog2e, -kLog2e));
+                            const float2 ndl = make_float2(-st4[k].z, -st4[k].w);
+#pragma unroll
+                            for (int L = 0; L < 2; ++L) {
+#pragma unroll
+                                for (int jh = 0; jh < 2; ++jh) {
+                                    // column pairs through the packed fp32 pipe (f32x2 FMA / add / mul)
+                                    const int e = 16 * L + 4 * k + 2 * jh;
+                                    const float2 a = ffma2(make_float2(__uint_as_float(sv[e]),
+                                                                       __uint_as_float(sv[e + 1])),
+                                                           make_float2(sl2, sl2), nl);
+                                    float2 p = make_float2(fast_exp2(a.x), fast_exp2(a.y));
+                                    if constexpr (decltype(masked)::value) {
+                                        const int q = q0 + 8 * k + cp;
+                                        const int kr = j * kTile + quarter * 32 + 16 * L + (lane >> 2) + 8 * jh;
+                                        if (!(q >= kr && q < S)) p.x = 0.f;
+                                        if (!(q + 1 >= kr && q + 1 < S)) p.y = 0.f;
+                                    }
+                                    const float2 ds = fmul2(p, fadd2(make_float2(__uint_as_float(dpv[e]),
+                                                                                 __uint_as_float(dpv[e + 1])),
+                                                                     ndl));
+                                    pp[8 * L + 2 * k + jh] = pack_bf16x2(p.x, p.y);
+                                    dd[8 * L + 2 * k + jh] = pack_bf16x2(ds.x, ds.y);
+                                }
+                            }
+                        }
+                    };
+                    if (interior) body(std::false_type{});
+                    else body(std::true_type{});
+                }
+                if (t + 1 < T) {   // operands of this half of tile t+1, issued right behind its dV/dK
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bars.st_full[(x + 2) % HS],
+                                                           ((x + 2) / HS) & 1, abort_flag));
+                    if (!ok) break;
+                }
+                tmem_st16x128b_x4_rows32_pair_sync(tS, pp, tP, dd);
+                tc_fence_before();
+                mbar_arrive(&bars.p_full[hf]);
+            }
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars.acc_done, items & 1, abort_flag));
+                if (ok) {
+                    tc_fence_after();
+                    store_dkdv_acc<D, kSplit>(
+                        wg, tmem + lane_off, kp < S,
+                        dv + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D,
+                        dkhat + (((size_t)sp.plane * G + g) * sr.S + sp.start + kp) * D,
+                        it.split ? part + ((size_t)it.bg * nw + it.witem) * 2 * kTile * D + (size_t)r * D
+                                 : nullptr);
+                }
+            }
+            if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+            if constexpr (kFuse) {
+                // dk and the item's dgamma_k partial from dKhat in TMEM, with the k rows
+                // and their (cos, sin) rows that the producer loaded after the last half
+                const int x0 = xb + 2 * T;
+                if (ok) ok = __all_sync(0xffffffffu,
+                                        mbar_wait(&bars.st_full[x0 % HS], (x0 / HS) & 1, abort_flag) &&
+                                        mbar_wait(&bars.st_full[(x0 + 1) % HS], ((x0 + 1) / HS) & 1,
+                                                  abort_flag) &&
+                                        mbar_wait(&bars.st_full[(x0 + 2) % HS], ((x0 + 2) / HS) & 1,
+                                                  abort_flag));
+                if (!ok && !*abort_flag) raise_error_b(err, abort_flag);
+                const uint8_t *sX = sStage + (x0 % HS) * C::kHStageBytes;
+                const uint8_t *cs_row = sStage + ((x0 + 1 + (r >> 6)) % HS) * C::kHStageBytes +
+                                        (r & 63) * 128;
+                finish_rows_dk<D>(ok, wg, quarter, lane, tmem + 384 + lane_off, sX, cs_row, kp < S,
+                                  escr, dk + (((size_t)sp.plane * sr.S + sp.start + kp) * G + g) * D,
+                                  pk);
+                // every softmax thread is done with the epilogue inputs (finish_rows ends
+                // on a named barrier): their half stages may be refilled
+                if (threadIdx.x == 0) {
+                    mbar_arrive(&bars.st_empty[x0 % HS]);
+                    mbar_arrive(&bars.st_empty[(x0 + 1) % HS]);
+                    mbar_arrive(&bars.st_empty[(x0 + 2) % HS]);
+                }
+            }
+            // stop together (a failed wait here, or one raised by another warp); the
+            // barrier also keeps the next item's P signals (and so its first
+            // accumulating MMAs) behind every thread's reads of the accumulators
+            if (softmax_bar_any(!ok || *abort_flag)) break;
+            xb += 2 * T + kEpiStages;
+            tg += T;
+            ++items;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+
 // Sums the chunk partials of the split key tiles in chunk order: block =
 // (split key tile j, unit x kv head), threads over the tile's rows x D.
 __global__ void __launch_bounds__(256)
@@ -1549,6 +1991,28 @@ cudaError_t launch_dkdv_d(const Problem &p, const BwdMaps &m, const float *lse, 
     cudaError_t e = split ? cudaSuccess : make_epi_maps<D>(p, ek, p.G, 64, mx, mcs);
     if (e != cudaSuccess) return e;
     if (split) mx = mcs = m.k;   // unused by the split kernel
+    // persistent when every item is short (at most kPersistTiles streamed tiles: the
+    // longest item, key tile 0, streams group x n_q) and there are several per SM,
+    // where a CTA's set-up, fill and epilogue would dominate; longer items keep one
+    // CTA each (the persistent form's extra loop state spills at the 96-register limit)
+    if constexpr (D <= 64) {
+        constexpr int kPersistTiles = 8;
+        const int n_q = (p.max_len + kTile - 1) / kTile;
+        if (!split && (p.H / p.G) * n_q <= kPersistTiles && blocks >= 2L * sm_count()) {
+            const long BG = (long)p.units * p.G;
+            const long n_items = blocks;
+            const long grid = std::min<long>(n_items, sm_count());
+            auto pk = k_bwd_dkdv_tc_p<D, false>;
+            e = cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
+            if (e != cudaSuccess) return e;
+            return launch_dependent(pk, dim3((unsigned)grid), dim3(kThreadsBwd), C::kSmemA, st,
+                                    m.k, m.v, m.q, m.dout, mx, mcs, lse, dlt, dkhat, (bf16 *)dv,
+                                    part, ek.gamma, ek.rstd, (bf16 *)ek.out, ek.part,
+                                    SeqRows{p.cu, p.S, p.max_len}, p.H, p.G, pl.n_kvt, pl.chunk,
+                                    pl.nw, (int)BG, (int)n_items, err,
+                                    (int)((test_stall_mask() & STALL_DKDV_TC) != 0));
+        }
+    }
     auto kern = split ? k_bwd_dkdv_tc<D, true> : k_bwd_dkdv_tc<D, false>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemA);
     if (e != cudaSuccess) return e;
