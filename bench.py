@@ -913,14 +913,29 @@ KERNEL_SOURCES = {
 SHARED_DEVICE_SOURCES = ["xt_common.cuh", "xt_tc.cuh"]
 
 
-def source_hash(kernel: str) -> str:
-    """Hash of the CUDA sources of one kernel, to tie stored ncu traffic to the
-    code it measured."""
+def code_text(src: str) -> str:
+    """CUDA source without its comments and blank lines: what source_hash covers,
+    so that comment edits keep stored traffic valid. (// inside a string literal
+    does not occur in these files.)"""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in src.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
+def source_hash(kernel: str, read=None) -> str:
+    """Hash of the code of a kernel's CUDA sources (comments left out), to tie
+    stored ncu traffic to the code it measured. read(name) -> text overrides
+    reading the working tree's files."""
     import hashlib
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel] + SHARED_DEVICE_SOURCES:
-        with open(os.path.join(ROOT, "causal_gqa_attention_xt_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        if read is not None:
+            text = read(name)
+        else:
+            with open(os.path.join(ROOT, "causal_gqa_attention_xt_gb300", "csrc", name)) as f:
+                text = f.read()
+        h.update(code_text(text).encode())
     return h.hexdigest()[:16]
 
 

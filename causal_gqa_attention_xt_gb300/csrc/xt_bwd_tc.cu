@@ -13,11 +13,12 @@
 //    the group's query heads r = 0..group-1 in order, each over the 128-row
 //    query tiles at or after its keys, accumulating dV += P^T dO and
 //    dKhat += dS^T Qhat in TMEM: the group sum happens inside the CTA.
-//  * k_bwd_dq_tc: a CTA owns 128 query rows of one (batch, head) and walks
-//    the 128-row key tiles at or before them, accumulating dQhat += dS Khat;
-//    its epilogue finishes dq (RoPE backward, then RMSNorm backward: Mint
-//    project report 5.4.4 and 5.5.2) and writes the CTA's dgamma_q partial,
-//    so dQhat never leaves TMEM.
+//    k_bwd_dkdv_tc_p is its persistent form for short items at D <= 64.
+//  * k_bwd_dq_tc: a persistent CTA walks (batch, head, 128 query rows) items;
+//    for each it walks the 128-row key tiles at or before the rows,
+//    accumulating dQhat += dS Khat; its epilogue finishes dq (RoPE backward,
+//    then RMSNorm backward: Mint project report 5.4.4 and 5.5.2) and writes the
+//    item's dgamma_q partial, so dQhat never leaves TMEM.
 // Both recompute S from the saved Qhat, Khat and lse.
 //
 // TMEM: S (or S^T) in columns [0,128), dP (or dP^T) in [128,256), the
@@ -40,13 +41,17 @@
 // loaded from the half stage as soon as it lands.
 //
 // dQ pipeline: S = Qhat Khat^T is TS-form (the owned Qhat rows are a
-// TMEM-resident A operand), dP = dO V^T SS-form (the owned dO rows in shared
-// memory); packed dS has its own 64 columns. As soon as every softmax thread
-// holds S(t) in registers, S(t+1) is issued, and dP(t+1) once they hold dP(t),
-// so both run during the softmax of t; dQ(t) follows once dS(t) is in TMEM.
-// K and V tiles come through separate rings (a V tile is released after its dP
-// MMA, a K tile after its dQ MMA). The kernel also computes Dlt = rowsum(dO o
-// O) of its rows and writes it for the dK/dV kernel, which is launched after it.
+// TMEM-resident A operand, TMA'd into the owned-row slot and copied into TMEM
+// by tcgen05.cp from the MMA warp, after which the slot takes the dO rows),
+// dP = dO V^T SS-form (the owned dO rows in shared memory); packed dS has its
+// own 64 columns. As soon as every softmax thread holds S(t) in registers,
+// S(t+1) is issued, and dP(t+1) once they hold dP(t), so both run during the
+// softmax of t; dQ(t) follows once dS(t) is in TMEM. K and V tiles come
+// through separate rings (a V tile is released after its dP MMA, a K tile
+// after its dQ MMA); the next item's Qhat copy, first S and first dP run during
+// the current item's epilogue, whose staged dq tile the producer stores by TMA
+// when it reloads the slot. The kernel also computes Dlt = rowsum(dO o O) of
+// its rows and writes it for the dK/dV kernel, which is launched after it.
 //
 // An mbarrier poll right after tcgen05.commit stalls the issuing thread until
 // earlier MMAs drain, so the TMA-arrival check for the next tile is done by the
