@@ -27,3 +27,18 @@ def test_reference_arm_prints_one_contract_line(mode):
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["config"]["workload"]
+
+
+def test_stored_traffic_hash_ignores_comments_only():
+    """The hash that ties profiles/traffic.json to the kernels' code changes with
+    the code and not with its comments."""
+    sys.path.insert(0, ROOT)
+    import bench
+    files = {name: "int f(int x) {  // one\n    return x + 1; /* two\n lines */\n}\n"
+             for name in bench.KERNEL_SOURCES["fwd_tcgen05_bf16"] + bench.SHARED_DEVICE_SOURCES}
+    h0 = bench.source_hash("fwd_tcgen05_bf16", read=files.__getitem__)
+    commented = {k: v.replace("// one", "// other words") + "// trailing note\n" for k, v in files.items()}
+    assert bench.source_hash("fwd_tcgen05_bf16", read=commented.__getitem__) == h0
+    changed = {k: v.replace("x + 1", "x + 2") for k, v in files.items()}
+    assert bench.source_hash("fwd_tcgen05_bf16", read=changed.__getitem__) != h0
+
